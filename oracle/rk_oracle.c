@@ -1,0 +1,271 @@
+/*
+ * rk_oracle.c -- float64 CPU oracle for deterministic paged-KV attention.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Nothing on the product path may include, link,
+ * load or call this file; only the test suite, the package smoke check and
+ * the benchmark's CPU-baseline leg use it.  It shares no code, header, table
+ * or constant generator with the CUDA path.
+ *
+ * What it computes (the plain definition, step by step, in float64):
+ *
+ *   "WS2 PR7 Fused Attention Backend Alignment", section "Current
+ *   Implementation": the strict control materialises the logical paged K/V
+ *   (block table -> logical token order) before any arithmetic, and the
+ *   output is restored to out [B, Hq, Sq, D] with an attention-domain LSE of
+ *   shape [B, Hq, Sq].
+ *
+ *   Same page, section "FlashInfer RoPE Fusion": pre-RoPE Q and a pre-RoPE K
+ *   cache are rotated with the Llama rotate-half (non-interleaved) rule,
+ *   theta = 1e6, rope_scale = 1.0, rotary_dim = head_dim.
+ *
+ *   "Add FlashInfer RoPE-fused paged attention scaffold" (PR #279), boundary
+ *   table: GQA packing fixed from the head layout, FP32 attention-domain LSE.
+ *
+ * Readings where the pages are silent (each also listed in the design notes):
+ *   - softmax scale: 1/sqrt(D) unless the caller passes another one;
+ *   - LSE: natural log of the sum of exp of the *scaled* scores;
+ *   - key t of row b sits at logical position t and is visible to a query at
+ *     position p iff t <= p and t < kv_len[b];
+ *   - query head h reads KV head h / (Hq / Hkv);
+ *   - rotation angle of pair i at position p: p * theta^(-2i/D) / rope_scale;
+ *   - a query with no visible key gets out = 0 and lse = -inf.
+ *
+ * The arithmetic for one output is exactly the definition: gather, convert
+ * to float64, rotate, score every visible key, subtract the maximum, sum the
+ * exponentials in ascending key order, divide.  Queries are distributed over
+ * OpenMP threads; that changes nothing inside any one output.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+#define ORACLE_OK 0
+#define ORACLE_E_ARG 1
+#define ORACLE_E_PAGE 2
+#define ORACLE_E_NOMEM 3
+
+/* Input element types accepted for q / k_cache / v_cache. */
+#define ORACLE_F64 0
+#define ORACLE_BF16 1 /* raw bfloat16 bit patterns (uint16) */
+
+static double to_f64(const void *base, int64_t idx, int dtype) {
+    if (dtype == ORACLE_BF16) {
+        uint32_t bits = ((uint32_t)((const uint16_t *)base)[idx]) << 16;
+        float f;
+        memcpy(&f, &bits, sizeof f);
+        return (double)f; /* exact: every bfloat16 is a float32 */
+    }
+    return ((const double *)base)[idx];
+}
+
+/* Inverse frequency of rotation pair i:  theta^(-2i/D). */
+static double inv_freq(int i, int D, double theta) {
+    return pow(theta, -2.0 * (double)i / (double)D);
+}
+
+/*
+ * Rotate-half RoPE of one D-vector x at position pos (float64 in and out).
+ * For i < D/2:  y[i]       = x[i] cos(a_i) - x[i + D/2] sin(a_i)
+ *               y[i + D/2] = x[i + D/2] cos(a_i) + x[i] sin(a_i)
+ * with a_i = pos * theta^(-2i/D) / rope_scale.
+ */
+void rk_oracle_rope(const double *x, int D, double pos, double theta,
+                    double rope_scale, double *y) {
+    int half = D / 2;
+    for (int i = 0; i < half; ++i) {
+        double a = pos * inv_freq(i, D, theta) / rope_scale;
+        double c = cos(a), s = sin(a);
+        double lo = x[i], hi = x[i + half];
+        y[i] = lo * c - hi * s;
+        y[i + half] = hi * c + lo * s;
+    }
+}
+
+/*
+ * Materialise the logical cache of one row: dst[h][t][d] = cache[page][slot][h][d]
+ * with page = block_table[b, t / page_size], slot = t % page_size, for
+ * t < kv_len[b].  Returns ORACLE_E_PAGE if a needed page id is outside
+ * [0, num_pages).
+ */
+int rk_oracle_materialize_row(const void *cache, int dtype, int num_pages,
+                              int page_size, int Hkv, int D,
+                              const int32_t *block_table, int W,
+                              const int32_t *kv_lens, int b, double *dst) {
+    int n = kv_lens[b];
+    if (n < 0 || n > W * page_size) return ORACLE_E_ARG;
+    for (int t = 0; t < n; ++t) {
+        int page = block_table[(int64_t)b * W + t / page_size];
+        int slot = t % page_size;
+        if (page < 0 || page >= num_pages) return ORACLE_E_PAGE;
+        for (int h = 0; h < Hkv; ++h) {
+            int64_t src = (((int64_t)page * page_size + slot) * Hkv + h) * D;
+            double *out = dst + ((int64_t)h * n + t) * D;
+            for (int d = 0; d < D; ++d) out[d] = to_f64(cache, src + d, dtype);
+        }
+    }
+    return ORACLE_OK;
+}
+
+/* One unit of work: row b, KV head kh, queries s in [s0, s1). */
+typedef struct {
+    int b, kh, s0, s1;
+} task_t;
+
+/*
+ * Paged causal attention with fused RoPE, float64.
+ *
+ *   q            [B, Hq, Sq, D]      (dtype qkv_dtype)
+ *   k_cache      [num_pages, page_size, Hkv, D]
+ *   v_cache      [num_pages, page_size, Hkv, D]
+ *   block_table  [B, W] int32
+ *   kv_lens      [B] int32
+ *   position_ids [B, Sq] int32
+ *   out          [B, Hq, Sq, D] float64
+ *   lse          [B, Hq, Sq] float64
+ *
+ * row_mask: optional [B, Sq] uint8; when non-NULL only queries with a
+ * non-zero entry are computed (the others are left untouched).
+ */
+int rk_oracle_attention(int B, int Sq, int Hq, int Hkv, int D, int page_size,
+                        int num_pages, int W, const void *q,
+                        const void *k_cache, const void *v_cache,
+                        int qkv_dtype, const int32_t *block_table,
+                        const int32_t *kv_lens, const int32_t *position_ids,
+                        double rope_theta, double rope_scale, double sm_scale,
+                        const uint8_t *row_mask, double *out, double *lse,
+                        int nthreads) {
+    if (B < 0 || Sq < 0 || Hq <= 0 || Hkv <= 0 || D <= 0 || (D % 2) ||
+        page_size <= 0 || W < 0 || Hq % Hkv)
+        return ORACLE_E_ARG;
+    const int G = Hq / Hkv;
+    const int CHUNK = 64;
+    int nchunks = (Sq + CHUNK - 1) / CHUNK;
+    int64_t ntask = (int64_t)B * Hkv * nchunks;
+    task_t *tasks = (task_t *)malloc(sizeof(task_t) * (size_t)(ntask > 0 ? ntask : 1));
+    if (!tasks) return ORACLE_E_NOMEM;
+    int64_t k = 0;
+    for (int b = 0; b < B; ++b)
+        for (int kh = 0; kh < Hkv; ++kh)
+            for (int c = 0; c < nchunks; ++c) {
+                tasks[k].b = b;
+                tasks[k].kh = kh;
+                tasks[k].s0 = c * CHUNK;
+                tasks[k].s1 = (c + 1) * CHUNK < Sq ? (c + 1) * CHUNK : Sq;
+                ++k;
+            }
+    int err = ORACLE_OK;
+#ifdef _OPENMP
+    if (nthreads > 0) omp_set_num_threads(nthreads);
+#pragma omp parallel for schedule(dynamic, 1)
+#endif
+    for (int64_t ti = 0; ti < ntask; ++ti) {
+        const task_t tk = tasks[ti];
+        const int b = tk.b, kh = tk.kh;
+        const int n_kv = kv_lens[b];
+        if (n_kv < 0 || n_kv > W * page_size) {
+#ifdef _OPENMP
+#pragma omp atomic write
+#endif
+            err = ORACLE_E_ARG;
+            continue;
+        }
+        /* Number of keys any query of this chunk may see. */
+        int need = 0;
+        for (int s = tk.s0; s < tk.s1; ++s) {
+            if (row_mask && !row_mask[(int64_t)b * Sq + s]) continue;
+            int p = position_ids[(int64_t)b * Sq + s];
+            int nv = p < 0 ? 0 : (p + 1 < n_kv ? p + 1 : n_kv);
+            if (nv > need) need = nv;
+        }
+        double *kr = (double *)malloc(sizeof(double) * ((size_t)need * D + 1));
+        double *vr = (double *)malloc(sizeof(double) * ((size_t)need * D + 1));
+        double *tmp = (double *)malloc(sizeof(double) * (size_t)D);
+        double *qr = (double *)malloc(sizeof(double) * (size_t)D);
+        double *sc = (double *)malloc(sizeof(double) * ((size_t)need + 1));
+        if (!kr || !vr || !tmp || !qr || !sc) {
+            free(kr); free(vr); free(tmp); free(qr); free(sc);
+#ifdef _OPENMP
+#pragma omp atomic write
+#endif
+            err = ORACLE_E_NOMEM;
+            continue;
+        }
+        /* Step 1: gather logical K/V for t < need; rotate K at position t. */
+        int bad = 0;
+        for (int t = 0; t < need && !bad; ++t) {
+            int page = block_table[(int64_t)b * W + t / page_size];
+            int slot = t % page_size;
+            if (page < 0 || page >= num_pages) { bad = 1; break; }
+            int64_t src = (((int64_t)page * page_size + slot) * Hkv + kh) * D;
+            for (int d = 0; d < D; ++d) {
+                tmp[d] = to_f64(k_cache, src + d, qkv_dtype);
+                vr[(int64_t)t * D + d] = to_f64(v_cache, src + d, qkv_dtype);
+            }
+            rk_oracle_rope(tmp, D, (double)t, rope_theta, rope_scale,
+                           kr + (int64_t)t * D);
+        }
+        if (bad) {
+            free(kr); free(vr); free(tmp); free(qr); free(sc);
+#ifdef _OPENMP
+#pragma omp atomic write
+#endif
+            err = ORACLE_E_PAGE;
+            continue;
+        }
+        /* Step 2: every query head of this KV head's group, every query. */
+        for (int g = 0; g < G; ++g) {
+            const int h = kh * G + g;
+            for (int s = tk.s0; s < tk.s1; ++s) {
+                if (row_mask && !row_mask[(int64_t)b * Sq + s]) continue;
+                const int p = position_ids[(int64_t)b * Sq + s];
+                const int nv = p < 0 ? 0 : (p + 1 < n_kv ? p + 1 : n_kv);
+                const int64_t qoff = (((int64_t)b * Hq + h) * Sq + s) * D;
+                double *o = out + qoff;
+                double *l = lse + ((int64_t)b * Hq + h) * Sq + s;
+                if (nv == 0) {
+                    for (int d = 0; d < D; ++d) o[d] = 0.0;
+                    *l = -INFINITY;
+                    continue;
+                }
+                for (int d = 0; d < D; ++d) tmp[d] = to_f64(q, qoff + d, qkv_dtype);
+                rk_oracle_rope(tmp, D, (double)p, rope_theta, rope_scale, qr);
+                double m = -INFINITY;
+                for (int t = 0; t < nv; ++t) {
+                    double acc = 0.0;
+                    const double *kt = kr + (int64_t)t * D;
+                    for (int d = 0; d < D; ++d) acc += qr[d] * kt[d];
+                    sc[t] = acc * sm_scale;
+                    if (sc[t] > m) m = sc[t];
+                }
+                double sum = 0.0;
+                for (int t = 0; t < nv; ++t) {
+                    sc[t] = exp(sc[t] - m);
+                    sum += sc[t];
+                }
+                for (int d = 0; d < D; ++d) o[d] = 0.0;
+                for (int t = 0; t < nv; ++t) {
+                    const double w = sc[t] / sum;
+                    const double *vt = vr + (int64_t)t * D;
+                    for (int d = 0; d < D; ++d) o[d] += w * vt[d];
+                }
+                *l = m + log(sum);
+            }
+        }
+        free(kr); free(vr); free(tmp); free(qr); free(sc);
+    }
+    free(tasks);
+    return err;
+}
+
+/* Threads OpenMP will use for a parallel region (1 without OpenMP). */
+int rk_oracle_max_threads(void) {
+#ifdef _OPENMP
+    return omp_get_max_threads();
+#else
+    return 1;
+#endif
+}
