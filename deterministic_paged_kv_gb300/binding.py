@@ -1,0 +1,204 @@
+"""ctypes binding of librk_paged.so (argument marshalling only).
+
+Every step of the attention runs in the library's CUDA kernels; this module
+only turns torch tensors into device pointers and the current CUDA stream
+into a ``cudaStream_t``, and raises ``RkError`` on a non-zero status.  It
+never computes a result itself and has no fallback: if the library is
+missing, every call raises.
+
+Names mirror the C ABI in ``include/rk_paged.h``:
+``plan`` (rk_paged_plan), ``attn_decode`` (rk_paged_attn_decode),
+``attn_prefill`` (rk_paged_attn_prefill), ``last_error``, ``policy``,
+``abi_version``.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "librk_paged.so")
+
+RK_OK = 0
+ERRORS = {
+    1: "RK_E_ARG", 2: "RK_E_UNSUPPORTED", 3: "RK_E_PAGE_OOB", 4: "RK_E_DUP_PAGE",
+    5: "RK_E_PAD", 6: "RK_E_KVLEN", 7: "RK_E_POSITION", 8: "RK_E_CUDA", 9: "RK_E_DEVICE",
+}
+CODES = {v: k for k, v in ERRORS.items()}
+STATUS_PAGE_OOB, STATUS_KVLEN, STATUS_POSITION, STATUS_TIMEOUT = 1, 2, 4, 8
+ABI_VERSION = 1
+
+
+class RkError(RuntimeError):
+    def __init__(self, code: int, msg: str):
+        super().__init__("%s (%d): %s" % (ERRORS.get(code, "?"), code, msg))
+        self.code = code
+        self.name = ERRORS.get(code, "?")
+        self.msg = msg
+
+
+class Plan(ctypes.Structure):
+    """Mirror of rk_paged_plan_t."""
+    _fields_ = [
+        ("abi", ctypes.c_uint32),
+        ("B", ctypes.c_int32), ("Sq", ctypes.c_int32), ("Hq", ctypes.c_int32),
+        ("Hkv", ctypes.c_int32), ("D", ctypes.c_int32), ("page_size", ctypes.c_int32),
+        ("W", ctypes.c_int32), ("num_pages", ctypes.c_int32),
+        ("causal", ctypes.c_int32), ("max_kv_len", ctypes.c_int32),
+        ("sm_scale", ctypes.c_float), ("validated", ctypes.c_int32),
+        ("rope_theta", ctypes.c_double), ("rope_scale", ctypes.c_double),
+        ("rope_turns", ctypes.c_uint64 * 64),
+    ]
+
+
+_lock = threading.Lock()
+_lib = None
+
+
+def load(path: str | None = None):
+    """Load the library (once).  Raises if it is missing: there is no fallback."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        p = path or LIB_PATH
+        if not os.path.exists(p):
+            raise RuntimeError("librk_paged.so not found at %s; build it with "
+                               "`python -c 'import __graft_entry__ as g; g.build()'`" % p)
+        lib = ctypes.CDLL(p)
+        vp, i32p = ctypes.c_void_p, ctypes.c_void_p
+        lib.rk_paged_plan.restype = ctypes.c_int
+        lib.rk_paged_plan.argtypes = [ctypes.POINTER(Plan)] + [ctypes.c_int32] * 8 + \
+            [i32p, i32p, i32p, ctypes.c_double, ctypes.c_double]
+        for name in ("rk_paged_attn_decode", "rk_paged_attn_prefill"):
+            f = getattr(lib, name)
+            f.restype = ctypes.c_int
+            f.argtypes = [ctypes.POINTER(Plan)] + [vp] * 10
+        lib.rk_last_error.restype = ctypes.c_char_p
+        lib.rk_last_error.argtypes = []
+        lib.rk_paged_policy.restype = ctypes.c_char_p
+        lib.rk_paged_policy.argtypes = []
+        lib.rk_paged_abi_version.restype = ctypes.c_uint32
+        lib.rk_paged_abi_version.argtypes = []
+        if lib.rk_paged_abi_version() != ABI_VERSION:
+            raise RuntimeError("librk_paged.so ABI %d != binding ABI %d"
+                               % (lib.rk_paged_abi_version(), ABI_VERSION))
+        _lib = lib
+        return lib
+
+
+def last_error() -> str:
+    return load().rk_last_error().decode()
+
+
+def policy() -> str:
+    return load().rk_paged_policy().decode()
+
+
+def abi_version() -> int:
+    return int(load().rk_paged_abi_version())
+
+
+def _check(rc: int):
+    if rc != RK_OK:
+        raise RkError(rc, last_error())
+
+
+def _host_i32(t):
+    """(keep-alive object, pointer) of a host int32 array (torch or numpy)."""
+    if t is None:
+        return None, None
+    import numpy as np
+    try:
+        import torch
+        if isinstance(t, torch.Tensor):
+            t = t.detach().to("cpu", torch.int32).contiguous().numpy()
+    except ImportError:  # pragma: no cover
+        pass
+    a = np.ascontiguousarray(t, dtype=np.int32)
+    return a, a.ctypes.data
+
+
+def plan(B, Sq, Hq, Hkv, D, page_size, num_pages, W, block_table=None, kv_lens=None,
+         position_ids=None, rope_theta=1e6, rope_scale=1.0) -> Plan:
+    """rk_paged_plan on HOST metadata (or none, for a shape-only plan)."""
+    lib = load()
+    p = Plan()
+    keep = [_host_i32(x) for x in (block_table, kv_lens, position_ids)]
+    rc = lib.rk_paged_plan(ctypes.byref(p), int(B), int(Sq), int(Hq), int(Hkv), int(D),
+                           int(page_size), int(num_pages), int(W),
+                           keep[0][1], keep[1][1], keep[2][1], float(rope_theta), float(rope_scale))
+    _check(rc)
+    return p
+
+
+def _dptr(t):
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise ValueError("expected a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError("expected a contiguous tensor")
+    return t.data_ptr()
+
+
+def _stream(stream):
+    if stream is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def _launch(fn, p, q, k_cache, v_cache, block_table, kv_lens, position_ids, out, lse, status,
+            stream):
+    import torch
+    for t, dt, name in ((q, torch.bfloat16, "q"), (k_cache, torch.bfloat16, "k_cache"),
+                        (v_cache, torch.bfloat16, "v_cache"), (out, torch.bfloat16, "out"),
+                        (lse, torch.float32, "lse"), (block_table, torch.int32, "block_table"),
+                        (kv_lens, torch.int32, "kv_lens"), (position_ids, torch.int32, "position_ids")):
+        if t.dtype != dt:
+            raise TypeError("%s must be %s (got %s)" % (name, dt, t.dtype))
+    if status is not None and status.dtype != torch.int32:
+        raise TypeError("status must be int32")
+    rc = fn(ctypes.byref(p), _dptr(q), _dptr(k_cache), _dptr(v_cache), _dptr(block_table),
+            _dptr(kv_lens), _dptr(position_ids), _dptr(out), _dptr(lse), _dptr(status),
+            _stream(stream))
+    _check(rc)
+
+
+def attn_decode(p: Plan, q, k_cache, v_cache, block_table, kv_lens, position_ids, out, lse,
+                status=None, stream=None):
+    """rk_paged_attn_decode on device tensors; asynchronous on ``stream``."""
+    _launch(load().rk_paged_attn_decode, p, q, k_cache, v_cache, block_table, kv_lens,
+            position_ids, out, lse, status, stream)
+
+
+def attn_prefill(p: Plan, q, k_cache, v_cache, block_table, kv_lens, position_ids, out, lse,
+                 status=None, stream=None):
+    """rk_paged_attn_prefill on device tensors; asynchronous on ``stream``."""
+    _launch(load().rk_paged_attn_prefill, p, q, k_cache, v_cache, block_table, kv_lens,
+            position_ids, out, lse, status, stream)
+
+
+def run(mode: str, q, k_cache, v_cache, block_table, kv_lens, position_ids, plan_obj=None,
+        rope_theta=1e6, rope_scale=1.0, status=None, stream=None):
+    """Allocate out / lse with torch and launch decode or prefill.
+
+    ``plan_obj`` defaults to a shape-only plan; pass one built from host
+    metadata to have the contents validated first.
+    """
+    import torch
+    B, Hq, Sq, D = q.shape
+    NP, P, Hkv, _ = k_cache.shape
+    if plan_obj is None:
+        plan_obj = plan(B, Sq, Hq, Hkv, D, P, NP, block_table.shape[1],
+                        rope_theta=rope_theta, rope_scale=rope_scale)
+    out = torch.empty_like(q)
+    lse = torch.empty((B, Hq, Sq), dtype=torch.float32, device=q.device)
+    fn = attn_decode if mode == "decode" else attn_prefill
+    fn(plan_obj, q, k_cache, v_cache, block_table, kv_lens, position_ids, out, lse,
+       status=status, stream=stream)
+    return out, lse

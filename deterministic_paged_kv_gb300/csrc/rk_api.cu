@@ -1,0 +1,370 @@
+// rk_api.cu -- the C ABI: host-side validation (rk_paged_plan), tensor-map
+// construction and the two asynchronous launch calls.  No device memory is
+// allocated and no call synchronises or reads device memory on the host.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <atomic>
+#include <climits>
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+#include <string>
+#include <vector>
+
+#include "rk_internal.h"
+#include "rk_paged.h"
+
+namespace rk {
+cudaError_t launch_decode(const CUtensorMap& km, const CUtensorMap& vm, const DecodeArgs& a,
+                          cudaStream_t stream);
+cudaError_t launch_prefill(const CUtensorMap& qm, const CUtensorMap& km, const CUtensorMap& vm,
+                           const PrefillArgs& a, cudaStream_t stream);
+}  // namespace rk
+
+namespace {
+
+thread_local std::string g_err;
+
+int fail(int code, const char* fmt, ...) {
+    char buf[512];
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(buf, sizeof buf, fmt, ap);
+    va_end(ap);
+    g_err = buf;
+    return code;
+}
+
+const double kTwoPi = 6.283185307179586476925286766559;
+
+// -------------------------------------------------------------- plan ----
+
+int check_shape(int32_t B, int32_t Sq, int32_t Hq, int32_t Hkv, int32_t D, int32_t page_size,
+                int32_t num_pages, int32_t W, double theta, double scale) {
+    if (B < 0 || Sq < 1 || Hq < 1 || Hkv < 1 || W < 0 || num_pages < 0)
+        return fail(RK_E_ARG, "bad sizes: B=%d Sq=%d Hq=%d Hkv=%d W=%d num_pages=%d", B, Sq, Hq, Hkv,
+                    W, num_pages);
+    if (!(theta > 1.0) || !std::isfinite(theta))
+        return fail(RK_E_ARG, "rope_theta must be a finite value > 1 (got %g)", theta);
+    if (!(scale > 0.0) || !std::isfinite(scale))
+        return fail(RK_E_ARG, "rope_scale must be a finite value > 0 (got %g)", scale);
+    if (D != rk::HEAD_DIM) return fail(RK_E_UNSUPPORTED, "head_dim %d unsupported (only 128)", D);
+    if (page_size != rk::PAGE)
+        return fail(RK_E_UNSUPPORTED, "page_size %d unsupported (only 16)", page_size);
+    if (Hq % Hkv) return fail(RK_E_UNSUPPORTED, "Hq=%d is not a multiple of Hkv=%d", Hq, Hkv);
+    const int G = Hq / Hkv;
+    if (G != 1 && G != 2 && G != 4 && G != 8)
+        return fail(RK_E_UNSUPPORTED, "GQA group size %d unsupported (1, 2, 4 or 8)", G);
+    if ((int64_t)W * rk::PAGE > INT32_MAX / 2) return fail(RK_E_ARG, "table width %d too large", W);
+    if ((int64_t)num_pages * rk::PAGE > INT32_MAX / 2)
+        return fail(RK_E_ARG, "num_pages %d too large", num_pages);
+    if ((int64_t)B * Hq * Sq > INT32_MAX) return fail(RK_E_ARG, "B * Hq * Sq too large");
+    return RK_OK;
+}
+
+int check_metadata(int32_t B, int32_t Sq, int32_t num_pages, int32_t W, const int32_t* bt,
+                   const int32_t* kv, const int32_t* pos, int32_t* max_kv) {
+    *max_kv = 0;
+    for (int b = 0; b < B; ++b) {
+        const int n = kv[b];
+        if (n < 0 || (int64_t)n > (int64_t)W * rk::PAGE)
+            return fail(RK_E_KVLEN, "row %d: kv_len %d outside [0, %d]", b, n, W * rk::PAGE);
+        if (n > *max_kv) *max_kv = n;
+    }
+    for (int b = 0; b < B; ++b) {
+        const int n = kv[b];
+        const int npg = (n + rk::PAGE - 1) / rk::PAGE;
+        const int32_t* row = bt + (size_t)b * W;
+        for (int j = 0; j < npg; ++j)
+            if (row[j] < 0 || row[j] >= num_pages)
+                return fail(RK_E_PAGE_OOB, "row %d: block_table[%d] = %d outside [0, %d)", b, j,
+                            row[j], num_pages);
+        for (int j = npg; j < W; ++j)
+            if (row[j] != -1)
+                return fail(RK_E_PAD, "row %d: inactive block_table[%d] = %d (must be -1)", b, j,
+                            row[j]);
+    }
+    std::vector<uint8_t> used((size_t)num_pages, 0);
+    for (int b = 0; b < B; ++b) {
+        const int npg = (kv[b] + rk::PAGE - 1) / rk::PAGE;
+        const int32_t* row = bt + (size_t)b * W;
+        for (int j = 0; j < npg; ++j) {
+            if (used[row[j]])
+                return fail(RK_E_DUP_PAGE, "physical page %d appears twice (row %d, entry %d)",
+                            row[j], b, j);
+            used[row[j]] = 1;
+        }
+    }
+    for (int b = 0; b < B; ++b) {
+        const int32_t* p = pos + (size_t)b * Sq;
+        for (int s = 0; s < Sq; ++s) {
+            if (p[s] < 0) return fail(RK_E_POSITION, "row %d: position_ids[%d] = %d < 0", b, s, p[s]);
+            if (s > 0 && p[s] != p[s - 1] + 1)
+                return fail(RK_E_POSITION, "row %d: positions not contiguous ascending at %d", b, s);
+        }
+        const int n = kv[b];
+        const int last = p[Sq - 1];
+        if (n == 0) {
+            if (Sq > 1)
+                return fail(RK_E_POSITION,
+                            "row %d: empty row with %d queries (only decode rows may be empty)", b, Sq);
+        } else if (last != n - 1 && last != n) {
+            return fail(RK_E_POSITION,
+                        "row %d: last query position %d is neither kv_len-1 = %d nor kv_len = %d", b,
+                        last, n - 1, n);
+        }
+    }
+    return RK_OK;
+}
+
+// ----------------------------------------------------------- device -----
+
+std::atomic<uint64_t> g_dev_ok{0}, g_dev_bad{0};
+
+int check_device() {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return fail(RK_E_CUDA, "cudaGetDevice: %s", cudaGetErrorString(e));
+    if (dev < 64) {
+        const uint64_t bit = 1ull << dev;
+        if (g_dev_ok.load() & bit) return RK_OK;
+        if (g_dev_bad.load() & bit)
+            return fail(RK_E_DEVICE, "device %d is not compute capability 10.3 (sm_103)", dev);
+    }
+    int major = 0, minor = 0;
+    e = cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev);
+    if (e != cudaSuccess) return fail(RK_E_CUDA, "cudaDeviceGetAttribute: %s", cudaGetErrorString(e));
+    const bool ok = (major == 10 && minor == 3);
+    if (dev < 64) (ok ? g_dev_ok : g_dev_bad).fetch_or(1ull << dev);
+    if (!ok)
+        return fail(RK_E_DEVICE, "device %d is compute capability %d.%d; this library is built for sm_103a",
+                    dev, major, minor);
+    return RK_OK;
+}
+
+// ------------------------------------------------------- tensor maps ----
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+    static EncodeTiledFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(p);
+    });
+    return fn;
+}
+
+int make_map(CUtensorMap* m, const void* base, int rank, const cuuint64_t* dims,
+             const cuuint64_t* strides_bytes, const cuuint32_t* box, CUtensorMapSwizzle swz,
+             const char* what) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return fail(RK_E_CUDA, "cuTensorMapEncodeTiled unavailable from the driver");
+    cuuint32_t estr[5] = {1, 1, 1, 1, 1};
+    CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, (cuuint32_t)rank, const_cast<void*>(base), dims,
+                    strides_bytes, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swz,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return fail(RK_E_CUDA, "cuTensorMapEncodeTiled(%s) failed: %d", what, (int)r);
+    return RK_OK;
+}
+
+// Page cache [num_pages, 16, Hkv, 128] seen as 3-D (d, head, token row).
+int make_cache_map(CUtensorMap* m, const void* cache, int num_pages, int Hkv, int box_d,
+                   CUtensorMapSwizzle swz, const char* what) {
+    const cuuint64_t dims[3] = {(cuuint64_t)rk::HEAD_DIM, (cuuint64_t)Hkv,
+                                (cuuint64_t)(num_pages > 0 ? num_pages : 1) * rk::PAGE};
+    const cuuint64_t strides[2] = {(cuuint64_t)rk::HEAD_DIM * 2, (cuuint64_t)Hkv * rk::HEAD_DIM * 2};
+    const cuuint32_t box[3] = {(cuuint32_t)box_d, 1, (cuuint32_t)rk::PAGE};
+    return make_map(m, cache, 3, dims, strides, box, swz, what);
+}
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+int check_launch_common(const rk_paged_plan_t* plan, const void* q, const void* kc, const void* vc,
+                        const int32_t* bt, const int32_t* kl, const int32_t* pos, const void* out,
+                        const float* lse) {
+    if (!plan) return fail(RK_E_ARG, "plan is NULL");
+    if (plan->abi != RK_PAGED_ABI_VERSION)
+        return fail(RK_E_ARG, "plan ABI %u does not match library ABI %u (plan not filled by rk_paged_plan?)",
+                    plan->abi, RK_PAGED_ABI_VERSION);
+    int rc = check_shape(plan->B, plan->Sq, plan->Hq, plan->Hkv, plan->D, plan->page_size,
+                         plan->num_pages, plan->W, plan->rope_theta, plan->rope_scale);
+    if (rc) return rc;
+    if (plan->B == 0) return RK_OK;
+    if (!q || !out || !lse || !kl || !pos) return fail(RK_E_ARG, "null device pointer");
+    if (plan->W > 0 && !bt) return fail(RK_E_ARG, "block_table is NULL");
+    if (plan->num_pages > 0 && (!kc || !vc)) return fail(RK_E_ARG, "k_cache / v_cache is NULL");
+    if (!aligned(q, 16) || !aligned(out, 16) || (kc && !aligned(kc, 16)) || (vc && !aligned(vc, 16)))
+        return fail(RK_E_ARG, "q, k_cache, v_cache and out must be 16-byte aligned");
+    if (!aligned(lse, 4) || !aligned(kl, 4) || !aligned(pos, 4) || (bt && !aligned(bt, 4)))
+        return fail(RK_E_ARG, "lse and metadata must be 4-byte aligned");
+    return check_device();
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* rk_last_error(void) { return g_err.c_str(); }
+
+uint32_t rk_paged_abi_version(void) { return RK_PAGED_ABI_VERSION; }
+
+const char* rk_paged_policy(void) {
+    return "split_kv=disabled;acc=fp32;lse=fp32,natural,scaled_scores;softmax_scale=1/sqrt(head_dim);"
+           "downcast=final_write,bf16,rne;order=ascending_kv;rope=llama_rotate_half,fused_q_and_k,"
+           "rotary_dim=head_dim;gqa=contiguous_groups;decode_tile=page16,slots=16,merge=slot_order;"
+           "prefill_tile=q128xkv128,score_mma=bf16(split_bf16_below_pos_1024),pv_mma=bf16;"
+           "batch_invariant=1;page_size=16;head_dim=128";
+}
+
+int rk_paged_plan(rk_paged_plan_t* plan, int32_t B, int32_t Sq, int32_t Hq, int32_t Hkv, int32_t D,
+                  int32_t page_size, int32_t num_pages, int32_t W, const int32_t* block_table_h,
+                  const int32_t* kv_lens_h, const int32_t* position_ids_h, double rope_theta,
+                  double rope_scale) {
+    g_err.clear();
+    if (!plan) return fail(RK_E_ARG, "plan is NULL");
+    std::memset(plan, 0, sizeof *plan);
+    int rc = check_shape(B, Sq, Hq, Hkv, D, page_size, num_pages, W, rope_theta, rope_scale);
+    if (rc) return rc;
+    const bool any = block_table_h || kv_lens_h || position_ids_h;
+    const bool check = kv_lens_h && position_ids_h && (block_table_h || W == 0);
+    if (any && !check)
+        return fail(RK_E_ARG, "pass all three host metadata arrays, or none for a shape-only plan");
+    int32_t max_kv = 0;
+    if (check && B > 0) {
+        static const int32_t kEmpty = -1;
+        rc = check_metadata(B, Sq, num_pages, W, block_table_h ? block_table_h : &kEmpty, kv_lens_h,
+                            position_ids_h, &max_kv);
+        if (rc) return rc;
+    }
+    plan->abi = RK_PAGED_ABI_VERSION;
+    plan->B = B;
+    plan->Sq = Sq;
+    plan->Hq = Hq;
+    plan->Hkv = Hkv;
+    plan->D = D;
+    plan->page_size = page_size;
+    plan->W = W;
+    plan->num_pages = num_pages;
+    plan->causal = 1;
+    plan->max_kv_len = max_kv;
+    plan->sm_scale = (float)(1.0 / std::sqrt((double)D));
+    plan->validated = check ? 1 : 0;
+    plan->rope_theta = rope_theta;
+    plan->rope_scale = rope_scale;
+    for (int i = 0; i < D / 2; ++i) {
+        // Turns per position of pair i: theta^(-2i/D) / (2 pi scale), in [0, 1/(2 pi)].
+        const double w = std::pow(rope_theta, -2.0 * (double)i / (double)D) / (kTwoPi * rope_scale);
+        const double fx = std::ldexp(w, 64);
+        plan->rope_turns[i] = fx >= 18446744073709551615.0 ? ~0ull : (uint64_t)fx;
+    }
+    return RK_OK;
+}
+
+int rk_paged_attn_decode(const rk_paged_plan_t* plan, const void* q, const void* k_cache,
+                         const void* v_cache, const int32_t* block_table_d, const int32_t* kv_lens_d,
+                         const int32_t* position_ids_d, void* out, float* lse, int32_t* status_d,
+                         rk_stream_t stream) {
+    g_err.clear();
+    int rc = check_launch_common(plan, q, k_cache, v_cache, block_table_d, kv_lens_d, position_ids_d,
+                                 out, lse);
+    if (rc) return rc;
+    if (plan->Sq != 1) return fail(RK_E_ARG, "decode needs a plan with Sq == 1 (got %d)", plan->Sq);
+    if (plan->B == 0) return RK_OK;
+    const bool have = plan->num_pages > 0;
+    CUtensorMap km, vm;
+    if ((rc = make_cache_map(&km, have ? k_cache : q, have ? plan->num_pages : 1, have ? plan->Hkv : 1,
+                             rk::HEAD_DIM, CU_TENSOR_MAP_SWIZZLE_NONE, "k_cache")))
+        return rc;
+    if ((rc = make_cache_map(&vm, have ? v_cache : q, have ? plan->num_pages : 1, have ? plan->Hkv : 1,
+                             rk::HEAD_DIM, CU_TENSOR_MAP_SWIZZLE_NONE, "v_cache")))
+        return rc;
+    rk::DecodeArgs a;
+    std::memset(&a, 0, sizeof a);
+    a.q = q;
+    a.block_table = block_table_d;
+    a.kv_lens = kv_lens_d;
+    a.position_ids = position_ids_d;
+    a.out = out;
+    a.lse = lse;
+    a.status = status_d;
+    a.B = plan->B;
+    a.Hq = plan->Hq;
+    a.Hkv = plan->Hkv;
+    a.G = plan->Hq / plan->Hkv;
+    a.W = plan->W;
+    a.num_pages = plan->num_pages;
+    a.qk_scale_log2 = (float)((1.0 / std::sqrt((double)plan->D)) * 1.4426950408889634074);
+    std::memcpy(a.rope_turns, plan->rope_turns, sizeof a.rope_turns);
+    cudaError_t e = rk::launch_decode(km, vm, a, reinterpret_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return fail(RK_E_CUDA, "decode launch: %s", cudaGetErrorString(e));
+    return RK_OK;
+}
+
+int rk_paged_attn_prefill(const rk_paged_plan_t* plan, const void* q, const void* k_cache,
+                          const void* v_cache, const int32_t* block_table_d, const int32_t* kv_lens_d,
+                          const int32_t* position_ids_d, void* out, float* lse, int32_t* status_d,
+                          rk_stream_t stream) {
+    g_err.clear();
+    int rc = check_launch_common(plan, q, k_cache, v_cache, block_table_d, kv_lens_d, position_ids_d,
+                                 out, lse);
+    if (rc) return rc;
+    if (plan->B == 0) return RK_OK;
+    const int G = plan->Hq / plan->Hkv;
+    const int rph = rk::PF_BM / G;
+    // Q [B, Hq, Sq, D] as 4-D (d, position, head, row); box = one 64-column
+    // half of a q-tile: (64, 128/G positions, G heads, 1 row), 128-byte swizzle.
+    CUtensorMap qm, km, vm;
+    {
+        const cuuint64_t dims[4] = {(cuuint64_t)rk::HEAD_DIM, (cuuint64_t)plan->Sq, (cuuint64_t)plan->Hq,
+                                    (cuuint64_t)plan->B};
+        const cuuint64_t strides[3] = {(cuuint64_t)rk::HEAD_DIM * 2,
+                                       (cuuint64_t)plan->Sq * rk::HEAD_DIM * 2,
+                                       (cuuint64_t)plan->Hq * plan->Sq * rk::HEAD_DIM * 2};
+        const cuuint32_t box[4] = {64, (cuuint32_t)rph, (cuuint32_t)G, 1};
+        if ((rc = make_map(&qm, q, 4, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B, "q"))) return rc;
+    }
+    const bool have = plan->num_pages > 0;
+    if ((rc = make_cache_map(&km, have ? k_cache : q, have ? plan->num_pages : 1, have ? plan->Hkv : 1, 64,
+                             CU_TENSOR_MAP_SWIZZLE_128B, "k_cache")))
+        return rc;
+    if ((rc = make_cache_map(&vm, have ? v_cache : q, have ? plan->num_pages : 1, have ? plan->Hkv : 1, 64,
+                             CU_TENSOR_MAP_SWIZZLE_128B, "v_cache")))
+        return rc;
+    rk::PrefillArgs a;
+    std::memset(&a, 0, sizeof a);
+    a.block_table = block_table_d;
+    a.kv_lens = kv_lens_d;
+    a.position_ids = position_ids_d;
+    a.out = out;
+    a.lse = lse;
+    a.status = status_d;
+    a.B = plan->B;
+    a.Sq = plan->Sq;
+    a.Hq = plan->Hq;
+    a.Hkv = plan->Hkv;
+    a.G = G;
+    a.W = plan->W;
+    a.num_pages = plan->num_pages;
+    a.rows_per_head = rph;
+    a.n_qtiles = (plan->Sq + rph - 1) / rph;
+    a.qk_scale_log2 = (float)((1.0 / std::sqrt((double)plan->D)) * 1.4426950408889634074);
+    std::memcpy(a.rope_turns, plan->rope_turns, sizeof a.rope_turns);
+    cudaError_t e = rk::launch_prefill(qm, km, vm, a, reinterpret_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return fail(RK_E_CUDA, "prefill launch: %s", cudaGetErrorString(e));
+    return RK_OK;
+}
+
+}  // extern "C"

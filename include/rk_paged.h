@@ -1,0 +1,181 @@
+/*
+ * rk_paged.h -- C ABI of the deterministic paged-KV attention library
+ * (librk_paged.so, sm_103a).
+ *
+ * Operation (both launch calls): batch-invariant causal attention over a
+ * block-table page cache with Llama rotate-half RoPE applied in-kernel to the
+ * query and to each key as it is read, one fixed ascending-KV reduction per
+ * row (no split-KV), FP32 accumulation, one final BF16 round-to-nearest-even
+ * write of `out`, and the FP32 attention-domain LSE.
+ *   - "WS2 PR7 Fused Attention Backend Alignment", section "Current
+ *     Implementation" (validate page table / positions, then run; restore
+ *     out -> [B, Hq, Sq, D], lse -> [B, Hq, Sq]);
+ *   - same page, "FlashInfer RoPE Fusion" (pre-RoPE Q and K cache, ROPE_LLAMA,
+ *     theta 1e6, scale 1.0, rotary_dim = head_dim, rotate-half);
+ *   - same page, "Split-KV Policy" (policy `disabled`) and "P2P NCCL reference
+ *     and strict arithmetic provenance" (FP32 accumulation, FP32 LSE,
+ *     downcast only at the final output write);
+ *   - "Add FlashInfer RoPE-fused paged attention scaffold", boundary table
+ *     (num_splits = 1, GQA packing from the head layout, FP32 LSE);
+ *   - "flashinfer_fa2 backend for Ada (SM89)", summary and design notes
+ *     (BF16, page size 16, head_dim 128, NHD; plan on host metadata, run on
+ *     device metadata; no host synchronisation in the run call).
+ *
+ * Semantics shared by every entry point:
+ *   q            bf16 [B, Hq, Sq, D], pre-RoPE, contiguous
+ *   k_cache      bf16 [num_pages, page_size, Hkv, D] (NHD), pre-RoPE
+ *   v_cache      bf16 [num_pages, page_size, Hkv, D]
+ *   block_table  int32 [B, W]: logical page j of row b -> physical page;
+ *                entries past ceil(kv_len/page_size) are -1
+ *   kv_lens      int32 [B]: tokens of row b in the cache (logical 0..kv_len-1)
+ *   position_ids int32 [B, Sq]: position of each query
+ *   out          bf16 [B, Hq, Sq, D]
+ *   lse          fp32 [B, Hq, Sq]: ln sum_t exp(score_t), scores scaled by
+ *                sm_scale = 1/sqrt(D)
+ * Key t of row b sits at position t; it is visible to query s iff
+ * t <= position_ids[b, s] and t < kv_len[b].  Query head h reads KV head
+ * h / (Hq/Hkv).  Angle of rotation pair i at position p:
+ * p * theta^(-2i/D) / rope_scale, pairing element i with element i + D/2.
+ * A query with no visible key gets out = 0 and lse = -inf.
+ *
+ * Ownership: the caller owns every buffer and the plan (plain struct).  The
+ * library allocates no device memory and keeps no per-call state; launches
+ * are asynchronous on the caller's stream, never synchronise and never read
+ * device memory on the host, so they can be captured in a CUDA graph and
+ * replayed with new metadata contents.
+ *
+ * Errors: every entry point returns RK_OK (0) or an RK_E_* code and sets a
+ * thread-local message readable with rk_last_error().  Nothing falls back to
+ * another implementation.
+ */
+#ifndef RK_PAGED_H
+#define RK_PAGED_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define RK_PAGED_ABI_VERSION 1u
+#define RK_PAGED_MAX_ROPE_PAIRS 64
+
+/* Status codes returned by the entry points. */
+enum rk_status {
+    RK_OK = 0,
+    RK_E_ARG = 1,          /* bad argument: null/misaligned pointer, negative size, plan mismatch */
+    RK_E_UNSUPPORTED = 2,  /* D != 128, page_size != 16, Hq % Hkv != 0, Hq/Hkv not in {1,2,4,8} */
+    RK_E_PAGE_OOB = 3,     /* an active block-table entry outside [0, num_pages) */
+    RK_E_DUP_PAGE = 4,     /* a physical page used twice among the batch's active entries */
+    RK_E_PAD = 5,          /* an inactive block-table entry that is not -1 */
+    RK_E_KVLEN = 6,        /* kv_len < 0 or kv_len > W * page_size */
+    RK_E_POSITION = 7,     /* positions negative, not contiguous ascending, or not trailing */
+    RK_E_CUDA = 8,         /* a CUDA runtime/driver call failed (message has the CUDA error) */
+    RK_E_DEVICE = 9        /* current device is not a compute capability 10.3 GPU */
+};
+
+/* Bits the kernels OR into *status_d when device-side metadata is unsafe.
+ * The affected row gets out = 0 and lse = NaN; no kernel ever traps. */
+#define RK_STATUS_PAGE_OOB (1 << 0) /* page id read by the kernel outside [0, num_pages) */
+#define RK_STATUS_KVLEN (1 << 1)    /* kv_len outside [0, W * page_size] */
+#define RK_STATUS_POSITION (1 << 2) /* a negative query position */
+#define RK_STATUS_TIMEOUT (1 << 3)  /* an internal pipeline wait gave up (kernel returned early) */
+
+/* Opaque stream handle; identical to cudaStream_t / CUstream. */
+typedef struct CUstream_st *rk_stream_t;
+
+/*
+ * Validated launch plan.  Plain data, owned by the caller, filled by
+ * rk_paged_plan and read by the launch calls.
+ */
+typedef struct rk_paged_plan {
+    uint32_t abi;         /* RK_PAGED_ABI_VERSION */
+    int32_t B, Sq, Hq, Hkv, D, page_size, W, num_pages;
+    int32_t causal;       /* always 1 */
+    int32_t max_kv_len;   /* largest kv_len seen at plan time (0 for a shape-only plan) */
+    float sm_scale;       /* 1 / sqrt(D) */
+    int32_t validated;    /* 1 when metadata contents were checked, 0 for a shape-only plan */
+    double rope_theta, rope_scale;
+    /* Rotation rate of pair i in turns per position as a 0.64 fixed-point
+     * fraction: round(2^64 * theta^(-2i/D) / (2 pi rope_scale)), i < D/2. */
+    uint64_t rope_turns[RK_PAGED_MAX_ROPE_PAIRS];
+} rk_paged_plan_t;
+
+/*
+ * rk_paged_plan -- validate shapes and host metadata, fill *plan.
+ * Follows the validation list of "WS2 PR7 Fused Attention Backend
+ * Alignment", section "Current Implementation" (page bounds, logical order,
+ * duplicate pages, canonical inactive metadata, trailing query positions).
+ *
+ *   block_table_h [B, W], kv_lens_h [B], position_ids_h [B, Sq]: HOST memory,
+ *   read only during the call.  Pass all three as NULL for a shape-only plan
+ *   (contents are then checked only by the kernels' memory-safety checks).
+ * Checks, in this order, returning the first failure:
+ *   RK_E_ARG         plan NULL, B < 0, Sq < 1, Hq/Hkv < 1, W/num_pages < 0,
+ *                    theta <= 1, rope_scale <= 0, only some metadata NULL
+ *   RK_E_UNSUPPORTED D != 128, page_size != 16, Hq % Hkv, Hq/Hkv not in {1,2,4,8}
+ *   RK_E_KVLEN       kv_len outside [0, W * 16]
+ *   RK_E_PAGE_OOB    first ceil(kv_len/16) entries of a row outside [0, num_pages)
+ *   RK_E_PAD         any later entry of the row not -1
+ *   RK_E_DUP_PAGE    a physical page in two active entries (whole batch)
+ *   RK_E_POSITION    a negative position, positions not contiguous ascending,
+ *                    kv_len > 0 with last position not in {kv_len-1, kv_len},
+ *                    kv_len == 0 with Sq > 1
+ * Runs on the host only; needs no GPU.
+ */
+int rk_paged_plan(rk_paged_plan_t *plan, int32_t B, int32_t Sq, int32_t Hq, int32_t Hkv,
+                  int32_t D, int32_t page_size, int32_t num_pages, int32_t W,
+                  const int32_t *block_table_h, const int32_t *kv_lens_h,
+                  const int32_t *position_ids_h, double rope_theta, double rope_scale);
+
+/*
+ * rk_paged_attn_decode -- one query per row (plan->Sq must be 1).
+ * Paged decode of "flashinfer_fa2 backend for Ada (SM89)" with split-KV
+ * disabled ("Split-KV is disabled" design note), RoPE fused as in
+ * "WS2 PR7 ...", "FlashInfer RoPE Fusion".
+ *   q [B, Hq, 1, D], out [B, Hq, 1, D], lse [B, Hq, 1]; all other buffers as
+ *   in the file header.  Every pointer is DEVICE memory of the current
+ *   device; q, k_cache, v_cache, out 16-byte aligned.  status_d: int32 the
+ *   kernel ORs RK_STATUS_* bits into (may be NULL); never cleared here.
+ * Returns RK_E_ARG for a null/misaligned pointer or a plan that is not a
+ * decode plan, RK_E_DEVICE off sm_103, RK_E_CUDA if the launch fails.
+ */
+int rk_paged_attn_decode(const rk_paged_plan_t *plan, const void *q, const void *k_cache,
+                         const void *v_cache, const int32_t *block_table_d,
+                         const int32_t *kv_lens_d, const int32_t *position_ids_d, void *out,
+                         float *lse, int32_t *status_d, rk_stream_t stream);
+
+/*
+ * rk_paged_attn_prefill -- causal chunked prefill against a paged prefix
+ * (any plan->Sq >= 1; queries at position_ids, keys 0..kv_len-1 from the
+ * cache, which already holds the chunk's own K/V).
+ * Paged prefill of "WS2 PR7 ...", "Current Implementation"
+ * (BatchPrefillWithPagedKVCacheWrapper role) with ROPE_LLAMA fused and
+ * split-KV disabled.  Buffers, alignment and errors as for decode.
+ */
+int rk_paged_attn_prefill(const rk_paged_plan_t *plan, const void *q, const void *k_cache,
+                          const void *v_cache, const int32_t *block_table_d,
+                          const int32_t *kv_lens_d, const int32_t *position_ids_d, void *out,
+                          float *lse, int32_t *status_d, rk_stream_t stream);
+
+/* Message of the last failing call on this thread ("" if none).  The
+ * pointer stays valid until the next library call on the same thread. */
+const char *rk_last_error(void);
+
+/*
+ * Fixed arithmetic policy of this library as "key=value;..." text: split-KV,
+ * accumulation and LSE types, LSE base, downcast point and rounding, KV
+ * reduction order, KV tile sizes.  Provenance in the sense of "WS2 PR7 ...",
+ * "P2P NCCL reference and strict arithmetic provenance" (FP32 accumulation,
+ * FP32 LSE, downcast only at the final write).  Static string.
+ */
+const char *rk_paged_policy(void);
+
+/* RK_PAGED_ABI_VERSION of the loaded library. */
+uint32_t rk_paged_abi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* RK_PAGED_H */

@@ -1,0 +1,184 @@
+"""Host-side tests of the C ABI (no GPU needed): the library loads, exports
+every declared symbol, validates metadata with the documented error codes,
+reports the pages' fixed policy and derives its RoPE constants correctly."""
+import json
+import math
+import os
+import re
+import subprocess
+
+import numpy as np
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "rk_paged.h")
+
+
+@pytest.fixture(scope="module")
+def rk():
+    from deterministic_paged_kv_gb300 import build, binding
+    build.build()
+    binding.load()
+    return binding
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(rk_[a-z_0-9]+)\s*\(", text)))
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for n in ["rk_paged_plan", "rk_paged_attn_decode", "rk_paged_attn_prefill",
+              "rk_last_error", "rk_paged_policy", "rk_paged_abi_version"]:
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(rk):
+    out = subprocess.run(["nm", "-D", "--defined-only", rk.LIB_PATH], capture_output=True,
+                         text=True, check=True).stdout
+    exported = set(re.findall(r" T (rk_\w+)", out))
+    missing = [n for n in declared_functions() if n not in exported]
+    assert not missing, missing
+    lib = rk.load()
+    for n in declared_functions():
+        assert hasattr(lib, n)
+
+
+def test_abi_and_policy_match_the_pages(rk):
+    g = json.load(open(os.path.join(ROOT, "tests", "golden", "pages_contract.json")))
+    assert rk.abi_version() == rk.ABI_VERSION
+    pol = dict(kv.split("=", 1) for kv in rk.policy().split(";"))
+    assert pol["split_kv"] == g["split_kv"]["value"]["policy"]
+    assert pol["acc"] == g["arithmetic"]["value"]["accumulation"]
+    assert pol["lse"].startswith(g["arithmetic"]["value"]["lse"])
+    assert pol["downcast"].startswith("final_write")
+    assert pol["order"] != g["unsupported_requests"]["value"]["reduction_order"]
+    assert int(pol["page_size"]) == g["cache"]["value"]["page_size"]
+    assert int(pol["head_dim"]) == g["cache"]["value"]["head_dim"]
+    assert "rotate_half" in pol["rope"]
+
+
+def _ok_case(B=2, Sq=1, W=4, NP=10):
+    bt = np.full((B, W), -1, np.int32)
+    bt[0, :2] = [3, 7]
+    bt[1, :3] = [0, 1, 9]
+    kv = np.array([20, 40], np.int32)
+    pos = np.array([[20], [40]], np.int32) if Sq == 1 else None
+    return bt, kv, pos
+
+
+def _plan(rk, B, Sq, Hq, Hkv, D, P, NP, W, bt, kv, pos, theta=1e6, scale=1.0):
+    return rk.plan(B, Sq, Hq, Hkv, D, P, NP, W, bt, kv, pos, theta, scale)
+
+
+def test_plan_accepts_valid_decode_and_fills_fields(rk):
+    bt, kv, pos = _ok_case()
+    p = _plan(rk, 2, 1, 32, 8, 128, 16, 10, 4, bt, kv, pos)
+    assert p.abi == 1 and p.B == 2 and p.Sq == 1 and p.W == 4 and p.num_pages == 10
+    assert p.causal == 1 and p.max_kv_len == 40 and p.validated == 1
+    assert p.sm_scale == pytest.approx(1 / math.sqrt(128))
+    # also the kv_len-1 convention and a shape-only plan
+    _plan(rk, 2, 1, 32, 8, 128, 16, 10, 4, bt, kv, pos - 1)
+    q = rk.plan(2, 1, 32, 8, 128, 16, 10, 4)
+    assert q.validated == 0
+
+
+def test_plan_rope_turns_match_oracle_frequencies(rk):
+    """The plan's fixed-point rates are the oracle's angular speeds / 2 pi."""
+    import oracle
+    p = rk.plan(1, 1, 32, 8, 128, 16, 1, 1, rope_theta=1e6, rope_scale=1.0)
+    for i in [0, 1, 7, 31, 63]:
+        e = np.zeros(128)
+        e[i] = 1.0
+        y = oracle.rope(e, 1.0)
+        speed = math.atan2(y[i + 64], y[i])
+        assert p.rope_turns[i] / 2.0 ** 64 * 2 * math.pi == pytest.approx(speed, rel=1e-12)
+    p2 = rk.plan(1, 1, 32, 8, 128, 16, 1, 1, rope_theta=1e6, rope_scale=4.0)
+    assert p2.rope_turns[5] == pytest.approx(p.rope_turns[5] / 4, rel=1e-12)
+
+
+@pytest.mark.parametrize("case,code", [
+    ("D", "RK_E_UNSUPPORTED"), ("page", "RK_E_UNSUPPORTED"), ("gqa3", "RK_E_UNSUPPORTED"),
+    ("gqa16", "RK_E_UNSUPPORTED"), ("kvneg", "RK_E_KVLEN"), ("kvbig", "RK_E_KVLEN"),
+    ("oob", "RK_E_PAGE_OOB"), ("neg_page", "RK_E_PAGE_OOB"), ("pad", "RK_E_PAD"),
+    ("dup", "RK_E_DUP_PAGE"), ("dup_cross_row", "RK_E_DUP_PAGE"), ("pos_neg", "RK_E_POSITION"),
+    ("pos_gap", "RK_E_POSITION"), ("pos_not_trailing", "RK_E_POSITION"),
+    ("empty_prefill", "RK_E_POSITION"), ("theta", "RK_E_ARG"), ("scale", "RK_E_ARG"),
+    ("Sq0", "RK_E_ARG"), ("partial_meta", "RK_E_ARG"),
+])
+def test_plan_rejections(rk, case, code):
+    B, Sq, Hq, Hkv, D, P, NP, W = 2, 1, 32, 8, 128, 16, 10, 4
+    bt, kv, pos = _ok_case()
+    theta, scale = 1e6, 1.0
+    if case == "D":
+        D = 64
+    elif case == "page":
+        P = 32
+    elif case == "gqa3":
+        Hq, Hkv = 24, 8
+    elif case == "gqa16":
+        Hq, Hkv = 32, 2
+    elif case == "kvneg":
+        kv[0] = -1
+    elif case == "kvbig":
+        kv[1] = W * 16 + 1
+    elif case == "oob":
+        bt[1, 2] = NP
+    elif case == "neg_page":
+        bt[0, 1] = -1
+    elif case == "pad":
+        bt[0, 3] = 5
+    elif case == "dup":
+        bt[1, 1] = 0
+    elif case == "dup_cross_row":
+        bt[1, 0] = 7
+    elif case == "pos_neg":
+        pos = np.array([[-1], [40]], np.int32)
+    elif case == "pos_gap":
+        Sq = 3
+        pos = np.array([[18, 19, 21], [38, 39, 40]], np.int32)
+    elif case == "pos_not_trailing":
+        pos = np.array([[18], [40]], np.int32)
+    elif case == "empty_prefill":
+        Sq = 2
+        kv[0] = 0
+        bt[0, :] = -1
+        pos = np.array([[0, 1], [39, 40]], np.int32)
+    elif case == "theta":
+        theta = 1.0
+    elif case == "scale":
+        scale = 0.0
+    elif case == "Sq0":
+        Sq = 0
+        pos = np.zeros((2, 1), np.int32)
+    elif case == "partial_meta":
+        pos = None
+    with pytest.raises(rk.RkError) as ei:
+        _plan(rk, B, Sq, Hq, Hkv, D, P, NP, W, bt, kv, pos, theta, scale)
+    assert ei.value.name == code, ei.value
+    assert rk.last_error()  # a message is set
+
+
+def test_plan_allows_empty_decode_rows(rk):
+    bt = np.full((2, 4), -1, np.int32)
+    bt[1, :1] = [2]
+    kv = np.array([0, 5], np.int32)
+    pos = np.array([[0], [5]], np.int32)
+    p = _plan(rk, 2, 1, 32, 8, 128, 16, 4, 4, bt, kv, pos)
+    assert p.max_kv_len == 5
+
+
+def test_launch_without_gpu_fails_closed(rk):
+    """With no device, a launch returns an error instead of computing anything."""
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("GPU present")
+    p = rk.plan(1, 1, 32, 8, 128, 16, 1, 1)
+    lib = rk.load()
+    buf = (ctypes_buf := np.zeros(1 << 16, np.uint8)).ctypes.data  # noqa: F841
+    al = (buf + 255) & ~255
+    import ctypes
+    rc = lib.rk_paged_attn_decode(ctypes.byref(p), al, al, al, al, al, al, al, al, None, None)
+    assert rc in (rk.CODES["RK_E_CUDA"], rk.CODES["RK_E_DEVICE"])
