@@ -42,6 +42,9 @@ struct DecShared {
     float4 step[ROPE_PAIRS / 2];  // (cos, sin) of a 16-position turn, two pairs per entry
     int abort;
 };
+static_assert(sizeof(DecShared) <= DEC_CTRL_BYTES, "decode control block exceeds its reservation");
+static_assert(16 * 4 * HEAD_DIM * 4 + 16 * 4 * 2 * 4 <= DEC_STAGES * DEC_STAGE_BYTES,
+              "merge scratch must fit in the stage ring");
 
 template <int GH>
 __device__ __forceinline__ void write_empty_row(const DecodeArgs& a, int b, int h0, float lse_val) {

@@ -22,7 +22,8 @@ constexpr int DEC_PAGE_BYTES = PAGE * HEAD_DIM * 2;  // one head of one page: 4 
 constexpr int DEC_STAGE_BYTES = 2 * DEC_PAGE_BYTES;  // K + V
 constexpr int DEC_REANCHOR = 16;                     // exact RoPE angles every 16 pages
 constexpr float DEC_RESCALE_THRESHOLD = 8.0f;        // log2-domain max slack
-constexpr int DEC_SMEM_BYTES = DEC_STAGES * DEC_STAGE_BYTES + 1024;
+constexpr int DEC_CTRL_BYTES = 2048;                   // barriers, RoPE tables, flags
+constexpr int DEC_SMEM_BYTES = DEC_STAGES * DEC_STAGE_BYTES + DEC_CTRL_BYTES;
 
 struct DecodeArgs {
     const void* q;                // bf16 [B, Hq, 1, D]
