@@ -1,0 +1,427 @@
+"""Benchmark: paged decode HBM GB/s and chunked paged prefill TFLOP/s.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+One step = one rk_paged_attn_decode call over the decode-throughput workload
+(B=64 rows, kv_len 4096 each, Hq=32/Hkv=8, d=128, page 16, 16384 shuffled
+pages; 1.075 GB of algorithmic traffic, larger than L2, so no flush is needed
+between steps).  The same run also times rk_paged_attn_prefill on the chunked
+prefill workload (B=4, 1536-token prefix + 512-token chunk) with an L2 flush
+between launches, reported in the "prefill" object.
+
+Multi-GPU (torchrun, one rank per GPU): replicas only -- every rank runs its
+own copy of the workload on its own GPU, there is no collective on the data
+path; the barrier and the max-over-ranks of the timed region are the only
+communication.  value = all ranks' bytes / max rank time ("scaling": "weak").
+
+--impl reference times the float64 CPU oracle on the host cores on a bounded
+sample of the same workload (the slow baseline arm).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0
+FALLBACK_BF16_TFLOPS_SUSTAINED = 1700.0
+
+
+# ------------------------------------------------------------ helpers ----
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return (float(d["hbm_gbs"]), float(d["bf16_tflops"]),
+                float(d.get("bf16_tflops_sustained", d["bf16_tflops"])), "measured")
+    return FALLBACK_HBM_GBS, FALLBACK_BF16_TFLOPS, FALLBACK_BF16_TFLOPS_SUSTAINED, "fallback"
+
+
+def decode_alg_bytes(w):
+    """Algorithmic bytes of one decode launch: every visible K and V row once,
+    Q, out, LSE and the metadata the kernel reads."""
+    kv_tokens = int(w.kv_lens.clamp(min=0).sum())
+    return (kv_tokens * w.Hkv * w.D * 2 * 2 + w.q.numel() * 2 * 2 + w.B * w.Hq * w.Sq * 4
+            + w.block_table.numel() * 4 + w.B * 4 * 2)
+
+
+def prefill_alg_flops(w):
+    """4 * D * (visible query-key pairs) * Hq: QK^T and PV over causal-visible pairs."""
+    pos = w.position_ids.long()
+    kv = w.kv_lens.long()[:, None]
+    vis = (pos + 1).clamp(min=0)
+    vis = vis.where(vis < kv, kv)
+    return 4.0 * w.D * float(vis.sum()) * w.Hq
+
+
+def source_hash(*names):
+    h = hashlib.sha256()
+    for n in names:
+        h.update(open(os.path.join(ROOT, "deterministic_paged_kv_gb300", "csrc", n), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def traffic_for(kernel, src_hash):
+    """Per-launch DRAM bytes from the committed ncu summary, if taken on this source."""
+    p = os.path.join(ROOT, "profiles", "ncu_traffic.json")
+    if not os.path.exists(p):
+        return None
+    d = json.load(open(p)).get(kernel)
+    if not d or d.get("source_hash") != src_hash:
+        return None
+    return d.get("dram_bytes_per_launch")
+
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), "--query-gpu=" + self.FIELDS,
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        self.out = ""
+        if self.proc is not None:
+            time.sleep(0.25)
+            self.proc.terminate()
+            try:
+                self.out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                self.out, _ = self.proc.communicate()
+
+    def summary(self):
+        rows = []
+        for line in (self.out or "").strip().splitlines():
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                rows.append((float(parts[1]), float(parts[2]), parts[5:9]))
+            except ValueError:
+                continue
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for _, _, r in rows for i in range(4) if r[i].lower() == "active"})
+        return {"sm_mhz": statistics.median(r[0] for r in rows), "sm_max_mhz": max(r[1] for r in rows),
+                "reasons": reasons, "samples": len(rows)}
+
+
+# -------------------------------------------------------- CPU oracle -----
+
+def cpu_baseline_decode(w, budget_s=15.0):
+    """Time the float64 oracle on whole rows of the decode workload until about
+    budget_s of CPU work; return GB/s of algorithmic bytes and what was run."""
+    import numpy as np
+
+    import oracle
+    oracle.build()
+    B = w.B
+    done, t_total = 0, 0.0
+    order = list(range(B))
+    while done < B and t_total < budget_s:
+        mask = np.zeros((B, 1), np.uint8)
+        mask[order[done]] = 1
+        t0 = time.perf_counter()
+        oracle.attention(w.q, w.k_cache, w.v_cache, w.block_table, w.kv_lens, w.position_ids,
+                         w.rope_theta, w.rope_scale, row_mask=mask)
+        t_total += time.perf_counter() - t0
+        done += 1
+    kv_tokens = int(w.kv_lens[:done].sum())
+    sample_bytes = kv_tokens * w.Hkv * w.D * 2 * 2 + done * w.Hq * w.D * 2 * 2 + done * w.Hq * 4
+    return {"value": sample_bytes / t_total / 1e9, "unit": "GB/s", "cores": oracle.max_threads(),
+            "kind": "oracle",
+            "sample": "%d of %d rows (all 32 heads, kv_len 4096 each), %.1f s of float64 oracle"
+                      % (done, B, t_total)}
+
+
+def run_reference(args):
+    """--impl reference: the oracle arm (host cores), same metric and config."""
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return 0
+    import numpy as np
+
+    import oracle
+    from deterministic_paged_kv_gb300 import workloads
+    oracle.build()
+    w = workloads.decode_throughput()
+    B = w.B
+    times, nbytes = [], []
+    for step in range(args.warmup + args.steps):
+        row = step % B
+        mask = np.zeros((B, 1), np.uint8)
+        mask[row] = 1
+        t0 = time.perf_counter()
+        oracle.attention(w.q, w.k_cache, w.v_cache, w.block_table, w.kv_lens, w.position_ids,
+                         w.rope_theta, w.rope_scale, row_mask=mask)
+        dt = time.perf_counter() - t0
+        if step >= args.warmup:
+            times.append(dt)
+            nbytes.append(int(w.kv_lens[row]) * w.Hkv * w.D * 4 + w.Hq * w.D * 4 + w.Hq * 4)
+    total = sum(times)
+    value = sum(nbytes) / total / 1e9
+    cores = oracle.max_threads()
+    line = {
+        "impl": "reference", "metric": "paged decode HBM GB/s", "value": value, "unit": "GB/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1e3 * total / len(times), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": w.name + " page=16", "sample_per_step": "one row (32 query heads)"},
+        "cpu_baseline": {"value": value, "unit": "GB/s", "cores": cores, "kind": "oracle",
+                         "sample": "one row of 64 per step, %d steps" % len(times)},
+        "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line))
+    return 0
+
+
+# -------------------------------------------------------------- ours -----
+
+def time_launches(fn, n, stream, flush=None):
+    """Per-launch CUDA-event durations (ms) on `stream`."""
+    import torch
+    out = []
+    for _ in range(n):
+        if flush is not None:
+            flush.zero_()
+        s = torch.cuda.Event(enable_timing=True)
+        e = torch.cuda.Event(enable_timing=True)
+        s.record(stream)
+        fn()
+        e.record(stream)
+        e.synchronize()
+        out.append(s.elapsed_time(e))
+    return out
+
+
+def measure_prefill(args, dev, stream, world, tf_burst, peak_kind):
+    """Time rk_paged_attn_prefill on the chunked-prefill workload (L2 flushed
+    between launches) and return the "prefill" object."""
+    import torch
+
+    from deterministic_paged_kv_gb300 import binding, workloads
+    names = ("q", "k_cache", "v_cache", "block_table", "kv_lens", "position_ids")
+    wp = workloads.prefill_chunk()
+    dp = {k: getattr(wp, k).to(dev) for k in names}
+    pp = binding.plan(wp.B, wp.Sq, wp.Hq, wp.Hkv, wp.D, 16, wp.num_pages, wp.W, wp.block_table,
+                      wp.kv_lens, wp.position_ids, wp.rope_theta, wp.rope_scale)
+    pout = torch.empty_like(dp["q"])
+    plse = torch.empty((wp.B, wp.Hq, wp.Sq), dtype=torch.float32, device=dev)
+
+    def pstep():
+        binding.attn_prefill(pp, dp["q"], dp["k_cache"], dp["v_cache"], dp["block_table"],
+                             dp["kv_lens"], dp["position_ids"], pout, plse, stream=stream)
+
+    for _ in range(max(3, args.warmup)):
+        pstep()
+    torch.cuda.synchronize()
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)  # > 129 MB L2
+    pl = time_launches(pstep, max(10, args.steps), stream, flush=flush)
+    p_ms = sum(pl) / len(pl)
+    pflops = prefill_alg_flops(wp)
+    pf_hash = source_hash("prefill.cu", "rk_device.cuh", "rk_internal.h")
+    prefill = {
+        "metric": "paged prefill TFLOP/s", "value": world * pflops / (p_ms * 1e-3) / 1e12,
+        "unit": "TFLOP/s", "ms_per_launch": p_ms, "launches": len(pl),
+        "config": {"workload": wp.name + " page=16", "l2": "flushed (256 MB write) between launches",
+                   "flops": "4*D*visible_pairs*Hq = %.4g" % pflops},
+        "roofline": {"bound": "tensor", "achieved": pflops / (p_ms * 1e-3) / 1e12, "peak": tf_burst,
+                     "unit": "TFLOP/s", "traffic": traffic_for("prefill_kernel", pf_hash),
+                     "kernel": "prefill_kernel", "peak_kind": peak_kind + " (bf16 dense, burst)"},
+    }
+    prefill["roofline"]["frac"] = prefill["roofline"]["achieved"] / tf_burst
+
+    return prefill
+
+
+def run_ours(args):
+    import torch
+    import torch.distributed as dist
+
+    from deterministic_paged_kv_gb300 import binding, workloads
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    dev = torch.device("cuda", local)
+    binding.load()
+    stream = torch.cuda.current_stream(dev)
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+
+    hbm, tf_burst, tf_sust, peak_kind = peaks()
+    names = ("q", "k_cache", "v_cache", "block_table", "kv_lens", "position_ids")
+    if args.prefill_only:
+        pf = measure_prefill(args, dev, stream, world, tf_burst, peak_kind)
+        if rank == 0:
+            print(json.dumps(pf))
+        return 0
+
+    # ---------------- decode: the step ----------------
+    w = workloads.decode_throughput()
+    d = {k: getattr(w, k).to(dev) for k in names}
+    p = binding.plan(w.B, 1, w.Hq, w.Hkv, w.D, 16, w.num_pages, w.W, w.block_table, w.kv_lens,
+                     w.position_ids, w.rope_theta, w.rope_scale)
+    out = torch.empty_like(d["q"])
+    lse = torch.empty((w.B, w.Hq, 1), dtype=torch.float32, device=dev)
+
+    def step():
+        binding.attn_decode(p, d["q"], d["k_cache"], d["v_cache"], d["block_table"], d["kv_lens"],
+                            d["position_ids"], out, lse, stream=stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    step_bytes = decode_alg_bytes(w)
+    clk = ClockSampler(local).__enter__()
+    if True:
+        barrier()
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        ev0 = torch.cuda.Event(enable_timing=True)
+        ev1 = torch.cuda.Event(enable_timing=True)
+        ev0.record(stream)
+        for _ in range(args.steps):
+            step()
+        ev1.record(stream)
+        torch.cuda.synchronize()
+        barrier()
+        wall = time.perf_counter() - t0
+    region_ms = ev0.elapsed_time(ev1)
+    if world > 1:
+        tt = torch.tensor([region_ms], device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        region_ms = float(tt.item())
+    value = world * step_bytes * args.steps / (region_ms * 1e-3) / 1e9
+    per_launch = time_launches(step, max(10, args.steps), stream)
+    avg_launch_ms = sum(per_launch) / len(per_launch)
+    dec_hash = source_hash("decode.cu", "rk_device.cuh", "rk_internal.h")
+    roof = {"bound": "hbm", "achieved": step_bytes / (avg_launch_ms * 1e-3) / 1e9, "peak": hbm,
+            "unit": "GB/s", "traffic": traffic_for("decode_kernel", dec_hash),
+            "kernel": "decode_kernel<4>", "peak_kind": peak_kind + " (copy bandwidth, burst)",
+            "alg_bytes_per_launch": step_bytes}
+    roof["frac"] = roof["achieved"] / roof["peak"]
+
+    # ---------------- e2e: host buffers through the public API ----------------
+    pinned = {k: getattr(w, k).pin_memory() for k in names}
+    h_out = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    h_lse = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
+
+    def e2e_step(with_cache):
+        for k in names:
+            if with_cache or k not in ("k_cache", "v_cache"):
+                d[k].copy_(pinned[k], non_blocking=True)
+        step()
+        h_out.copy_(out, non_blocking=True)
+        h_lse.copy_(lse, non_blocking=True)
+
+    def e2e_measure(with_cache, n):
+        for _ in range(2):
+            e2e_step(with_cache)
+        torch.cuda.synchronize()
+        t = time.perf_counter()
+        for _ in range(n):
+            e2e_step(with_cache)
+        torch.cuda.synchronize()
+        return (time.perf_counter() - t) / n
+
+    n_e2e = max(3, min(args.steps, 10))
+    t_full = e2e_measure(True, n_e2e) if not args.no_e2e else float("nan")
+    t_res = e2e_measure(False, n_e2e) if not args.no_e2e else float("nan")
+    h2d_full = sum(pinned[k].numel() * pinned[k].element_size() for k in names)
+    h2d_res = sum(pinned[k].numel() * pinned[k].element_size() for k in names
+                  if k not in ("k_cache", "v_cache"))
+    d2h = h_out.numel() * 2 + h_lse.numel() * 4
+
+    prefill = None if args.no_prefill else measure_prefill(args, dev, stream, world, tf_burst, peak_kind)
+
+    clk.__exit__(None, None, None)
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline_decode(w, budget_s=args.cpu_budget)
+
+    clocks = clk.summary()
+    if rank == 0:
+        line = {
+            "metric": "paged decode HBM GB/s", "value": value, "unit": "GB/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": region_ms / args.steps,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic",
+            "config": {"workload": w.name + " page=16 (16384 shuffled pages, fused RoPE, FP32 LSE)",
+                       "l2": "inputs larger than L2 (%.3f GB per step)" % (step_bytes / 1e9),
+                       "parallelism": "replicas x%d" % world if world > 1 else "single GPU"},
+            "roofline": roof,
+            "cpu_baseline": cpu,
+            "e2e": {"value": world * step_bytes / t_full / 1e9, "unit": "GB/s",
+                    "h2d_bytes_per_step": h2d_full, "d2h_bytes_per_step": d2h,
+                    "note": "every input incl. the 1 GB K/V cache copied from pinned host memory each step"},
+            "e2e_resident_cache": {"value": world * step_bytes / t_res / 1e9, "unit": "GB/s",
+                                   "h2d_bytes_per_step": h2d_res, "d2h_bytes_per_step": d2h,
+                                   "note": "K/V cache resident in HBM; q and metadata copied each step"},
+            "gpu_launches": args.steps + (0 if prefill is None else 0),
+            "clocks": clocks,
+            "wall_s_timed_region": wall,
+            "prefill": prefill,
+        }
+        if args.no_e2e:
+            line["e2e"] = line["e2e_resident_cache"] = None
+        print(json.dumps(line))
+    if world > 1:
+        dist.destroy_process_group()
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--cpu-budget", type=float, default=15.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-prefill", action="store_true",
+                    help="skip the prefill object (profiling runs of the decode kernel)")
+    ap.add_argument("--prefill-only", action="store_true",
+                    help="time only the prefill workload and print its object (profiling runs)")
+    args = ap.parse_args()
+    if args.warmup < 3 and args.impl == "ours":
+        args.warmup = 3
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

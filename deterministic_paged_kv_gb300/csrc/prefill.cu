@@ -25,10 +25,14 @@
 //               slack of 8 before the running max moves (rescale of the O row
 //               in TMEM only then), P rounded to BF16 into shared memory;
 //               epilogue O / l -> BF16 once, LSE -> FP32.
-// q-tiles whose first position is below PF_PRECISE_POS form the score MMA
-// from split BF16 operands (hi + lo for Q and K: hi*hi + hi*lo + lo*hi) so
-// rows that see few keys still meet an FP32-grade LSE; that choice depends on
-// the logical position only.  Nothing depends on B, W or the grid.
+// Score precision: the rotated Q is kept as two BF16 terms (hi + lo) and the
+// score MMA is Q_hi K^T + Q_lo K^T, so only K's BF16 rounding remains (its
+// error is independent per key and averages out in the LSE; a single BF16 Q
+// rounding shifts every score of a row the same way and does not).  q-tiles
+// whose first position is below PF_PRECISE_POS also split K (adding
+// Q_hi K_lo^T), so rows that see few keys keep an FP32-grade LSE.  Both
+// choices depend on the logical position only.  Nothing depends on B, W or
+// the grid.
 #include <atomic>
 
 #include "rk_device.cuh"
@@ -45,7 +49,7 @@ constexpr float RESCALE_SLACK = 8.0f;
 
 // Shared memory carve (offsets from a 1024-byte aligned base).
 constexpr int OFF_Q = 0;                        // Q hi  [2 blocks][128 rows][128 B]
-constexpr int OFF_QLO = OFF_Q + PF_TILE_BYTES;  // Q lo (precise tiles only)
+constexpr int OFF_QLO = OFF_Q + PF_TILE_BYTES;  // Q lo: rotated Q minus its BF16 rounding
 constexpr int OFF_K = OFF_QLO + PF_TILE_BYTES;  // K stage 0, K stage 1 (= K lo when precise)
 constexpr int OFF_V = OFF_K + 2 * PF_TILE_BYTES;
 constexpr int OFF_P = OFF_V + 2 * PF_TILE_BYTES;
@@ -259,8 +263,8 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
 #pragma unroll
                     for (int e = 0; e < 8; ++e) rope_cos_sin((uint32_t)p, a.rope_turns[8 * u + e], c[e], sn[e]);
                     const uint32_t off = sw_off(r, u);
-                    rotate_chunk(q0 + off, q0 + 16384 + off, c, sn, precise ? sm + OFF_QLO + off : nullptr,
-                                 precise ? sm + OFF_QLO + 16384 + off : nullptr);
+                    rotate_chunk(q0 + off, q0 + 16384 + off, c, sn, sm + OFF_QLO + off,
+                                 sm + OFF_QLO + 16384 + off);
                 }
             }
             fence_proxy_async_smem();
@@ -328,12 +332,12 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
                 const uint32_t kt = s_base + OFF_K + k * PF_TILE_BYTES;
 #pragma unroll 1
                 for (int ks = 0; ks < 8; ++ks) umma_ss(tS, kmajor_desc(q, ks), kmajor_desc(kt, ks), idS, ks > 0);
+#pragma unroll 1
+                for (int ks = 0; ks < 8; ++ks) umma_ss(tS, kmajor_desc(qlo, ks), kmajor_desc(kt, ks), idS, 1);
                 if (precise) {
                     const uint32_t klo = s_base + OFF_K + PF_TILE_BYTES;
 #pragma unroll 1
                     for (int ks = 0; ks < 8; ++ks) umma_ss(tS, kmajor_desc(q, ks), kmajor_desc(klo, ks), idS, 1);
-#pragma unroll 1
-                    for (int ks = 0; ks < 8; ++ks) umma_ss(tS, kmajor_desc(qlo, ks), kmajor_desc(kt, ks), idS, 1);
                 }
                 umma_commit(smem_u32(&bars->s_full));
                 return true;
