@@ -26,7 +26,7 @@ ERRORS = {
     5: "RK_E_PAD", 6: "RK_E_KVLEN", 7: "RK_E_POSITION", 8: "RK_E_CUDA", 9: "RK_E_DEVICE",
 }
 CODES = {v: k for k, v in ERRORS.items()}
-STATUS_PAGE_OOB, STATUS_KVLEN, STATUS_POSITION, STATUS_TIMEOUT = 1, 2, 4, 8
+STATUS_PAGE_OOB, STATUS_KVLEN, STATUS_POSITION, STATUS_TIMEOUT, STATUS_RANGE = 1, 2, 4, 8, 16
 ABI_VERSION = 1
 
 

@@ -225,7 +225,7 @@ const char* rk_paged_policy(void) {
     return "split_kv=disabled;acc=fp32;lse=fp32,natural,scaled_scores;softmax_scale=1/sqrt(head_dim);"
            "downcast=final_write,bf16,rne;order=ascending_kv;rope=llama_rotate_half,fused_q_and_k,"
            "rotary_dim=head_dim;gqa=contiguous_groups;decode_tile=page16,slots=16,merge=slot_order;"
-           "prefill_tile=q128xkv128,score_mma=bf16(q_hi+q_lo;k_hi+k_lo_below_pos_1024),pv_mma=bf16;"
+           "prefill_tile=2xq128xkv128,score_mma=fp16_operands_fp32_acc,pv_mma=bf16_operands_fp32_acc;"
            "batch_invariant=1;page_size=16;head_dim=128";
 }
 

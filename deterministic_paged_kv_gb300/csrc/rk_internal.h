@@ -46,10 +46,6 @@ constexpr int PF_BM = 128;          // accumulator rows per tile
 constexpr int PF_BN = 128;          // KV tokens per tile (8 pages)
 constexpr int PF_PAGES_PER_TILE = PF_BN / PAGE;
 constexpr int PF_TILE_BYTES = PF_BM * HEAD_DIM * 2;  // 32 KiB bf16 operand tile
-// q-tiles whose first position is below this also split K into BF16 hi + lo
-// in the score MMA (Q is always split), so rows with few visible keys keep an
-// FP32-grade LSE.
-constexpr int PF_PRECISE_POS = 1024;
 
 struct PrefillArgs {
     const int32_t* block_table;   // [B, W]

@@ -80,6 +80,7 @@ enum rk_status {
 #define RK_STATUS_KVLEN (1 << 1)    /* kv_len outside [0, W * page_size] */
 #define RK_STATUS_POSITION (1 << 2) /* a negative query position */
 #define RK_STATUS_TIMEOUT (1 << 3)  /* an internal pipeline wait gave up (kernel returned early) */
+#define RK_STATUS_RANGE (1 << 4)    /* prefill: a pre-RoPE q or k element of the tile has |x| >= 2^15 */
 
 /* Opaque stream handle; identical to cudaStream_t / CUstream. */
 typedef struct CUstream_st *rk_stream_t;
@@ -152,6 +153,10 @@ int rk_paged_attn_decode(const rk_paged_plan_t *plan, const void *q, const void 
  * Paged prefill of "WS2 PR7 ...", "Current Implementation"
  * (BatchPrefillWithPagedKVCacheWrapper role) with ROPE_LLAMA fused and
  * split-KV disabled.  Buffers, alignment and errors as for decode.
+ * The score MMA takes the rotated q and k as FP16 (FP32 accumulation), so
+ * pre-RoPE q / k elements must stay below 2^15 in magnitude: a q-tile that
+ * meets a larger value (in its queries or any key it reads) is not computed;
+ * its rows get out = 0, lse = NaN and RK_STATUS_RANGE is set.
  */
 int rk_paged_attn_prefill(const rk_paged_plan_t *plan, const void *q, const void *k_cache,
                           const void *v_cache, const int32_t *block_table_d,

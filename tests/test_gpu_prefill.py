@@ -133,3 +133,28 @@ def test_prefill_deterministic_repeat():
     a = run_gpu(w, validate=False)
     b = run_gpu(w, validate=False)
     assert bitwise_equal(a[0], b[0]) and bitwise_equal(a[1], b[1])
+
+
+def test_prefill_range_guard_flags_instead_of_overflowing():
+    """A pre-RoPE key element of 40000 (beyond the FP16 score-operand range once
+    rotated): that (row, KV head)'s rows are zeroed with NaN LSE and the status
+    bit is set; every other output still matches the oracle."""
+    w = workloads.random_case(2, 8, 32, 8, 128, [60, 90], seed=41, mode="prefill")
+    page = int(w.block_table[1, 0])
+    w.k_cache[page, 3, 0, 5] = 40000.0
+    d = to_dev(w)
+    p = binding.plan(2, 8, 32, 8, 128, 16, w.num_pages, w.W)
+    out = torch.empty_like(d["q"])
+    lse = torch.empty((2, 32, 8), dtype=torch.float32, device="cuda")
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    binding.attn_prefill(p, d["q"], d["k_cache"], d["v_cache"], d["block_table"], d["kv_lens"],
+                         d["position_ids"], out, lse, status=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == binding.STATUS_RANGE
+    assert torch.all(out[1, 0:4] == 0) and torch.all(torch.isnan(lse[1, 0:4]))
+    ro, rl = oracle_ref(w)
+    keep = np.ones((2, 32), bool)
+    keep[1, 0:4] = False
+    o = out.float().cpu().numpy()[keep]
+    l_ = lse.cpu().numpy()[keep]
+    assert np.max(np.abs(o - ro[keep])) <= 2e-2 and np.max(np.abs(l_ - rl[keep])) <= 1e-3
