@@ -42,8 +42,11 @@ namespace rk {
 namespace {
 
 constexpr int PF_THREADS = 512;
-constexpr int WARP_TMA = 12;
+constexpr int WARP_TMA_K = 12;
 constexpr int WARP_MMA = 13;
+constexpr int WARP_TMA_V = 14;
+constexpr int KSTAGES = 3;
+constexpr int VSTAGES = 2;
 constexpr uint32_t TMEM_COLS = 512;  // S0 [0,128) S1 [128,256) O0 [256,384) O1 [384,512)
 constexpr float RESCALE_SLACK = 8.0f;
 constexpr uint32_t RANGE_LIMIT_BF16 = 0x4700u;  // bf16 bit pattern of 2^15
@@ -54,17 +57,18 @@ constexpr int REG_SOFTMAX = 184;
 constexpr int REG_CTRL = 40;
 static_assert(REG_XFORM + 2 * REG_SOFTMAX + REG_CTRL == 4 * 128, "register split must sum to the launch budget");
 
-// Shared memory carve (offsets from a 1024-byte aligned base).
+// Shared memory carve (the dynamic shared memory base is 1024-byte aligned).
 constexpr int OFF_Q = 0;  // Q tile j at OFF_Q + j * 32 KiB
 constexpr int OFF_K = OFF_Q + 2 * PF_TILE_BYTES;
-constexpr int OFF_V = OFF_K + 2 * PF_TILE_BYTES;
-constexpr int OFF_BAR = OFF_V + 2 * PF_TILE_BYTES;
+constexpr int OFF_V = OFF_K + KSTAGES * PF_TILE_BYTES;
+constexpr int OFF_BAR = OFF_V + VSTAGES * PF_TILE_BYTES;
 constexpr int PF_CTRL_BYTES = 2048;
-constexpr int PF_SMEM_BYTES = OFF_BAR + PF_CTRL_BYTES + 1024;  // control block + alignment slack
+constexpr int PF_SMEM_BYTES = OFF_BAR + PF_CTRL_BYTES;
 
 struct PfBars {
     uint64_t q_full, q_ready;
-    uint64_t kv_full[2], kv_ready[2], kv_empty[2];
+    uint64_t k_full[KSTAGES], k_ready[KSTAGES], k_empty[KSTAGES];
+    uint64_t v_full[VSTAGES], v_empty[VSTAGES], v_tail;
     uint64_t s_full[2], p_ready[2], o_done[2];
     uint32_t tmem_base;
     int abort;
@@ -154,11 +158,14 @@ __device__ __forceinline__ void write_rows(const PrefillArgs& a, int b, int kvh,
 __global__ void __launch_bounds__(PF_THREADS, 1)
     prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap kmap,
                    const __grid_constant__ CUtensorMap vmap, const __grid_constant__ PrefillArgs a) {
-    extern __shared__ uint8_t smem_raw[];
-    uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
-                                             ~static_cast<uintptr_t>(1023));
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    uint8_t* sm = smem_raw;
     PfBars* bars = reinterpret_cast<PfBars*>(sm + OFF_BAR);
     const uint32_t s_base = smem_u32(sm);
+    if (s_base & 1023u) {  // the swizzled operand layout needs a 1024-byte aligned base
+        if (threadIdx.x == 0 && a.status) atomicOr(a.status, RK_STATUS_TIMEOUT);
+        return;
+    }
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, wg = warp >> 2;
 
     // ---- work unit: longest q-tile pairs first (later positions see more keys) ----
@@ -190,6 +197,11 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
     const int n_keys = max(ti[0].n_keys, ti[1].n_keys);
     const int n_tiles = max(ti[0].n_tiles, ti[1].n_tiles);
     const int n_pages = (n_keys + PAGE - 1) / PAGE;
+    // The row's last page is in this CTA's last tile and is only partly
+    // filled: its cache rows past kv_len hold arbitrary bits and are zeroed in
+    // V after the copy lands (they meet P = 0, which would not cancel a
+    // non-finite value).
+    const bool has_tail = n_keys == kv_len && (kv_len & (PAGE - 1)) != 0;
     const int32_t* bt = a.block_table + (size_t)b * a.W;
     int oob = 0;
     for (int i = tid; i < n_pages; i += PF_THREADS) {
@@ -201,16 +213,27 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
         bars->range_bad = 0;
         mbar_init(smem_u32(&bars->q_full), 1);
         mbar_init(smem_u32(&bars->q_ready), 128);
-        for (int k = 0; k < 2; ++k) {
-            mbar_init(smem_u32(&bars->kv_full[k]), 1);
-            mbar_init(smem_u32(&bars->kv_ready[k]), 128);
-            mbar_init(smem_u32(&bars->kv_empty[k]), 1);
-            mbar_init(smem_u32(&bars->s_full[k]), 1);
-            mbar_init(smem_u32(&bars->p_ready[k]), 128);
-            mbar_init(smem_u32(&bars->o_done[k]), 1);
+        for (int k = 0; k < KSTAGES; ++k) {
+            mbar_init(smem_u32(&bars->k_full[k]), 1);
+            mbar_init(smem_u32(&bars->k_ready[k]), 128);
+            mbar_init(smem_u32(&bars->k_empty[k]), 1);
+        }
+        for (int k = 0; k < VSTAGES; ++k) {
+            mbar_init(smem_u32(&bars->v_full[k]), 1);
+            mbar_init(smem_u32(&bars->v_empty[k]), 1);
+        }
+        mbar_init(smem_u32(&bars->v_tail), 1);
+        for (int j = 0; j < 2; ++j) {
+            mbar_init(smem_u32(&bars->s_full[j]), 1);
+            mbar_init(smem_u32(&bars->p_ready[j]), 128);
+            mbar_init(smem_u32(&bars->o_done[j]), 1);
         }
         fence_mbar_init();
     }
+    // V stages start as zeros: rows of pages a tile does not load stay finite.
+    for (int i = tid; i < VSTAGES * PF_TILE_BYTES / 16; i += PF_THREADS)
+        reinterpret_cast<uint4*>(sm + OFF_V)[i] = make_uint4(0, 0, 0, 0);
+    fence_proxy_async_smem();
     if (tid < ROPE_PAIRS) {
         bars->turns[tid] = a.rope_turns[tid];
         float c, s;
@@ -239,49 +262,71 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
 
     if (wg == 3) {
         asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(REG_CTRL));
-        if (warp == WARP_TMA) {
-            // ============================================ TMA producer ====
+        if (warp == WARP_TMA_K || warp == WARP_TMA_V) {
+            // ======================================= TMA producers ====
+            // warp 12 loads Q and the K tiles, warp 14 the V tiles; lane p
+            // issues the boxes of page p of a tile.
+            const bool is_k = warp == WARP_TMA_K;
+            const CUtensorMap* map = is_k ? &kmap : &vmap;
             if (lane == 0) {
-                prefetch_tmap(&qmap);
-                prefetch_tmap(&kmap);
-                prefetch_tmap(&vmap);
-                const uint32_t qb = smem_u32(&bars->q_full);
-                mbar_arrive_expect_tx(qb, 2 * PF_TILE_BYTES);
-                for (int j = 0; j < 2; ++j) {
-                    tma_load_4d(s_base + OFF_Q + j * PF_TILE_BYTES, &qmap, qb, 0, ti[j].s0, kvh * a.G, b);
-                    tma_load_4d(s_base + OFF_Q + j * PF_TILE_BYTES + 16384, &qmap, qb, 64, ti[j].s0, kvh * a.G,
-                                b);
+                prefetch_tmap(map);
+                if (is_k) {
+                    prefetch_tmap(&qmap);
+                    const uint32_t qb = smem_u32(&bars->q_full);
+                    mbar_arrive_expect_tx(qb, 2 * PF_TILE_BYTES);
+                    for (int j = 0; j < 2; ++j) {
+                        tma_load_4d(s_base + OFF_Q + j * PF_TILE_BYTES, &qmap, qb, 0, ti[j].s0, kvh * a.G, b);
+                        tma_load_4d(s_base + OFF_Q + j * PF_TILE_BYTES + 16384, &qmap, qb, 64, ti[j].s0,
+                                    kvh * a.G, b);
+                    }
                 }
             }
+            const int nst = is_k ? KSTAGES : VSTAGES;
             int issued = 0;
             for (int i = 0; i < n_tiles; ++i) {
-                const int k = i & 1;
+                const int k = i % nst;
+                const uint32_t use = (uint32_t)(i / nst);
                 const int p0 = i * PF_PAGES_PER_TILE;
                 const int np = min(PF_PAGES_PER_TILE, n_pages - p0);
                 const int pg = lane < np ? __ldg(bt + p0 + lane) : 0;
+                const uint32_t eb = smem_u32(is_k ? &bars->k_empty[k] : &bars->v_empty[k]);
+                const uint32_t fb = smem_u32(is_k ? &bars->k_full[k] : &bars->v_full[k]);
                 int good = 1;
-                if (lane == 0)
-                    good = mbar_wait(smem_u32(&bars->kv_empty[k]), (uint32_t)(((i >> 1) & 1) ^ 1), abort);
+                if (lane == 0) {
+                    good = mbar_wait(eb, (use & 1u) ^ 1u, abort);
+                    if (good) mbar_arrive_expect_tx(fb, (uint32_t)np * 2 * 2048);
+                }
                 good = __shfl_sync(0xffffffffu, good, 0);
                 if (!good) break;
-                if (lane == 0) mbar_arrive_expect_tx(smem_u32(&bars->kv_full[k]), (uint32_t)np * 4 * 2048);
-                for (int p = 0; p < np; ++p) {
-                    const int page = __shfl_sync(0xffffffffu, pg, p);
-                    if (lane == 0) {
-                        const uint32_t fb = smem_u32(&bars->kv_full[k]);
-                        const uint32_t kt = s_base + OFF_K + k * PF_TILE_BYTES + p * 2048;
-                        const uint32_t vt = s_base + OFF_V + k * PF_TILE_BYTES + p * 2048;
-                        tma_load_3d(kt, &kmap, fb, 0, kvh, page * PAGE);
-                        tma_load_3d(kt + 16384, &kmap, fb, 64, kvh, page * PAGE);
-                        tma_load_3d(vt, &vmap, fb, 0, kvh, page * PAGE);
-                        tma_load_3d(vt + 16384, &vmap, fb, 64, kvh, page * PAGE);
+                if (lane < np) {
+                    const uint32_t t = s_base + (is_k ? OFF_K : OFF_V) + k * PF_TILE_BYTES + lane * 2048;
+                    tma_load_3d(t, map, fb, 0, kvh, pg * PAGE);
+                    tma_load_3d(t + 16384, map, fb, 64, kvh, pg * PAGE);
+                }
+                __syncwarp();
+                if (!is_k && has_tail && i == n_tiles - 1) {
+                    // this warp armed the phase it waits for: no parity aliasing
+                    const int ok_full = __shfl_sync(0xffffffffu, lane == 0 ? (int)mbar_wait(fb, use & 1u, abort) : 0, 0);
+                    if (ok_full) {
+                        const int tail = kv_len - i * PF_BN;
+                        const int r_end = min(PF_BN, (tail + PAGE - 1) & ~(PAGE - 1));
+                        uint8_t* vt = sm + OFF_V + k * PF_TILE_BYTES;
+                        for (int idx = lane; idx < (r_end - tail) * 16; idx += 32) {
+                            const int rr = tail + (idx >> 4), ch = idx & 15;
+                            *reinterpret_cast<uint4*>(vt + (ch >> 3) * 16384 + rr * 128 + (ch & 7) * 16) =
+                                make_uint4(0, 0, 0, 0);
+                        }
+                        fence_proxy_async_smem();
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(smem_u32(&bars->v_tail));
                     }
                 }
                 ++issued;
             }
             if (lane == 0 && *abort) {
-                for (int i = max(0, issued - 2); i < issued; ++i)
-                    mbar_wait_drain(smem_u32(&bars->kv_full[i & 1]), (uint32_t)((i >> 1) & 1));
+                for (int i = max(0, issued - nst); i < issued; ++i)
+                    mbar_wait_drain(smem_u32(is_k ? &bars->k_full[i % nst] : &bars->v_full[i % nst]),
+                                    (uint32_t)((i / nst) & 1));
             }
         } else if (warp == WARP_MMA && lane == 0) {
             // ============================================= MMA issuer ====
@@ -291,8 +336,11 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
             bool ok = mbar_wait(smem_u32(&bars->q_ready), 0, abort);
             auto issue_pv = [&](int j, int i) -> bool {  // O_j += P_j(i) V(i)
                 if (!mbar_wait(smem_u32(&bars->p_ready[j]), (uint32_t)(i & 1), abort)) return false;
+                if (!mbar_wait(smem_u32(&bars->v_full[i % VSTAGES]), (uint32_t)((i / VSTAGES) & 1), abort))
+                    return false;
+                if (has_tail && i == n_tiles - 1 && !mbar_wait(smem_u32(&bars->v_tail), 0, abort)) return false;
                 tc_fence_after();
-                const uint32_t vt = s_base + OFF_V + (i & 1) * PF_TILE_BYTES;
+                const uint32_t vt = s_base + OFF_V + (i % VSTAGES) * PF_TILE_BYTES;
                 const uint32_t pt = tmem + j * 128;
 #pragma unroll 1
                 for (int ks = 0; ks < 8; ++ks)
@@ -301,16 +349,18 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
                 return true;
             };
             for (int i = 0; i < n_tiles && ok; ++i) {
-                const int k = i & 1;
-                if (!mbar_wait(smem_u32(&bars->kv_ready[k]), (uint32_t)((i >> 1) & 1), abort)) {
-                    ok = false;
-                    break;
-                }
-                tc_fence_after();
-                const uint32_t kt = s_base + OFF_K + k * PF_TILE_BYTES;
+                const int k = i % KSTAGES;
+                bool k_in = false;
                 for (int j = 0; j < 2 && ok; ++j) {
                     if (i < ti[j].n_tiles) {
                         if (i > 0 && !(ok = issue_pv(j, i - 1))) break;
+                        if (!k_in) {
+                            if (!(ok = mbar_wait(smem_u32(&bars->k_ready[k]), (uint32_t)((i / KSTAGES) & 1), abort)))
+                                break;
+                            tc_fence_after();
+                            k_in = true;
+                        }
+                        const uint32_t kt = s_base + OFF_K + k * PF_TILE_BYTES;
                         const uint32_t qt = s_base + OFF_Q + j * PF_TILE_BYTES;
 #pragma unroll 1
                         for (int ks = 0; ks < 8; ++ks)
@@ -322,7 +372,9 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
                         umma_commit(smem_u32(&bars->o_done[j]));
                     }
                 }
-                if (ok && i > 0) umma_commit(smem_u32(&bars->kv_empty[(i - 1) & 1]));
+                if (!ok) break;
+                umma_commit(smem_u32(&bars->k_empty[k]));                       // K(i) read by S(i)
+                if (i > 0) umma_commit(smem_u32(&bars->v_empty[(i - 1) % VSTAGES]));  // V(i-1) read by PV(i-1)
             }
             for (int j = 0; j < 2 && ok; ++j) {
                 if (ti[j].n_tiles == n_tiles) {
@@ -374,14 +426,14 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
             dsn[e] = st.y;
         }
         for (int i = 0; i < n_tiles; ++i) {
-            const int k = i & 1;
-            if (!mbar_wait(smem_u32(&bars->kv_full[k]), (uint32_t)((i >> 1) & 1), abort)) break;
+            const int k = i % KSTAGES;
+            if (!mbar_wait(smem_u32(&bars->k_full[k]), (uint32_t)((i / KSTAGES) & 1), abort)) break;
             uint8_t* kt = sm + OFF_K + k * PF_TILE_BYTES;
             const int t0 = i * PF_BN;
             float c[8], sn[8];
 #pragma unroll
             for (int e = 0; e < 8; ++e) rope_cos_sin((uint32_t)(t0 + r0), bars->turns[8 * u + e], c[e], sn[e]);
-#pragma unroll 1
+#pragma unroll 2
             for (int m = 0; m < 8; ++m) {
                 const int r = r0 + 16 * m;
                 const uint32_t off = sw_off(r, u);
@@ -394,20 +446,9 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
                     sn[e] = snn;
                 }
             }
-            // V rows past the last key of this CTA: zero (they meet P = 0 and
-            // must not bring stale or non-finite bits into the MMA).
-            if (t0 + PF_BN > n_keys) {
-                uint8_t* vt = sm + OFF_V + k * PF_TILE_BYTES;
-                for (int idx = tid; idx < PF_BN * 16; idx += 128) {
-                    const int r = idx >> 4, ch = idx & 15;
-                    if (t0 + r >= n_keys)
-                        *reinterpret_cast<uint4*>(vt + (ch >> 3) * 16384 + r * 128 + (ch & 7) * 16) =
-                            make_uint4(0, 0, 0, 0);
-                }
-            }
             if (range_exceeded(range)) bars->range_bad = 1;
             fence_proxy_async_smem();
-            mbar_arrive(smem_u32(&bars->kv_ready[k]));
+            mbar_arrive(smem_u32(&bars->k_ready[k]));
         }
         named_bar_sync(1, 384);  // transform done: the range flag is final for the epilogues
         named_bar_sync(2, PF_THREADS);
