@@ -83,6 +83,22 @@ def traffic_for(kernel, src_hash):
     return d.get("dram_bytes_per_launch")
 
 
+def max_over_ranks(value, world, device="cpu"):
+    """Max of a per-rank float over all ranks (the slowest replica sets the time)."""
+    if world <= 1:
+        return float(value)
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_rate(units_per_rank_step, steps, world, region_ms):
+    """Units processed by all replicas per second over the (max) timed region."""
+    return world * units_per_rank_step * steps / (region_ms * 1e-3)
+
+
 class ClockSampler:
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
@@ -318,12 +334,8 @@ def run_ours(args):
         torch.cuda.synchronize()
         barrier()
         wall = time.perf_counter() - t0
-    region_ms = ev0.elapsed_time(ev1)
-    if world > 1:
-        tt = torch.tensor([region_ms], device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        region_ms = float(tt.item())
-    value = world * step_bytes * args.steps / (region_ms * 1e-3) / 1e9
+    region_ms = max_over_ranks(ev0.elapsed_time(ev1), world, dev)
+    value = whole_job_rate(step_bytes, args.steps, world, region_ms) / 1e9
     per_launch = time_launches(step, max(10, args.steps), stream)
     avg_launch_ms = sum(per_launch) / len(per_launch)
     dec_hash = source_hash("decode.cu", "rk_device.cuh", "rk_internal.h")
