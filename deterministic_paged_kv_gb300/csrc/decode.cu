@@ -1,30 +1,38 @@
-// decode.cu -- split-free paged decode with fused RoPE and GQA packing.
+// decode.cu -- split-free paged decode on the 5th-gen tensor cores, RoPE
+// applied to K as it is read.
 //
 // Operation: paged decode of "flashinfer_fa2 backend for Ada (SM89)" (BF16,
-// page 16, head_dim 128, NHD, split-KV disabled so a row's reduction does not
+// page 16, head_dim 128, NHD; split-KV disabled so a row's reduction does not
 // depend on plan width or batch), with ROPE_LLAMA fused as in "WS2 PR7 Fused
 // Attention Backend Alignment", "FlashInfer RoPE Fusion", and the FP32 LSE of
-// the same page's "Original PR7 Requirements" table.
+// that page's "Original PR7 Requirements" table.
 //
-// Design (bandwidth-bound: 512 B of K+V per token and KV head):
-//   * one CTA per (row b, KV head, up to 4 query heads); the CTA streams the
-//     row's pages in ascending logical order, one page (16 tokens x 256 B for
-//     K, the same for V) per pipeline stage, fetched by a dedicated producer
-//     warp with TMA into an 8-deep shared-memory ring;
-//   * four consumer warps; the 8-lane group g of warp w owns token slot
-//     4w+g of every page, each lane 16 of the 128 dimensions laid out so a
-//     lane holds both members of its 8 rotate-half pairs (dims 8j..8j+7 and
-//     64+8j..64+8j+7): K is rotated in registers in FP32 as it is read;
-//   * the rotation angles come from an exact fixed-point anchor every 16
-//     pages and an angle-addition step of 16 positions in between;
-//   * scores are reduced over the group with an xor butterfly (bitwise
-//     identical in all 8 lanes), online softmax in the log2 domain with a
-//     slack of 8 before the running maximum is moved (exact result, fewer
-//     rescales), PV accumulated in FP32 registers;
-//   * the 16 slot partial states are merged in fixed slot order 0..15, then
-//     out is rounded to BF16 once (RNE) and the LSE written in FP32.
-// Every choice above depends only on the row's own data and logical token
-// index, never on B, W, grid size or which SM runs the CTA.
+// One CTA per (row b, KV head); all G = Hq/Hkv query heads of the group are
+// served by one pass over the row's pages (GQA packing: every K/V byte is
+// read once).  The row's tokens are swept in ascending tiles of 128 (8 pages):
+//   warps 8 / 10  TMA producers: K pages (3-stage ring) and V pages (2-stage
+//                 ring) as 16-token x 64-dim boxes with 128-byte swizzle, i.e.
+//                 already in the UMMA operand layout; the V producer zeroes
+//                 cache rows past kv_len in a partial last page;
+//   warps 0-3     transform: rotate each K row in FP32 (angles from an exact
+//                 fixed-point anchor plus 16-position steps) and store it as
+//                 FP16 in place; rotate the G query rows once (FP16 Q^T);
+//   warp 9        MMA issuer: S^T = K Q^T (M = 128 tokens, N = 16 >= G heads,
+//                 FP16 operands, FP32 in TMEM, double-buffered) and
+//                 O^T += V^T P^T (M = 128 dims, N = 16, BF16, FP32 in TMEM);
+//   warps 4-7     softmax: thread t owns token t of the tile: masks, takes the
+//                 tile max per head over the 128 tokens (xor-butterfly + fixed
+//                 warp order), moves the running max only when it grows by
+//                 more than 8 (log2 domain; then the O^T column is rescaled in
+//                 TMEM), writes P^T as BF16 to shared memory and keeps a
+//                 per-thread partial of l; epilogue reduces l in a fixed
+//                 tree, writes out = O / l (BF16, once) and the LSE (FP32).
+// Score precision: FP16 rotated operands (11-bit mantissa) keep the LSE
+// within 1e-3 of float64 even for a single visible key; pre-RoPE q / k
+// elements at or above 2^15 would overflow FP16 once rotated and are
+// reported (RK_STATUS_RANGE) instead of computed.
+// Every choice depends only on the row's data and logical token index, never
+// on B, W, the grid or the SM.
 #include <atomic>
 
 #include "rk_device.cuh"
@@ -33,64 +41,60 @@ namespace rk {
 
 namespace {
 
-constexpr uint32_t FULL = 0xffffffffu;
+constexpr int WARP_TMA_K = 8;
+constexpr int WARP_MMA = 9;
+constexpr int WARP_TMA_V = 10;
+constexpr uint32_t TMEM_COLS = 64;  // S^T buffers [0,16) [16,32), O^T [32,48)
+constexpr float RESCALE_SLACK = 8.0f;
+constexpr int NH = 16;  // N of both MMAs: query heads of the group, zero padded
 
-struct DecShared {
-    uint64_t full_bar[DEC_STAGES];
-    uint64_t empty_bar[DEC_STAGES];
-    uint64_t turns[ROPE_PAIRS];
-    float4 step[ROPE_PAIRS / 2];  // (cos, sin) of a 16-position turn, two pairs per entry
+constexpr int OFF_K = 0;
+constexpr int OFF_V = OFF_K + DEC_KSTAGES * DEC_TILE_BYTES;
+constexpr int OFF_QT = OFF_V + DEC_VSTAGES * DEC_TILE_BYTES;  // Q^T: 16 rows x 128 dims FP16
+constexpr int OFF_PT = OFF_QT + NH * HEAD_DIM * 2;            // P^T: 16 rows x 128 tokens BF16
+constexpr int OFF_CTRL = OFF_PT + NH * DEC_BN * 2;
+static_assert(OFF_CTRL + DEC_CTRL_BYTES == DEC_SMEM_BYTES, "decode shared memory carve");
+
+struct DecCtrl {
+    uint64_t q_ready;
+    uint64_t k_full[DEC_KSTAGES], k_ready[DEC_KSTAGES], k_empty[DEC_KSTAGES];
+    uint64_t v_full[DEC_VSTAGES], v_empty[DEC_VSTAGES], v_tail;
+    uint64_t s_full[2], s_free[2], p_ready, pv_done, o_done;
+    uint64_t red_bar[2];  // the 4 softmax warps' tile maxima are in red[sb]
+    uint32_t tmem_base;
     int abort;
+    int range_bad;
+    uint64_t turns[ROPE_PAIRS];
+    float2 step16[ROPE_PAIRS];
+    float red[2][4][8];  // per-warp tile maxima, double-buffered by tile parity
+    float lred[4][8];    // per-warp partial l at the end
 };
-static_assert(sizeof(DecShared) <= DEC_CTRL_BYTES, "decode control block exceeds its reservation");
-static_assert(16 * 4 * HEAD_DIM * 4 + 16 * 4 * 2 * 4 <= DEC_STAGES * DEC_STAGE_BYTES,
-              "merge scratch must fit in the stage ring");
+static_assert(sizeof(DecCtrl) <= DEC_CTRL_BYTES, "decode control block exceeds its reservation");
 
-template <int GH>
 __device__ __forceinline__ void write_empty_row(const DecodeArgs& a, int b, int h0, float lse_val) {
     __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(a.out);
-    for (int i = threadIdx.x; i < GH * HEAD_DIM; i += blockDim.x) {
+    for (int i = threadIdx.x; i < a.G * HEAD_DIM; i += blockDim.x) {
         const int hh = i / HEAD_DIM, d = i % HEAD_DIM;
         out[((size_t)b * a.Hq + h0 + hh) * HEAD_DIM + d] = __float2bfloat16_rn(0.0f);
     }
-    if (threadIdx.x < GH) a.lse[(size_t)b * a.Hq + h0 + threadIdx.x] = lse_val;
+    if (threadIdx.x < a.G) a.lse[(size_t)b * a.Hq + h0 + threadIdx.x] = lse_val;
 }
 
-// 16 bf16 (two 16-byte chunks: dims 8j.. and 64+8j..) -> rotated floats.
-__device__ __forceinline__ void load_rotate16(const uint4& lo4, const uint4& hi4, const float (&c)[8],
-                                              const float (&s)[8], float (&x)[16]) {
-    const uint32_t lw[4] = {lo4.x, lo4.y, lo4.z, lo4.w};
-    const uint32_t hw[4] = {hi4.x, hi4.y, hi4.z, hi4.w};
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {
-        const float l0 = bf16lo(lw[k]), l1 = bf16hi(lw[k]);
-        const float u0 = bf16lo(hw[k]), u1 = bf16hi(hw[k]);
-        const int e0 = 2 * k, e1 = 2 * k + 1;
-        x[e0] = l0 * c[e0] - u0 * s[e0];
-        x[8 + e0] = u0 * c[e0] + l0 * s[e0];
-        x[e1] = l1 * c[e1] - u1 * s[e1];
-        x[8 + e1] = u1 * c[e1] + l1 * s[e1];
-    }
-}
-
-template <int GH>
-__global__ void __launch_bounds__(DEC_THREADS, 2)
+__global__ void __launch_bounds__(DEC_THREADS, 1)
     decode_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
                   const __grid_constant__ DecodeArgs a) {
-    extern __shared__ __align__(1024) uint8_t smem[];
-    uint8_t* stages = smem;
-    DecShared* sh = reinterpret_cast<DecShared*>(smem + DEC_STAGES * DEC_STAGE_BYTES);
+    extern __shared__ __align__(1024) uint8_t sm[];
+    DecCtrl* ctl = reinterpret_cast<DecCtrl*>(sm + OFF_CTRL);
+    const uint32_t s_base = smem_u32(sm);
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int kvh = blockIdx.x % a.Hkv, b = blockIdx.x / a.Hkv;
+    const int G = a.G, h0 = kvh * G;
+    if (s_base & 1023u) {  // the swizzled operand layout needs a 1024-byte aligned base
+        if (tid == 0 && a.status) atomicOr(a.status, RK_STATUS_TIMEOUT);
+        return;
+    }
 
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int n_hg = a.G / GH;
-    int unit = blockIdx.x;
-    const int hg = unit % n_hg;
-    unit /= n_hg;
-    const int kvh = unit % a.Hkv;
-    const int b = unit / a.Hkv;
-    const int h0 = kvh * a.G + hg * GH;
-
-    // ---- row metadata and memory-safety checks (device copy of metadata) --
+    // ---- row metadata (device copy) and memory-safety checks ----
     const int kv_len = a.kv_lens[b];
     const int qpos = a.position_ids[b];
     int bad = 0;
@@ -98,266 +102,391 @@ __global__ void __launch_bounds__(DEC_THREADS, 2)
     if (qpos < 0) bad |= RK_STATUS_POSITION;
     const int n_vis = bad ? 0 : (qpos >= kv_len ? kv_len : qpos + 1);
     const int n_pages = (n_vis + PAGE - 1) / PAGE;
+    const int n_tiles = (n_vis + DEC_BN - 1) / DEC_BN;
+    // Last page partly filled and inside the visible range: its rows past
+    // kv_len hold arbitrary bits and are zeroed in V after the copy lands.
+    const bool has_tail = n_vis == kv_len && (kv_len & (PAGE - 1)) != 0;
     const int32_t* bt = a.block_table + (size_t)b * a.W;
     int oob = 0;
-    for (int i = threadIdx.x; i < n_pages; i += blockDim.x) {
+    for (int i = tid; i < n_pages; i += DEC_THREADS) {
         const int pg = __ldg(bt + i);
         oob |= (pg < 0) | (pg >= a.num_pages);
     }
-    if (threadIdx.x < ROPE_PAIRS) sh->turns[threadIdx.x] = a.rope_turns[threadIdx.x];
-    if (threadIdx.x < ROPE_PAIRS / 2) {
-        float c0, s0, c1, s1;
-        rope_cos_sin((uint32_t)PAGE, a.rope_turns[2 * threadIdx.x], c0, s0);
-        rope_cos_sin((uint32_t)PAGE, a.rope_turns[2 * threadIdx.x + 1], c1, s1);
-        sh->step[threadIdx.x] = make_float4(c0, s0, c1, s1);
-    }
-    if (threadIdx.x == 0) {
-        sh->abort = 0;
-        for (int s = 0; s < DEC_STAGES; ++s) {
-            mbar_init(smem_u32(&sh->full_bar[s]), 1);
-            mbar_init(smem_u32(&sh->empty_bar[s]), DEC_CWARPS);
+    if (tid == 0) {
+        ctl->abort = 0;
+        ctl->range_bad = 0;
+        mbar_init(smem_u32(&ctl->q_ready), 128);
+        for (int k = 0; k < DEC_KSTAGES; ++k) {
+            mbar_init(smem_u32(&ctl->k_full[k]), 1);
+            mbar_init(smem_u32(&ctl->k_ready[k]), 128);
+            mbar_init(smem_u32(&ctl->k_empty[k]), 1);
         }
+        for (int k = 0; k < DEC_VSTAGES; ++k) {
+            mbar_init(smem_u32(&ctl->v_full[k]), 1);
+            mbar_init(smem_u32(&ctl->v_empty[k]), 1);
+        }
+        mbar_init(smem_u32(&ctl->v_tail), 1);
+        for (int k = 0; k < 2; ++k) {
+            mbar_init(smem_u32(&ctl->s_full[k]), 1);
+            mbar_init(smem_u32(&ctl->s_free[k]), 128);
+        }
+        mbar_init(smem_u32(&ctl->p_ready), 128);
+        mbar_init(smem_u32(&ctl->pv_done), 1);
+        mbar_init(smem_u32(&ctl->o_done), 1);
+        mbar_init(smem_u32(&ctl->red_bar[0]), 4);
+        mbar_init(smem_u32(&ctl->red_bar[1]), 4);
         fence_mbar_init();
     }
+    if (tid < ROPE_PAIRS) {
+        ctl->turns[tid] = a.rope_turns[tid];
+        float c, s;
+        rope_cos_sin((uint32_t)PAGE, a.rope_turns[tid], c, s);
+        ctl->step16[tid] = make_float2(c, s);
+    }
+    // V stages, Q^T and P^T start as zeros (rows never written stay finite).
+    for (int i = tid; i < (OFF_CTRL - OFF_V) / 16; i += DEC_THREADS)
+        reinterpret_cast<uint4*>(sm + OFF_V)[i] = make_uint4(0, 0, 0, 0);
+    fence_proxy_async_smem();
     if (__syncthreads_or(oob)) bad |= RK_STATUS_PAGE_OOB;
     if (bad) {
-        if (threadIdx.x == 0 && a.status) atomicOr(a.status, bad);
-        write_empty_row<GH>(a, b, h0, __int_as_float(0x7fc00000));
+        if (tid == 0 && a.status) atomicOr(a.status, bad);
+        write_empty_row(a, b, h0, __int_as_float(0x7fc00000));
         return;
     }
     if (n_vis == 0) {
-        write_empty_row<GH>(a, b, h0, -INFINITY);
+        write_empty_row(a, b, h0, -INFINITY);
         return;
     }
 
-    if (warp == DEC_CWARPS) {
-        // ------------------------------------------------ TMA producer ----
-        prefetch_tmap(&kmap);
-        prefetch_tmap(&vmap);
-        bool ok = true;
+    if (warp == WARP_MMA) {
+        tmem_alloc(smem_u32(&ctl->tmem_base), TMEM_COLS);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = ctl->tmem_base;
+    const uint32_t tO = tmem + 32;
+    volatile int* abort = &ctl->abort;
+
+    if (warp == WARP_TMA_K || warp == WARP_TMA_V) {
+        // ========================================== TMA producers ====
+        const bool is_k = warp == WARP_TMA_K;
+        const CUtensorMap* map = is_k ? &kmap : &vmap;
+        const int nst = is_k ? DEC_KSTAGES : DEC_VSTAGES;
+        constexpr int PPT = DEC_BN / PAGE;  // pages per tile
+        if (lane == 0) prefetch_tmap(map);
         int issued = 0;
-        for (int base = 0; base < n_pages && ok; base += 32) {
-            const int idx = base + lane;
-            const int pg = idx < n_pages ? __ldg(bt + idx) : 0;
-            const int cnt = min(32, n_pages - base);
-            for (int jj = 0; jj < cnt; ++jj) {
-                const int page = __shfl_sync(FULL, pg, jj);
-                const int it = base + jj;
-                const int st = it % DEC_STAGES;
-                const uint32_t ph = (uint32_t)(it / DEC_STAGES) & 1u;
-                int good = 1;
-                if (lane == 0) {
-                    good = mbar_wait(smem_u32(&sh->empty_bar[st]), ph ^ 1u, &sh->abort);
-                    if (good) {
-                        const uint32_t fb = smem_u32(&sh->full_bar[st]);
-                        mbar_arrive_expect_tx(fb, DEC_STAGE_BYTES);
-                        const uint32_t dst = smem_u32(stages + st * DEC_STAGE_BYTES);
-                        tma_load_3d(dst, &kmap, fb, 0, kvh, page * PAGE);
-                        tma_load_3d(dst + DEC_PAGE_BYTES, &vmap, fb, 0, kvh, page * PAGE);
+        int pg_next = lane < min(PPT, n_pages) ? __ldg(bt + lane) : 0;
+        for (int i = 0; i < n_tiles; ++i) {
+            const int k = i % nst;
+            const uint32_t use = (uint32_t)(i / nst);
+            const int np = min(PPT, n_pages - i * PPT);
+            const int pg = pg_next;
+            const int nxt = (i + 1) * PPT + lane;  // the next tile's page ids, loaded ahead
+            pg_next = (i + 1 < n_tiles && lane < PPT && nxt < n_pages) ? __ldg(bt + nxt) : 0;
+            const uint32_t eb = smem_u32(is_k ? &ctl->k_empty[k] : &ctl->v_empty[k]);
+            const uint32_t fb = smem_u32(is_k ? &ctl->k_full[k] : &ctl->v_full[k]);
+            int good = 1;
+            if (lane == 0) {
+                good = mbar_wait(eb, (use & 1u) ^ 1u, abort);
+                if (good) mbar_arrive_expect_tx(fb, (uint32_t)np * 2 * 2048);
+            }
+            good = __shfl_sync(0xffffffffu, good, 0);
+            if (!good) break;
+            if (lane < np) {
+                const uint32_t t = s_base + (is_k ? OFF_K : OFF_V) + k * DEC_TILE_BYTES + lane * 2048;
+                tma_load_3d(t, map, fb, 0, kvh, pg * PAGE);
+                tma_load_3d(t + 16384, map, fb, 64, kvh, pg * PAGE);
+            }
+            __syncwarp();
+            if (!is_k && has_tail && i == n_tiles - 1) {
+                // this warp armed the phase it waits for: no parity aliasing
+                const int landed =
+                    __shfl_sync(0xffffffffu, lane == 0 ? (int)mbar_wait(fb, use & 1u, abort) : 0, 0);
+                if (landed) {
+                    const int tail = kv_len - i * DEC_BN;
+                    const int r_end = min(DEC_BN, (tail + PAGE - 1) & ~(PAGE - 1));
+                    uint8_t* vt = sm + OFF_V + k * DEC_TILE_BYTES;
+                    for (int idx = lane; idx < (r_end - tail) * 16; idx += 32) {
+                        const int rr = tail + (idx >> 4), ch = idx & 15;
+                        *reinterpret_cast<uint4*>(vt + (ch >> 3) * 16384 + rr * 128 + (ch & 7) * 16) =
+                            make_uint4(0, 0, 0, 0);
                     }
+                    fence_proxy_async_smem();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(smem_u32(&ctl->v_tail));
                 }
-                ok = __shfl_sync(FULL, good, 0) != 0;
-                if (!ok) break;
-                ++issued;
             }
+            ++issued;
         }
-        if (!ok && lane == 0) {
-            // Let copies already issued land before the CTA exits.
-            for (int it = max(0, issued - DEC_STAGES); it < issued; ++it)
-                mbar_wait_drain(smem_u32(&sh->full_bar[it % DEC_STAGES]),
-                                (uint32_t)(it / DEC_STAGES) & 1u);
-            if (a.status) atomicOr(a.status, RK_STATUS_TIMEOUT);
+        if (lane == 0 && *abort) {
+            for (int i = max(0, issued - nst); i < issued; ++i)
+                mbar_wait_drain(smem_u32(is_k ? &ctl->k_full[i % nst] : &ctl->v_full[i % nst]),
+                                (uint32_t)((i / nst) & 1));
         }
-        return;
-    }
-
-    // ---------------------------------------------------------- consumers --
-    const int g = lane >> 3, j = lane & 7;
-    const int slot = warp * 4 + g;
-    const uint32_t gmask = 0xffu << (8 * g);
-
-    // Query: rotate at its position, pre-scale by sm_scale * log2(e).
-    float qv[GH][16];
-    {
-        float c[8], s[8];
-#pragma unroll
-        for (int e = 0; e < 8; ++e) rope_cos_sin((uint32_t)qpos, sh->turns[8 * j + e], c[e], s[e]);
-        const __nv_bfloat16* qb = reinterpret_cast<const __nv_bfloat16*>(a.q);
-#pragma unroll
-        for (int hh = 0; hh < GH; ++hh) {
-            const uint4* row =
-                reinterpret_cast<const uint4*>(qb + ((size_t)b * a.Hq + h0 + hh) * HEAD_DIM);
-            load_rotate16(__ldg(row + j), __ldg(row + 8 + j), c, s, qv[hh]);
-#pragma unroll
-            for (int e = 0; e < 16; ++e) qv[hh][e] *= a.qk_scale_log2;
-        }
-    }
-
-    // Key rotation state for this lane's 8 pairs at token t = 16*it + slot.
-    float kc[8], ks[8];
-#pragma unroll
-    for (int e = 0; e < 8; ++e) rope_cos_sin((uint32_t)slot, sh->turns[8 * j + e], kc[e], ks[e]);
-
-    float m[GH], l[GH], acc[GH][16];
-#pragma unroll
-    for (int hh = 0; hh < GH; ++hh) {
-        m[hh] = -INFINITY;
-        l[hh] = 0.0f;
-#pragma unroll
-        for (int e = 0; e < 16; ++e) acc[hh][e] = 0.0f;
-    }
-
-    bool ok = true;
-    for (int it = 0; it < n_pages; ++it) {
-        const int st = it % DEC_STAGES;
-        const uint32_t ph = (uint32_t)(it / DEC_STAGES) & 1u;
-        if (!mbar_wait(smem_u32(&sh->full_bar[st]), ph, &sh->abort)) {
-            ok = false;
-            break;
-        }
-        const int t = it * PAGE + slot;
-        if (t < n_vis) {
-            const uint8_t* kbase = stages + st * DEC_STAGE_BYTES + slot * (HEAD_DIM * 2);
-            const uint4* krow = reinterpret_cast<const uint4*>(kbase);
-            float kf[16];
-            load_rotate16(krow[j], krow[8 + j], kc, ks, kf);
-            float sc[GH];
-#pragma unroll
-            for (int hh = 0; hh < GH; ++hh) {
-                float p0 = 0.f, p1 = 0.f;
-#pragma unroll
-                for (int e = 0; e < 16; e += 2) {
-                    p0 = fmaf(qv[hh][e], kf[e], p0);
-                    p1 = fmaf(qv[hh][e + 1], kf[e + 1], p1);
-                }
-                sc[hh] = p0 + p1;
+    } else if (warp == WARP_MMA) {
+        // ============================================= MMA issuer ====
+        if (lane == 0) {
+            const uint32_t idS = idesc_f16_f32(DEC_BN, NH);
+            const uint32_t idO = idesc_bf16_f32(HEAD_DIM, NH, 1, 0);
+            const uint32_t qt = s_base + OFF_QT, pt = s_base + OFF_PT;
+            bool ok = mbar_wait(smem_u32(&ctl->q_ready), 0, abort);
+            auto issue_pv = [&](int i) -> bool {
+                if (!mbar_wait(smem_u32(&ctl->p_ready), (uint32_t)(i & 1), abort)) return false;
+                if (!mbar_wait(smem_u32(&ctl->v_full[i % DEC_VSTAGES]), (uint32_t)((i / DEC_VSTAGES) & 1), abort))
+                    return false;
+                if (has_tail && i == n_tiles - 1 && !mbar_wait(smem_u32(&ctl->v_tail), 0, abort)) return false;
+                tc_fence_after();
+                const uint32_t vt = s_base + OFF_V + (i % DEC_VSTAGES) * DEC_TILE_BYTES;
+#pragma unroll 1
+                for (int ks = 0; ks < 8; ++ks)
+                    umma_ss(tO, smem_desc(vt + ks * 2048, 16384, 1024, 2),
+                            smem_desc(pt + (ks >> 2) * 2048 + (ks & 3) * 32, 16, 1024, 2), idO,
+                            (i > 0 || ks > 0) ? 1u : 0u);
+                umma_commit(smem_u32(&ctl->pv_done));
+                umma_commit(smem_u32(&ctl->v_empty[i % DEC_VSTAGES]));
+                return true;
+            };
+            for (int i = 0; i < n_tiles && ok; ++i) {
+                const int k = i % DEC_KSTAGES, sb = i & 1;
+                if (!(ok = mbar_wait(smem_u32(&ctl->k_ready[k]), (uint32_t)((i / DEC_KSTAGES) & 1), abort))) break;
+                if (i >= 2 &&
+                    !(ok = mbar_wait(smem_u32(&ctl->s_free[sb]), (uint32_t)(((i >> 1) - 1) & 1), abort)))
+                    break;
+                tc_fence_after();
+                const uint32_t kt = s_base + OFF_K + k * DEC_TILE_BYTES;
+#pragma unroll 1
+                for (int ks = 0; ks < 8; ++ks)
+                    umma_ss(tmem + sb * NH, smem_desc(kt + (ks >> 2) * 16384 + (ks & 3) * 32, 16, 1024, 2),
+                            smem_desc(qt + (ks >> 2) * 2048 + (ks & 3) * 32, 16, 1024, 2), idS,
+                            ks > 0 ? 1u : 0u);
+                umma_commit(smem_u32(&ctl->s_full[sb]));
+                umma_commit(smem_u32(&ctl->k_empty[k]));
+                if (i >= 1 && !(ok = issue_pv(i - 1))) break;
             }
-#pragma unroll
-            for (int off = 4; off >= 1; off >>= 1) {
-#pragma unroll
-                for (int hh = 0; hh < GH; ++hh) sc[hh] += __shfl_xor_sync(gmask, sc[hh], off);
-            }
-            float p[GH];
-#pragma unroll
-            for (int hh = 0; hh < GH; ++hh) {
-                if (sc[hh] > m[hh] + DEC_RESCALE_THRESHOLD) {
-                    const float alpha = ex2(m[hh] - sc[hh]);
-                    m[hh] = sc[hh];
-                    l[hh] *= alpha;
-#pragma unroll
-                    for (int e = 0; e < 16; ++e) acc[hh][e] *= alpha;
-                }
-                p[hh] = ex2(sc[hh] - m[hh]);
-                l[hh] += p[hh];
-            }
-            const uint4* vrow = reinterpret_cast<const uint4*>(kbase + DEC_PAGE_BYTES);
-            const uint4 vlo = vrow[j], vhi = vrow[8 + j];
-            const uint32_t lw[4] = {vlo.x, vlo.y, vlo.z, vlo.w};
-            const uint32_t hw[4] = {vhi.x, vhi.y, vhi.z, vhi.w};
-#pragma unroll
-            for (int k = 0; k < 4; ++k) {
-                const float v0 = bf16lo(lw[k]), v1 = bf16hi(lw[k]);
-                const float w0 = bf16lo(hw[k]), w1 = bf16hi(hw[k]);
-#pragma unroll
-                for (int hh = 0; hh < GH; ++hh) {
-                    acc[hh][2 * k] = fmaf(p[hh], v0, acc[hh][2 * k]);
-                    acc[hh][2 * k + 1] = fmaf(p[hh], v1, acc[hh][2 * k + 1]);
-                    acc[hh][8 + 2 * k] = fmaf(p[hh], w0, acc[hh][8 + 2 * k]);
-                    acc[hh][8 + 2 * k + 1] = fmaf(p[hh], w1, acc[hh][8 + 2 * k + 1]);
+            if (ok && (ok = issue_pv(n_tiles - 1))) umma_commit(smem_u32(&ctl->o_done));
+            if (!ok) {
+                const uint64_t t0 = global_timer_ns();  // let issued MMAs drain before TMEM is released
+                while (global_timer_ns() - t0 < 1000000ull) {
                 }
             }
         }
         __syncwarp();
-        if (lane == 0) mbar_arrive(smem_u32(&sh->empty_bar[st]));
-        // Advance this lane's angles by one page (16 positions).
-        if ((it + 1) % DEC_REANCHOR == 0) {
+    } else if (warp < 4) {
+        // ============================================== transform WG ====
+        uint32_t range = 0;
+        {
+            // Q^T: thread (h, u) rotates chunk pair u of query head h at qpos.
+            if (tid < G * 8) {
+                const int h = tid >> 3, u = tid & 7;
+                const uint4* row = reinterpret_cast<const uint4*>(reinterpret_cast<const __nv_bfloat16*>(a.q) +
+                                                                  ((size_t)b * a.Hq + h0 + h) * HEAD_DIM);
+                __align__(16) uint8_t tmp[32];
+                *reinterpret_cast<uint4*>(tmp) = __ldg(row + u);
+                *reinterpret_cast<uint4*>(tmp + 16) = __ldg(row + 8 + u);
+                float c[8], sn[8];
 #pragma unroll
-            for (int e = 0; e < 8; ++e)
-                rope_cos_sin((uint32_t)(t + PAGE), sh->turns[8 * j + e], kc[e], ks[e]);
-        } else {
-#pragma unroll
-            for (int e2 = 0; e2 < 4; ++e2) {
-                const float4 st4 = sh->step[4 * j + e2];
-                const float d0c = st4.x, d0s = st4.y, d1c = st4.z, d1s = st4.w;
-                const int e0 = 2 * e2, e1 = 2 * e2 + 1;
-                const float c0 = kc[e0] * d0c - ks[e0] * d0s, s0 = ks[e0] * d0c + kc[e0] * d0s;
-                const float c1 = kc[e1] * d1c - ks[e1] * d1s, s1 = ks[e1] * d1c + kc[e1] * d1s;
-                kc[e0] = c0; ks[e0] = s0; kc[e1] = c1; ks[e1] = s1;
+                for (int e = 0; e < 8; ++e) rope_cos_sin((uint32_t)qpos, ctl->turns[8 * u + e], c[e], sn[e]);
+                range = rotate_chunk_f16(tmp, tmp + 16, c, sn, range);
+                const uint32_t off = sw128_off(h, u);
+                *reinterpret_cast<uint4*>(sm + OFF_QT + off) = *reinterpret_cast<const uint4*>(tmp);
+                *reinterpret_cast<uint4*>(sm + OFF_QT + 2048 + off) = *reinterpret_cast<const uint4*>(tmp + 16);
             }
+            if (range_exceeded(range)) ctl->range_bad = 1;
+            fence_proxy_async_smem();
+            mbar_arrive(smem_u32(&ctl->q_ready));
+        }
+        const int u = tid & 7, r0 = tid >> 3;
+        float dcs[8], dsn[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+            const float2 st = ctl->step16[8 * u + e];
+            dcs[e] = st.x;
+            dsn[e] = st.y;
+        }
+        for (int i = 0; i < n_tiles; ++i) {
+            const int k = i % DEC_KSTAGES;
+            if (!mbar_wait(smem_u32(&ctl->k_full[k]), (uint32_t)((i / DEC_KSTAGES) & 1), abort)) break;
+            uint8_t* kt = sm + OFF_K + k * DEC_TILE_BYTES;
+            const int t0 = i * DEC_BN;
+            float c[8], sn[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) rope_cos_sin((uint32_t)(t0 + r0), ctl->turns[8 * u + e], c[e], sn[e]);
+#pragma unroll 2
+            for (int m = 0; m < 8; ++m) {
+                const int r = r0 + 16 * m;
+                const uint32_t off = sw128_off(r, u);
+                if (t0 + r < n_vis) range = rotate_chunk_f16(kt + off, kt + 16384 + off, c, sn, range);
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    const float cn = c[e] * dcs[e] - sn[e] * dsn[e];
+                    const float snn = sn[e] * dcs[e] + c[e] * dsn[e];
+                    c[e] = cn;
+                    sn[e] = snn;
+                }
+            }
+            if (range_exceeded(range)) ctl->range_bad = 1;
+            fence_proxy_async_smem();
+            mbar_arrive(smem_u32(&ctl->k_ready[k]));
+        }
+        named_bar_sync(2, 256);  // transform done: the range flag is final for the epilogue
+    } else if (warp < 8) {
+        // =============================================== softmax WG ====
+        const int t = tid - 128;  // token of the tile == TMEM lane (S^T rows) == output dim (O^T rows)
+        const int wq = warp & 3;
+        const uint32_t lane_addr = (uint32_t)(wq * 32) << 16;
+        const float scl = a.qk_scale_log2;
+        float m[8], lp[8];
+#pragma unroll
+        for (int h = 0; h < 8; ++h) {
+            m[h] = -INFINITY;
+            lp[h] = 0.0f;
+        }
+        bool ok = true;
+        for (int i = 0; i < n_tiles; ++i) {
+            const int sb = i & 1;
+            if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&ctl->s_full[sb]), (uint32_t)((i >> 1) & 1), abort))) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            uint32_t sr[16];
+            tmem_ld16(tmem + sb * NH + lane_addr, sr);
+            tmem_ld_wait();
+            tc_fence_before();
+            mbar_arrive(smem_u32(&ctl->s_free[sb]));
+            const bool vis = i * DEC_BN + t < n_vis;
+            float x[8];
+#pragma unroll
+            for (int h = 0; h < 8; ++h) {
+                x[h] = (vis && h < G) ? __uint_as_float(sr[h]) * scl : -INFINITY;
+                float v = x[h];
+#pragma unroll
+                for (int off = 16; off >= 1; off >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, off));
+                if (lane == 0) ctl->red[sb][wq][h] = v;
+            }
+            // Exchange the four warps' maxima through an mbarrier (bounded wait,
+            // so a warp that gave up cannot strand the others at a barrier).
+            __syncwarp();
+            if (lane == 0) mbar_arrive(smem_u32(&ctl->red_bar[sb]));
+            if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&ctl->red_bar[sb]), (uint32_t)((i >> 1) & 1), abort))) {
+                ok = false;
+                break;
+            }
+            float alpha[8];
+            bool resc = false;
+#pragma unroll
+            for (int h = 0; h < 8; ++h) {
+                const float mt = fmaxf(fmaxf(ctl->red[sb][0][h], ctl->red[sb][1][h]),
+                                       fmaxf(ctl->red[sb][2][h], ctl->red[sb][3][h]));
+                alpha[h] = 1.0f;
+                if (mt > m[h] + RESCALE_SLACK) {
+                    alpha[h] = ex2(m[h] - mt);  // 0 when m = -inf
+                    m[h] = mt;
+                    resc = true;
+                }
+            }
+            float p[8];
+#pragma unroll
+            for (int h = 0; h < 8; ++h) {
+                p[h] = m[h] == -INFINITY ? 0.0f : ex2(x[h] - m[h]);
+                lp[h] = lp[h] * alpha[h] + p[h];
+            }
+            if (i > 0) {
+                // PV(i-1) done: P^T may be overwritten and O^T is stable.
+                if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&ctl->pv_done), (uint32_t)((i - 1) & 1), abort))) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                if (resc) {  // uniform across the warpgroup: every thread saw the same maxima
+                    uint32_t orow[16];
+                    tmem_ld16(tO + lane_addr, orow);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int h = 0; h < 8; ++h) orow[h] = __float_as_uint(__uint_as_float(orow[h]) * alpha[h]);
+                    tmem_st16(tO + lane_addr, orow);
+                    tmem_st_wait();
+                }
+            }
+            uint8_t* ptb = sm + OFF_PT + (t >> 6) * 2048 + (t & 7) * 2;
+#pragma unroll
+            for (int h = 0; h < 8; ++h)
+                if (h < G)
+                    *reinterpret_cast<__nv_bfloat16*>(ptb + sw128_off(h, (t & 63) >> 3)) = __float2bfloat16_rn(p[h]);
+            fence_proxy_async_smem();
+            tc_fence_before();
+            mbar_arrive(smem_u32(&ctl->p_ready));
+        }
+        named_bar_sync(2, 256);
+        if (ok) ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&ctl->o_done), 0, abort));
+        // ---- epilogue: fixed-order reduction of l, out = O / l once, LSE ----
+        float L[8];
+#pragma unroll
+        for (int h = 0; h < 8; ++h) {
+            float v = lp[h];
+#pragma unroll
+            for (int off = 16; off >= 1; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
+            if (lane == 0) ctl->lred[wq][h] = v;
+        }
+        named_bar_sync(1, 128);
+#pragma unroll
+        for (int h = 0; h < 8; ++h) L[h] = ((ctl->lred[0][h] + ctl->lred[1][h]) + ctl->lred[2][h]) + ctl->lred[3][h];
+        const bool range_bad = ctl->range_bad != 0;
+        __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(a.out);
+        if (ok) {
+            tc_fence_after();
+            uint32_t orow[16];
+            tmem_ld16(tO + lane_addr, orow);
+            tmem_ld_wait();
+#pragma unroll
+            for (int h = 0; h < 8; ++h) {
+                if (h < G) {
+                    const float o = (range_bad || !(L[h] > 0.0f)) ? 0.0f : __uint_as_float(orow[h]) / L[h];
+                    out[((size_t)b * a.Hq + h0 + h) * HEAD_DIM + t] = __float2bfloat16_rn(o);
+                }
+            }
+#pragma unroll
+            for (int h = 0; h < 8; ++h)
+                if (t == h && h < G)
+                    a.lse[(size_t)b * a.Hq + h0 + h] =
+                        range_bad ? __int_as_float(0x7fc00000)
+                                  : (L[h] > 0.0f ? (m[h] + log2f(L[h])) * 0.693147180559945309f : -INFINITY);
+            if (range_bad && t == 0 && a.status) atomicOr(a.status, RK_STATUS_RANGE);
+        } else if (t == 0 && a.status) {
+            atomicOr(a.status, RK_STATUS_TIMEOUT);
         }
     }
 
-    // ------------------------------------ fixed-order merge of 16 slots ----
-    named_bar_sync(1, DEC_CWARPS * 32);
-    if (!ok || sh->abort) {
-        if (threadIdx.x == 0 && a.status) atomicOr(a.status, RK_STATUS_TIMEOUT);
-        return;
-    }
-    float* part = reinterpret_cast<float*>(stages);  // [16][GH][128]
-    float* ml = part + 16 * GH * HEAD_DIM;           // [16][GH][2]
-#pragma unroll
-    for (int hh = 0; hh < GH; ++hh) {
-        float* dst = part + (slot * GH + hh) * HEAD_DIM;
-        *reinterpret_cast<float4*>(dst + 8 * j) = make_float4(acc[hh][0], acc[hh][1], acc[hh][2], acc[hh][3]);
-        *reinterpret_cast<float4*>(dst + 8 * j + 4) =
-            make_float4(acc[hh][4], acc[hh][5], acc[hh][6], acc[hh][7]);
-        *reinterpret_cast<float4*>(dst + 64 + 8 * j) =
-            make_float4(acc[hh][8], acc[hh][9], acc[hh][10], acc[hh][11]);
-        *reinterpret_cast<float4*>(dst + 64 + 8 * j + 4) =
-            make_float4(acc[hh][12], acc[hh][13], acc[hh][14], acc[hh][15]);
-        if (j == 0) {
-            ml[(slot * GH + hh) * 2 + 0] = m[hh];
-            ml[(slot * GH + hh) * 2 + 1] = l[hh];
-        }
-    }
-    named_bar_sync(1, DEC_CWARPS * 32);
-    const int d = threadIdx.x;  // 0..127: one output dimension per thread
-    __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(a.out);
-#pragma unroll 1
-    for (int hh = 0; hh < GH; ++hh) {
-        float M = -INFINITY;
-#pragma unroll
-        for (int sl = 0; sl < 16; ++sl) M = fmaxf(M, ml[(sl * GH + hh) * 2]);
-        float L = 0.f, O = 0.f;
-#pragma unroll
-        for (int sl = 0; sl < 16; ++sl) {
-            const float w = ex2(ml[(sl * GH + hh) * 2] - M);
-            L = fmaf(ml[(sl * GH + hh) * 2 + 1], w, L);
-            O = fmaf(part[(sl * GH + hh) * HEAD_DIM + d], w, O);
-        }
-        out[((size_t)b * a.Hq + h0 + hh) * HEAD_DIM + d] = __float2bfloat16_rn(O / L);
-        if (d == 0) a.lse[(size_t)b * a.Hq + h0 + hh] = (M + log2f(L)) * 0.693147180559945309f;
+    // ---- teardown: all roles done; no MMA or TMEM access in flight ----
+    tc_fence_before();
+    __syncthreads();
+    if (warp == WARP_MMA) {
+        tc_fence_after();
+        tmem_dealloc(tmem, TMEM_COLS);
     }
 }
 
 }  // namespace
 
-template <int GH>
-static cudaError_t launch_decode_gh(const CUtensorMap& km, const CUtensorMap& vm, const DecodeArgs& a,
-                                    cudaStream_t stream) {
+cudaError_t launch_decode(const CUtensorMap& km, const CUtensorMap& vm, const DecodeArgs& a,
+                          cudaStream_t stream) {
     static std::atomic<uint64_t> configured{0};  // one bit per device
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     const uint64_t bit = dev < 64 ? (1ull << dev) : 0;
     if (!bit || !(configured.load() & bit)) {
-        e = cudaFuncSetAttribute(decode_kernel<GH>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 DEC_SMEM_BYTES);
+        e = cudaFuncSetAttribute(decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, DEC_SMEM_BYTES);
         if (e != cudaSuccess) return e;
         configured.fetch_or(bit);
     }
-    const int grid = a.B * a.Hkv * (a.G / GH);
-    decode_kernel<GH><<<grid, DEC_THREADS, DEC_SMEM_BYTES, stream>>>(km, vm, a);
+    const long long grid = (long long)a.B * a.Hkv;
+    if (grid <= 0) return cudaSuccess;
+    if (grid > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+    decode_kernel<<<(unsigned)grid, DEC_THREADS, DEC_SMEM_BYTES, stream>>>(km, vm, a);
     return cudaGetLastError();
-}
-
-cudaError_t launch_decode(const CUtensorMap& km, const CUtensorMap& vm, const DecodeArgs& a,
-                          cudaStream_t stream) {
-    switch (a.G) {
-        case 1: return launch_decode_gh<1>(km, vm, a, stream);
-        case 2: return launch_decode_gh<2>(km, vm, a, stream);
-        default: return launch_decode_gh<4>(km, vm, a, stream);  // G = 4, or 8 as two CTAs
-    }
 }
 
 }  // namespace rk

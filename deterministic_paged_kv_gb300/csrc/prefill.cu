@@ -49,7 +49,6 @@ constexpr int KSTAGES = 3;
 constexpr int VSTAGES = 2;
 constexpr uint32_t TMEM_COLS = 512;  // S0 [0,128) S1 [128,256) O0 [256,384) O1 [384,512)
 constexpr float RESCALE_SLACK = 8.0f;
-constexpr uint32_t RANGE_LIMIT_BF16 = 0x4700u;  // bf16 bit pattern of 2^15
 
 // setmaxnreg split (sum 4 x 128 = the 512 x 128 registers the CTA launches with)
 constexpr int REG_XFORM = 104;
@@ -79,9 +78,7 @@ struct PfBars {
 static_assert(sizeof(PfBars) <= PF_CTRL_BYTES, "prefill control block exceeds its reservation");
 static_assert(PF_SMEM_BYTES <= 232448, "prefill shared memory above the 227 KiB opt-in limit");
 
-__device__ __forceinline__ uint32_t sw_off(int row, int chunk) {
-    return (uint32_t)(row * 128 + ((chunk ^ (row & 7)) << 4));
-}
+__device__ __forceinline__ uint32_t sw_off(int row, int chunk) { return sw128_off(row, chunk); }
 
 // K-major 128-byte-swizzled operand: k-step ks (16 elements) of a 128x128 tile.
 __device__ __forceinline__ uint64_t kmajor_desc(uint32_t tile, int ks) {
@@ -90,50 +87,6 @@ __device__ __forceinline__ uint64_t kmajor_desc(uint32_t tile, int ks) {
 // MN-major 128-byte-swizzled operand ([token][64 dims] blocks): k-step = 16 tokens.
 __device__ __forceinline__ uint64_t mnmajor_desc(uint32_t tile, int ks) {
     return smem_desc(tile + ks * 2048, 16384, 1024, 2);
-}
-
-// D[tmem] (+)= A[tmem] * B[smem]; A is 16-bit, two elements per 32-bit column.
-__device__ __forceinline__ void umma_ts(uint32_t d, uint32_t a_tmem, uint64_t bdesc, uint32_t idesc,
-                                        uint32_t acc) {
-    asm volatile(
-        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d),
-        "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(acc)
-        : "memory");
-}
-
-__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
-    uint32_t r;
-    asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
-    return r;
-}
-
-// Rotate one chunk pair (8 rotate-half pairs: 16 bf16 at lo_ptr / hi_ptr) and
-// write FP16 in place.  Returns the running max of the |input| bit patterns.
-__device__ __forceinline__ uint32_t rotate_chunk_f16(uint8_t* lo_ptr, uint8_t* hi_ptr, const float (&c)[8],
-                                                     const float (&s)[8], uint32_t range) {
-    const uint4 a = *reinterpret_cast<const uint4*>(lo_ptr);
-    const uint4 b = *reinterpret_cast<const uint4*>(hi_ptr);
-    const uint32_t aw[4] = {a.x, a.y, a.z, a.w};
-    const uint32_t bw[4] = {b.x, b.y, b.z, b.w};
-    uint32_t ow[4], pw[4];
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {
-        range = __vmaxu2(range, aw[k] & 0x7fff7fffu);
-        range = __vmaxu2(range, bw[k] & 0x7fff7fffu);
-        const int e0 = 2 * k, e1 = 2 * k + 1;
-        const float l0 = bf16lo(aw[k]), l1 = bf16hi(aw[k]);
-        const float u0 = bf16lo(bw[k]), u1 = bf16hi(bw[k]);
-        ow[k] = pack_f16x2(l0 * c[e0] - u0 * s[e0], l1 * c[e1] - u1 * s[e1]);
-        pw[k] = pack_f16x2(u0 * c[e0] + l0 * s[e0], u1 * c[e1] + l1 * s[e1]);
-    }
-    *reinterpret_cast<uint4*>(lo_ptr) = make_uint4(ow[0], ow[1], ow[2], ow[3]);
-    *reinterpret_cast<uint4*>(hi_ptr) = make_uint4(pw[0], pw[1], pw[2], pw[3]);
-    return range;
-}
-
-__device__ __forceinline__ bool range_exceeded(uint32_t r) {
-    return (r & 0xffffu) >= RANGE_LIMIT_BF16 || (r >> 16) >= RANGE_LIMIT_BF16;
 }
 
 struct TileInfo {

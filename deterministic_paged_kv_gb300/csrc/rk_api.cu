@@ -224,7 +224,8 @@ uint32_t rk_paged_abi_version(void) { return RK_PAGED_ABI_VERSION; }
 const char* rk_paged_policy(void) {
     return "split_kv=disabled;acc=fp32;lse=fp32,natural,scaled_scores;softmax_scale=1/sqrt(head_dim);"
            "downcast=final_write,bf16,rne;order=ascending_kv;rope=llama_rotate_half,fused_q_and_k,"
-           "rotary_dim=head_dim;gqa=contiguous_groups;decode_tile=page16,slots=16,merge=slot_order;"
+           "rotary_dim=head_dim;gqa=contiguous_groups;decode_tile=kv128,score_mma=fp16_operands_fp32_acc,"
+           "pv_mma=bf16_operands_fp32_acc,l_merge=fixed_tree;"
            "prefill_tile=2xq128xkv128,score_mma=fp16_operands_fp32_acc,pv_mma=bf16_operands_fp32_acc;"
            "batch_invariant=1;page_size=16;head_dim=128";
 }
@@ -285,11 +286,11 @@ int rk_paged_attn_decode(const rk_paged_plan_t* plan, const void* q, const void*
     if (plan->B == 0) return RK_OK;
     const bool have = plan->num_pages > 0;
     CUtensorMap km, vm;
-    if ((rc = make_cache_map(&km, have ? k_cache : q, have ? plan->num_pages : 1, have ? plan->Hkv : 1,
-                             rk::HEAD_DIM, CU_TENSOR_MAP_SWIZZLE_NONE, "k_cache")))
+    if ((rc = make_cache_map(&km, have ? k_cache : q, have ? plan->num_pages : 1, have ? plan->Hkv : 1, 64,
+                             CU_TENSOR_MAP_SWIZZLE_128B, "k_cache")))
         return rc;
-    if ((rc = make_cache_map(&vm, have ? v_cache : q, have ? plan->num_pages : 1, have ? plan->Hkv : 1,
-                             rk::HEAD_DIM, CU_TENSOR_MAP_SWIZZLE_NONE, "v_cache")))
+    if ((rc = make_cache_map(&vm, have ? v_cache : q, have ? plan->num_pages : 1, have ? plan->Hkv : 1, 64,
+                             CU_TENSOR_MAP_SWIZZLE_128B, "v_cache")))
         return rc;
     rk::DecodeArgs a;
     std::memset(&a, 0, sizeof a);

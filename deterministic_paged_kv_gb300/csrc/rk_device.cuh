@@ -239,6 +239,87 @@ __device__ __forceinline__ void tmem_st_wait() {
     asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
 
+// 32 lanes x 16 consecutive 32-bit columns.
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+        "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+          "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
+          "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+        : "r"(taddr));
+}
+
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&r)[16]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
+        "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(taddr),
+        "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
+        "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]),
+        "r"(r[15])
+        : "memory");
+}
+
+// D[tmem] (+)= A[tmem] * B[smem]; A is 16-bit, two elements per 32-bit column.
+__device__ __forceinline__ void umma_ts(uint32_t d, uint32_t a_tmem, uint64_t bdesc, uint32_t idesc,
+                                        uint32_t acc) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d),
+        "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(acc)
+        : "memory");
+}
+
+// Instruction descriptor for kind::f16 with FP16 A and B, FP32 D, both K-major.
+__host__ __device__ constexpr uint32_t idesc_f16_f32(int M, int N) {
+    return (1u << 4) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+
+// Two floats -> packed f16x2, round-to-nearest-even (lo in the low half).
+__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
+    uint32_t r;
+    asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+
+// 128-byte swizzle: byte offset of 16-byte chunk `chunk` (0..7) of 128-byte row `row`
+// inside a 1024-byte aligned swizzle atom sequence.
+__device__ __forceinline__ uint32_t sw128_off(int row, int chunk) {
+    return (uint32_t)(row * 128 + ((chunk ^ (row & 7)) << 4));
+}
+
+// Rotate one chunk pair (8 rotate-half pairs: 16 bf16 at lo_ptr / hi_ptr) in FP32
+// and write FP16 in place.  Returns the running max of the |input| bf16 bit
+// patterns (for the FP16 range check).
+__device__ __forceinline__ uint32_t rotate_chunk_f16(uint8_t* lo_ptr, uint8_t* hi_ptr, const float (&c)[8],
+                                                     const float (&s)[8], uint32_t range) {
+    const uint4 a = *reinterpret_cast<const uint4*>(lo_ptr);
+    const uint4 b = *reinterpret_cast<const uint4*>(hi_ptr);
+    const uint32_t aw[4] = {a.x, a.y, a.z, a.w};
+    const uint32_t bw[4] = {b.x, b.y, b.z, b.w};
+    uint32_t ow[4], pw[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        range = __vmaxu2(range, aw[k] & 0x7fff7fffu);
+        range = __vmaxu2(range, bw[k] & 0x7fff7fffu);
+        const int e0 = 2 * k, e1 = 2 * k + 1;
+        const float l0 = bf16lo(aw[k]), l1 = bf16hi(aw[k]);
+        const float u0 = bf16lo(bw[k]), u1 = bf16hi(bw[k]);
+        ow[k] = pack_f16x2(l0 * c[e0] - u0 * s[e0], l1 * c[e1] - u1 * s[e1]);
+        pw[k] = pack_f16x2(u0 * c[e0] + l0 * s[e0], u1 * c[e1] + l1 * s[e1]);
+    }
+    *reinterpret_cast<uint4*>(lo_ptr) = make_uint4(ow[0], ow[1], ow[2], ow[3]);
+    *reinterpret_cast<uint4*>(hi_ptr) = make_uint4(pw[0], pw[1], pw[2], pw[3]);
+    return range;
+}
+
+// bf16 bit pattern of 2^15: pre-RoPE inputs at or above it may overflow FP16
+// once rotated (|rotated| <= sqrt(2) * max |input|).
+constexpr uint32_t RANGE_LIMIT_BF16 = 0x4700u;
+__device__ __forceinline__ bool range_exceeded(uint32_t r) {
+    return (r & 0xffffu) >= RANGE_LIMIT_BF16 || (r >> 16) >= RANGE_LIMIT_BF16;
+}
+
 // -------------------------------------------------------------- RoPE -----
 
 // cos / sin of the rotation angle of one pair at integer position t.

@@ -13,17 +13,16 @@ constexpr int PAGE = 16;
 constexpr int ROPE_PAIRS = HEAD_DIM / 2;
 
 // ------------------------------------------------------------ decode ----
-// One CTA per (row, KV head, group of up to 4 query heads).  Four consumer
-// warps; warp w, lane group g (8 lanes) owns token slot 4w+g of every page.
-constexpr int DEC_CWARPS = 4;
-constexpr int DEC_THREADS = (DEC_CWARPS + 1) * 32;  // + one TMA producer warp
-constexpr int DEC_STAGES = 8;                        // pages in flight per CTA
-constexpr int DEC_PAGE_BYTES = PAGE * HEAD_DIM * 2;  // one head of one page: 4 KiB
-constexpr int DEC_STAGE_BYTES = 2 * DEC_PAGE_BYTES;  // K + V
-constexpr int DEC_REANCHOR = 16;                     // exact RoPE angles every 16 pages
-constexpr float DEC_RESCALE_THRESHOLD = 8.0f;        // log2-domain max slack
-constexpr int DEC_CTRL_BYTES = 2048;                   // barriers, RoPE tables, flags
-constexpr int DEC_SMEM_BYTES = DEC_STAGES * DEC_STAGE_BYTES + DEC_CTRL_BYTES;
+// One CTA per (row, KV head): transform warpgroup, softmax warpgroup, K and V
+// TMA producer warps and one MMA warp (11 warps).  Tiles of 128 tokens.
+constexpr int DEC_THREADS = 11 * 32;
+constexpr int DEC_BN = 128;                           // tokens per KV tile (8 pages)
+constexpr int DEC_KSTAGES = 3;
+constexpr int DEC_VSTAGES = 2;
+constexpr int DEC_TILE_BYTES = DEC_BN * HEAD_DIM * 2;  // 32 KiB
+constexpr int DEC_CTRL_BYTES = 2048;                   // barriers, RoPE tables, reductions
+constexpr int DEC_SMEM_BYTES = (DEC_KSTAGES + DEC_VSTAGES) * DEC_TILE_BYTES + 16 * HEAD_DIM * 2 +
+                               16 * DEC_BN * 2 + DEC_CTRL_BYTES;
 
 struct DecodeArgs {
     const void* q;                // bf16 [B, Hq, 1, D]

@@ -173,3 +173,28 @@ def test_decode_launch_does_not_synchronize():
     finally:
         torch.cuda.set_sync_debug_mode("default")
     torch.cuda.synchronize()
+
+
+def test_decode_range_guard_flags_instead_of_overflowing():
+    """A pre-RoPE key element of 40000 (beyond the FP16 score-operand range once
+    rotated): that (row, KV head)'s heads get zeros and NaN LSE and the status
+    bit is set; all other outputs still match the oracle."""
+    w = workloads.random_case(2, 1, 32, 8, 128, [60, 90], seed=43, mode="decode")
+    page = int(w.block_table[1, 2])
+    w.k_cache[page, 5, 3, 7] = -40000.0
+    d = to_dev(w)
+    p = binding.plan(2, 1, 32, 8, 128, 16, w.num_pages, w.W)
+    out = torch.empty_like(d["q"])
+    lse = torch.empty((2, 32, 1), dtype=torch.float32, device="cuda")
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    binding.attn_decode(p, d["q"], d["k_cache"], d["v_cache"], d["block_table"], d["kv_lens"],
+                        d["position_ids"], out, lse, status=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == binding.STATUS_RANGE
+    assert torch.all(out[1, 12:16] == 0) and torch.all(torch.isnan(lse[1, 12:16]))
+    ro, rl = oracle_ref(w)
+    keep = np.ones((2, 32), bool)
+    keep[1, 12:16] = False
+    o = out.float().cpu().numpy()[keep]
+    l_ = lse.cpu().numpy()[keep]
+    assert np.max(np.abs(o - ro[keep])) <= 2e-2 and np.max(np.abs(l_ - rl[keep])) <= 1e-3
