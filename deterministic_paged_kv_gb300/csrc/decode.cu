@@ -10,17 +10,17 @@
 // One CTA per (row b, KV head); all G = Hq/Hkv query heads of the group are
 // served by one pass over the row's pages (GQA packing: every K/V byte is
 // read once).  The row's tokens are swept in ascending tiles of 128 (8 pages):
-//   warps 8 / 10  TMA producers: K pages (3-stage ring) and V pages (2-stage
+//   warps 12 / 14 TMA producers: K pages (3-stage ring) and V pages (2-stage
 //                 ring) as 16-token x 64-dim boxes with 128-byte swizzle, i.e.
 //                 already in the UMMA operand layout; the V producer zeroes
 //                 cache rows past kv_len in a partial last page;
-//   warps 0-3     transform: rotate each K row in FP32 (angles from an exact
-//                 fixed-point anchor plus 16-position steps) and store it as
+//   warps 0-7     transform: rotate each K row in FP32 (angles from an exact
+//                 fixed-point anchor plus 32-position steps) and store it as
 //                 FP16 in place; rotate the G query rows once (FP16 Q^T);
-//   warp 9        MMA issuer: S^T = K Q^T (M = 128 tokens, N = 16 >= G heads,
+//   warp 13       MMA issuer: S^T = K Q^T (M = 128 tokens, N = 16 >= G heads,
 //                 FP16 operands, FP32 in TMEM, double-buffered) and
 //                 O^T += V^T P^T (M = 128 dims, N = 16, BF16, FP32 in TMEM);
-//   warps 4-7     softmax: thread t owns token t of the tile: masks, takes the
+//   warps 8-11    softmax: thread t owns token t of the tile: masks, takes the
 //                 tile max per head over the 128 tokens (xor-butterfly + fixed
 //                 warp order), moves the running max only when it grows by
 //                 more than 8 (log2 domain; then the O^T column is rescaled in
@@ -41,9 +41,12 @@ namespace rk {
 
 namespace {
 
-constexpr int WARP_TMA_K = 8;
-constexpr int WARP_MMA = 9;
-constexpr int WARP_TMA_V = 10;
+constexpr int WARP_SOFTMAX0 = DEC_XFORM_THREADS / 32;  // warps 8-11
+constexpr int WARP_TMA_K = WARP_SOFTMAX0 + 4;
+constexpr int WARP_MMA = WARP_TMA_K + 1;
+constexpr int WARP_TMA_V = WARP_TMA_K + 2;
+constexpr int XF_ROW_STEP = DEC_XFORM_THREADS / 8;      // rows between a thread's K rows
+constexpr int XF_ROWS = DEC_BN / XF_ROW_STEP;           // K rows per transform thread per tile
 constexpr uint32_t TMEM_COLS = 64;  // S^T buffers [0,16) [16,32), O^T [32,48)
 constexpr float RESCALE_SLACK = 8.0f;
 constexpr int NH = 16;  // N of both MMAs: query heads of the group, zero padded
@@ -65,7 +68,7 @@ struct DecCtrl {
     int abort;
     int range_bad;
     uint64_t turns[ROPE_PAIRS];
-    float2 step16[ROPE_PAIRS];
+    float2 step[ROPE_PAIRS];  // cos/sin of an XF_ROW_STEP-position turn per pair
     float red[2][4][8];  // per-warp tile maxima, double-buffered by tile parity
     float lred[4][8];    // per-warp partial l at the end
 };
@@ -115,10 +118,10 @@ __global__ void __launch_bounds__(DEC_THREADS, 1)
     if (tid == 0) {
         ctl->abort = 0;
         ctl->range_bad = 0;
-        mbar_init(smem_u32(&ctl->q_ready), 128);
+        mbar_init(smem_u32(&ctl->q_ready), DEC_XFORM_THREADS);
         for (int k = 0; k < DEC_KSTAGES; ++k) {
             mbar_init(smem_u32(&ctl->k_full[k]), 1);
-            mbar_init(smem_u32(&ctl->k_ready[k]), 128);
+            mbar_init(smem_u32(&ctl->k_ready[k]), DEC_XFORM_THREADS);
             mbar_init(smem_u32(&ctl->k_empty[k]), 1);
         }
         for (int k = 0; k < DEC_VSTAGES; ++k) {
@@ -140,8 +143,8 @@ __global__ void __launch_bounds__(DEC_THREADS, 1)
     if (tid < ROPE_PAIRS) {
         ctl->turns[tid] = a.rope_turns[tid];
         float c, s;
-        rope_cos_sin((uint32_t)PAGE, a.rope_turns[tid], c, s);
-        ctl->step16[tid] = make_float2(c, s);
+        rope_cos_sin((uint32_t)XF_ROW_STEP, a.rope_turns[tid], c, s);
+        ctl->step[tid] = make_float2(c, s);
     }
     // V stages, Q^T and P^T start as zeros (rows never written stay finite).
     for (int i = tid; i < (OFF_CTRL - OFF_V) / 16; i += DEC_THREADS)
@@ -232,40 +235,58 @@ __global__ void __launch_bounds__(DEC_THREADS, 1)
             const uint32_t idO = idesc_bf16_f32(HEAD_DIM, NH, 1, 0);
             const uint32_t qt = s_base + OFF_QT, pt = s_base + OFF_PT;
             bool ok = mbar_wait(smem_u32(&ctl->q_ready), 0, abort);
-            auto issue_pv = [&](int i) -> bool {
-                if (!mbar_wait(smem_u32(&ctl->p_ready), (uint32_t)(i & 1), abort)) return false;
-                if (!mbar_wait(smem_u32(&ctl->v_full[i % DEC_VSTAGES]), (uint32_t)((i / DEC_VSTAGES) & 1), abort))
-                    return false;
-                if (has_tail && i == n_tiles - 1 && !mbar_wait(smem_u32(&ctl->v_tail), 0, abort)) return false;
-                tc_fence_after();
-                const uint32_t vt = s_base + OFF_V + (i % DEC_VSTAGES) * DEC_TILE_BYTES;
+            // Event-driven issue: the next score MMA and the next PV MMA are
+            // started as soon as their own inputs are ready, so neither waits
+            // behind the other's producer (MMAs still retire in issue order).
+            int next_s = 0, next_pv = 0;
+            uint64_t idle_since = global_timer_ns();
+            while (ok && next_pv < n_tiles) {
+                bool progressed = false;
+                if (next_s < n_tiles) {
+                    const int i = next_s, k = i % DEC_KSTAGES, sb = i & 1;
+                    if (mbar_test(smem_u32(&ctl->k_ready[k]), (uint32_t)((i / DEC_KSTAGES) & 1)) &&
+                        (i < 2 || mbar_test(smem_u32(&ctl->s_free[sb]), (uint32_t)(((i >> 1) - 1) & 1)))) {
+                        tc_fence_after();
+                        const uint32_t kt = s_base + OFF_K + k * DEC_TILE_BYTES;
 #pragma unroll 1
-                for (int ks = 0; ks < 8; ++ks)
-                    umma_ss(tO, smem_desc(vt + ks * 2048, 16384, 1024, 2),
-                            smem_desc(pt + (ks >> 2) * 2048 + (ks & 3) * 32, 16, 1024, 2), idO,
-                            (i > 0 || ks > 0) ? 1u : 0u);
-                umma_commit(smem_u32(&ctl->pv_done));
-                umma_commit(smem_u32(&ctl->v_empty[i % DEC_VSTAGES]));
-                return true;
-            };
-            for (int i = 0; i < n_tiles && ok; ++i) {
-                const int k = i % DEC_KSTAGES, sb = i & 1;
-                if (!(ok = mbar_wait(smem_u32(&ctl->k_ready[k]), (uint32_t)((i / DEC_KSTAGES) & 1), abort))) break;
-                if (i >= 2 &&
-                    !(ok = mbar_wait(smem_u32(&ctl->s_free[sb]), (uint32_t)(((i >> 1) - 1) & 1), abort)))
-                    break;
-                tc_fence_after();
-                const uint32_t kt = s_base + OFF_K + k * DEC_TILE_BYTES;
+                        for (int ks = 0; ks < 8; ++ks)
+                            umma_ss(tmem + sb * NH, smem_desc(kt + (ks >> 2) * 16384 + (ks & 3) * 32, 16, 1024, 2),
+                                    smem_desc(qt + (ks >> 2) * 2048 + (ks & 3) * 32, 16, 1024, 2), idS,
+                                    ks > 0 ? 1u : 0u);
+                        umma_commit(smem_u32(&ctl->s_full[sb]));
+                        umma_commit(smem_u32(&ctl->k_empty[k]));
+                        ++next_s;
+                        progressed = true;
+                    }
+                }
+                if (next_pv < next_s) {
+                    const int i = next_pv;
+                    if (mbar_test(smem_u32(&ctl->p_ready), (uint32_t)(i & 1)) &&
+                        mbar_test(smem_u32(&ctl->v_full[i % DEC_VSTAGES]), (uint32_t)((i / DEC_VSTAGES) & 1)) &&
+                        (!(has_tail && i == n_tiles - 1) || mbar_test(smem_u32(&ctl->v_tail), 0))) {
+                        tc_fence_after();
+                        const uint32_t vt = s_base + OFF_V + (i % DEC_VSTAGES) * DEC_TILE_BYTES;
 #pragma unroll 1
-                for (int ks = 0; ks < 8; ++ks)
-                    umma_ss(tmem + sb * NH, smem_desc(kt + (ks >> 2) * 16384 + (ks & 3) * 32, 16, 1024, 2),
-                            smem_desc(qt + (ks >> 2) * 2048 + (ks & 3) * 32, 16, 1024, 2), idS,
-                            ks > 0 ? 1u : 0u);
-                umma_commit(smem_u32(&ctl->s_full[sb]));
-                umma_commit(smem_u32(&ctl->k_empty[k]));
-                if (i >= 1 && !(ok = issue_pv(i - 1))) break;
+                        for (int ks = 0; ks < 8; ++ks)
+                            umma_ss(tO, smem_desc(vt + ks * 2048, 16384, 1024, 2),
+                                    smem_desc(pt + (ks >> 2) * 2048 + (ks & 3) * 32, 16, 1024, 2), idO,
+                                    (i > 0 || ks > 0) ? 1u : 0u);
+                        umma_commit(smem_u32(&ctl->pv_done));
+                        umma_commit(smem_u32(&ctl->v_empty[i % DEC_VSTAGES]));
+                        ++next_pv;
+                        progressed = true;
+                    }
+                }
+                if (progressed) {
+                    idle_since = global_timer_ns();
+                } else if (*abort) {
+                    ok = false;
+                } else if (global_timer_ns() - idle_since > RK_WAIT_LIMIT_NS) {
+                    *abort = 1;
+                    ok = false;
+                }
             }
-            if (ok && (ok = issue_pv(n_tiles - 1))) umma_commit(smem_u32(&ctl->o_done));
+            if (ok) umma_commit(smem_u32(&ctl->o_done));
             if (!ok) {
                 const uint64_t t0 = global_timer_ns();  // let issued MMAs drain before TMEM is released
                 while (global_timer_ns() - t0 < 1000000ull) {
@@ -273,8 +294,8 @@ __global__ void __launch_bounds__(DEC_THREADS, 1)
             }
         }
         __syncwarp();
-    } else if (warp < 4) {
-        // ============================================== transform WG ====
+    } else if (warp < WARP_SOFTMAX0) {
+        // ============================================= transform WGs ====
         uint32_t range = 0;
         {
             // Q^T: thread (h, u) rotates chunk pair u of query head h at qpos.
@@ -285,9 +306,12 @@ __global__ void __launch_bounds__(DEC_THREADS, 1)
                 __align__(16) uint8_t tmp[32];
                 *reinterpret_cast<uint4*>(tmp) = __ldg(row + u);
                 *reinterpret_cast<uint4*>(tmp + 16) = __ldg(row + 8 + u);
-                float c[8], sn[8];
+                float2 c[4], sn[4];
 #pragma unroll
-                for (int e = 0; e < 8; ++e) rope_cos_sin((uint32_t)qpos, ctl->turns[8 * u + e], c[e], sn[e]);
+                for (int e = 0; e < 4; ++e) {
+                    rope_cos_sin((uint32_t)qpos, ctl->turns[8 * u + 2 * e], c[e].x, sn[e].x);
+                    rope_cos_sin((uint32_t)qpos, ctl->turns[8 * u + 2 * e + 1], c[e].y, sn[e].y);
+                }
                 range = rotate_chunk_f16(tmp, tmp + 16, c, sn, range);
                 const uint32_t off = sw128_off(h, u);
                 *reinterpret_cast<uint4*>(sm + OFF_QT + off) = *reinterpret_cast<const uint4*>(tmp);
@@ -297,43 +321,40 @@ __global__ void __launch_bounds__(DEC_THREADS, 1)
             fence_proxy_async_smem();
             mbar_arrive(smem_u32(&ctl->q_ready));
         }
-        const int u = tid & 7, r0 = tid >> 3;
-        float dcs[8], dsn[8];
+        const int u = tid & 7, r0 = tid >> 3;  // rows r0 + XF_ROW_STEP * m
+        float2 dcs[4], dsn[4];
 #pragma unroll
-        for (int e = 0; e < 8; ++e) {
-            const float2 st = ctl->step16[8 * u + e];
-            dcs[e] = st.x;
-            dsn[e] = st.y;
+        for (int e = 0; e < 4; ++e) {
+            const float2 s0 = ctl->step[8 * u + 2 * e], s1 = ctl->step[8 * u + 2 * e + 1];
+            dcs[e] = make_float2(s0.x, s1.x);
+            dsn[e] = make_float2(s0.y, s1.y);
         }
         for (int i = 0; i < n_tiles; ++i) {
             const int k = i % DEC_KSTAGES;
             if (!mbar_wait(smem_u32(&ctl->k_full[k]), (uint32_t)((i / DEC_KSTAGES) & 1), abort)) break;
             uint8_t* kt = sm + OFF_K + k * DEC_TILE_BYTES;
             const int t0 = i * DEC_BN;
-            float c[8], sn[8];
+            float2 c[4], sn[4];
 #pragma unroll
-            for (int e = 0; e < 8; ++e) rope_cos_sin((uint32_t)(t0 + r0), ctl->turns[8 * u + e], c[e], sn[e]);
+            for (int e = 0; e < 4; ++e) {
+                rope_cos_sin((uint32_t)(t0 + r0), ctl->turns[8 * u + 2 * e], c[e].x, sn[e].x);
+                rope_cos_sin((uint32_t)(t0 + r0), ctl->turns[8 * u + 2 * e + 1], c[e].y, sn[e].y);
+            }
 #pragma unroll 2
-            for (int m = 0; m < 8; ++m) {
-                const int r = r0 + 16 * m;
+            for (int m = 0; m < XF_ROWS; ++m) {
+                const int r = r0 + XF_ROW_STEP * m;
                 const uint32_t off = sw128_off(r, u);
                 if (t0 + r < n_vis) range = rotate_chunk_f16(kt + off, kt + 16384 + off, c, sn, range);
-#pragma unroll
-                for (int e = 0; e < 8; ++e) {
-                    const float cn = c[e] * dcs[e] - sn[e] * dsn[e];
-                    const float snn = sn[e] * dcs[e] + c[e] * dsn[e];
-                    c[e] = cn;
-                    sn[e] = snn;
-                }
+                rope_step(c, sn, dcs, dsn);
             }
             if (range_exceeded(range)) ctl->range_bad = 1;
             fence_proxy_async_smem();
             mbar_arrive(smem_u32(&ctl->k_ready[k]));
         }
-        named_bar_sync(2, 256);  // transform done: the range flag is final for the epilogue
-    } else if (warp < 8) {
+        named_bar_sync(2, DEC_XFORM_THREADS + 128);  // transform done: the range flag is final
+    } else if (warp < WARP_SOFTMAX0 + 4) {
         // =============================================== softmax WG ====
-        const int t = tid - 128;  // token of the tile == TMEM lane (S^T rows) == output dim (O^T rows)
+        const int t = tid - DEC_XFORM_THREADS;  // token of the tile == TMEM lane (S^T rows) == output dim (O^T rows)
         const int wq = warp & 3;
         const uint32_t lane_addr = (uint32_t)(wq * 32) << 16;
         const float scl = a.qk_scale_log2;
@@ -419,7 +440,7 @@ __global__ void __launch_bounds__(DEC_THREADS, 1)
             tc_fence_before();
             mbar_arrive(smem_u32(&ctl->p_ready));
         }
-        named_bar_sync(2, 256);
+        named_bar_sync(2, DEC_XFORM_THREADS + 128);
         if (ok) ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&ctl->o_done), 0, abort));
         // ---- epilogue: fixed-order reduction of l, out = O / l once, LSE ----
         float L[8];

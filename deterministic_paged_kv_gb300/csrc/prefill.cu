@@ -358,9 +358,12 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
                 uint8_t* qt = sm + OFF_Q + j * PF_TILE_BYTES;
 #pragma unroll 1
                 for (int u = 0; u < 8; ++u) {
-                    float c[8], sn[8];
+                    float2 c[4], sn[4];
 #pragma unroll
-                    for (int e = 0; e < 8; ++e) rope_cos_sin((uint32_t)p, bars->turns[8 * u + e], c[e], sn[e]);
+                    for (int e = 0; e < 4; ++e) {
+                        rope_cos_sin((uint32_t)p, bars->turns[8 * u + 2 * e], c[e].x, sn[e].x);
+                        rope_cos_sin((uint32_t)p, bars->turns[8 * u + 2 * e + 1], c[e].y, sn[e].y);
+                    }
                     const uint32_t off = sw_off(r, u);
                     range = rotate_chunk_f16(qt + off, qt + 16384 + off, c, sn, range);
                 }
@@ -371,33 +374,30 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
         }
         // K tiles: thread handles pair-chunk u = tid % 8 of rows r0 + 16 m.
         const int u = tid & 7, r0 = tid >> 3;
-        float dcs[8], dsn[8];
+        float2 dcs[4], dsn[4];
 #pragma unroll
-        for (int e = 0; e < 8; ++e) {
-            const float2 st = bars->step16[8 * u + e];
-            dcs[e] = st.x;
-            dsn[e] = st.y;
+        for (int e = 0; e < 4; ++e) {
+            const float2 s0 = bars->step16[8 * u + 2 * e], s1 = bars->step16[8 * u + 2 * e + 1];
+            dcs[e] = make_float2(s0.x, s1.x);
+            dsn[e] = make_float2(s0.y, s1.y);
         }
         for (int i = 0; i < n_tiles; ++i) {
             const int k = i % KSTAGES;
             if (!mbar_wait(smem_u32(&bars->k_full[k]), (uint32_t)((i / KSTAGES) & 1), abort)) break;
             uint8_t* kt = sm + OFF_K + k * PF_TILE_BYTES;
             const int t0 = i * PF_BN;
-            float c[8], sn[8];
+            float2 c[4], sn[4];
 #pragma unroll
-            for (int e = 0; e < 8; ++e) rope_cos_sin((uint32_t)(t0 + r0), bars->turns[8 * u + e], c[e], sn[e]);
+            for (int e = 0; e < 4; ++e) {
+                rope_cos_sin((uint32_t)(t0 + r0), bars->turns[8 * u + 2 * e], c[e].x, sn[e].x);
+                rope_cos_sin((uint32_t)(t0 + r0), bars->turns[8 * u + 2 * e + 1], c[e].y, sn[e].y);
+            }
 #pragma unroll 2
             for (int m = 0; m < 8; ++m) {
                 const int r = r0 + 16 * m;
                 const uint32_t off = sw_off(r, u);
                 if (t0 + r < n_keys) range = rotate_chunk_f16(kt + off, kt + 16384 + off, c, sn, range);
-#pragma unroll
-                for (int e = 0; e < 8; ++e) {
-                    const float cn = c[e] * dcs[e] - sn[e] * dsn[e];
-                    const float snn = sn[e] * dcs[e] + c[e] * dsn[e];
-                    c[e] = cn;
-                    sn[e] = snn;
-                }
+                rope_step(c, sn, dcs, dsn);
             }
             if (range_exceeded(range)) bars->range_bad = 1;
             fence_proxy_async_smem();

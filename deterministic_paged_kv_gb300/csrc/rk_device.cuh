@@ -72,6 +72,19 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
     return ok != 0;
 }
 
+// Non-blocking test of whether phase `parity` of an mbarrier has completed.
+__device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
 // Wait for phase `parity` of an mbarrier to complete.  Gives up (returns
 // false) after RK_WAIT_LIMIT_NS of wall time or as soon as *abort is set by
 // another warp, so that a pipeline that lost a participant cannot hang.
@@ -288,11 +301,31 @@ __device__ __forceinline__ uint32_t sw128_off(int row, int chunk) {
     return (uint32_t)(row * 128 + ((chunk ^ (row & 7)) << 4));
 }
 
+// Packed FP32 pair arithmetic (sm_100+): two lanes of a*b+c / a*b in one instruction.
+__device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) {
+    float2 d;
+    asm("{\n\t.reg .b64 ra, rb, rc, rd;\n\t"
+        "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\tmov.b64 rc, {%6, %7};\n\t"
+        "fma.rn.f32x2 rd, ra, rb, rc;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+        : "=f"(d.x), "=f"(d.y)
+        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y));
+    return d;
+}
+__device__ __forceinline__ float2 fmul2(float2 a, float2 b) {
+    float2 d;
+    asm("{\n\t.reg .b64 ra, rb, rd;\n\t"
+        "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t"
+        "mul.rn.f32x2 rd, ra, rb;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+        : "=f"(d.x), "=f"(d.y)
+        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+    return d;
+}
+
 // Rotate one chunk pair (8 rotate-half pairs: 16 bf16 at lo_ptr / hi_ptr) in FP32
-// and write FP16 in place.  Returns the running max of the |input| bf16 bit
-// patterns (for the FP16 range check).
-__device__ __forceinline__ uint32_t rotate_chunk_f16(uint8_t* lo_ptr, uint8_t* hi_ptr, const float (&c)[8],
-                                                     const float (&s)[8], uint32_t range) {
+// and write FP16 in place.  c2 / s2 hold the cos / sin of pairs (2k, 2k+1).
+// Returns the running max of the |input| bf16 bit patterns (FP16 range check).
+__device__ __forceinline__ uint32_t rotate_chunk_f16(uint8_t* lo_ptr, uint8_t* hi_ptr, const float2 (&c2)[4],
+                                                     const float2 (&s2)[4], uint32_t range) {
     const uint4 a = *reinterpret_cast<const uint4*>(lo_ptr);
     const uint4 b = *reinterpret_cast<const uint4*>(hi_ptr);
     const uint32_t aw[4] = {a.x, a.y, a.z, a.w};
@@ -302,15 +335,31 @@ __device__ __forceinline__ uint32_t rotate_chunk_f16(uint8_t* lo_ptr, uint8_t* h
     for (int k = 0; k < 4; ++k) {
         range = __vmaxu2(range, aw[k] & 0x7fff7fffu);
         range = __vmaxu2(range, bw[k] & 0x7fff7fffu);
-        const int e0 = 2 * k, e1 = 2 * k + 1;
-        const float l0 = bf16lo(aw[k]), l1 = bf16hi(aw[k]);
-        const float u0 = bf16lo(bw[k]), u1 = bf16hi(bw[k]);
-        ow[k] = pack_f16x2(l0 * c[e0] - u0 * s[e0], l1 * c[e1] - u1 * s[e1]);
-        pw[k] = pack_f16x2(u0 * c[e0] + l0 * s[e0], u1 * c[e1] + l1 * s[e1]);
+        const float2 lo = make_float2(bf16lo(aw[k]), bf16hi(aw[k]));
+        const float2 hi = make_float2(bf16lo(bw[k]), bf16hi(bw[k]));
+        const float2 nhi = make_float2(-hi.x, -hi.y);
+        const float2 x = ffma2(nhi, s2[k], fmul2(lo, c2[k]));  // lo*c - hi*s
+        const float2 y = ffma2(lo, s2[k], fmul2(hi, c2[k]));   // hi*c + lo*s
+        ow[k] = pack_f16x2(x.x, x.y);
+        pw[k] = pack_f16x2(y.x, y.y);
     }
     *reinterpret_cast<uint4*>(lo_ptr) = make_uint4(ow[0], ow[1], ow[2], ow[3]);
     *reinterpret_cast<uint4*>(hi_ptr) = make_uint4(pw[0], pw[1], pw[2], pw[3]);
     return range;
+}
+
+// Advance 8 pairs' (cos, sin) by a fixed angle step (cos, sin) = (dc, ds):
+// c' = c dc - s ds, s' = s dc + c ds.
+__device__ __forceinline__ void rope_step(float2 (&c2)[4], float2 (&s2)[4], const float2 (&dc2)[4],
+                                          const float2 (&ds2)[4]) {
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        const float2 ns = make_float2(-s2[k].x, -s2[k].y);
+        const float2 cn = ffma2(ns, ds2[k], fmul2(c2[k], dc2[k]));
+        const float2 sn = ffma2(c2[k], ds2[k], fmul2(s2[k], dc2[k]));
+        c2[k] = cn;
+        s2[k] = sn;
+    }
 }
 
 // bf16 bit pattern of 2^15: pre-RoPE inputs at or above it may overflow FP16

@@ -13,11 +13,13 @@ constexpr int PAGE = 16;
 constexpr int ROPE_PAIRS = HEAD_DIM / 2;
 
 // ------------------------------------------------------------ decode ----
-// One CTA per (row, KV head): transform warpgroup, softmax warpgroup, K and V
-// TMA producer warps and one MMA warp (11 warps).  Tiles of 128 tokens.
-constexpr int DEC_THREADS = 11 * 32;
+// One CTA per (row, KV head): two transform warpgroups, one softmax
+// warpgroup, K and V TMA producer warps and one MMA warp (15 warps).  Tiles
+// of 128 tokens.
+constexpr int DEC_XFORM_THREADS = 256;
+constexpr int DEC_THREADS = 15 * 32;
 constexpr int DEC_BN = 128;                           // tokens per KV tile (8 pages)
-constexpr int DEC_KSTAGES = 3;
+constexpr int DEC_KSTAGES = 4;
 constexpr int DEC_VSTAGES = 2;
 constexpr int DEC_TILE_BYTES = DEC_BN * HEAD_DIM * 2;  // 32 KiB
 constexpr int DEC_CTRL_BYTES = 2048;                   // barriers, RoPE tables, reductions
