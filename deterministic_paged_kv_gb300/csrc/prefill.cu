@@ -432,13 +432,21 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
                 tmem_ld32(tS + lane_addr + c4 * 32, *reinterpret_cast<uint32_t(*)[32]>(&xr[c4 * 32]));
             tmem_ld_wait();
             const int lim = n_vis - i * PF_BN;  // columns < lim are visible
-            float mt = -INFINITY;
+            // Mask only where some row of the warp ends inside this tile.
+            if (__any_sync(0xffffffffu, lim < PF_BN)) {
 #pragma unroll
-            for (int c = 0; c < 128; ++c) {
-                const float v = c < lim ? __uint_as_float(xr[c]) * scl : -INFINITY;
-                xr[c] = __float_as_uint(v);
-                mt = fmaxf(mt, v);
+                for (int c = 0; c < 128; ++c) xr[c] = c < lim ? xr[c] : 0xff800000u;  // -inf
             }
+            // Row max on the raw scores (scale > 0 commutes with max), 4 chains.
+            float mx0 = -INFINITY, mx1 = -INFINITY, mx2 = -INFINITY, mx3 = -INFINITY;
+#pragma unroll
+            for (int c = 0; c < 128; c += 4) {
+                mx0 = fmaxf(mx0, __uint_as_float(xr[c]));
+                mx1 = fmaxf(mx1, __uint_as_float(xr[c + 1]));
+                mx2 = fmaxf(mx2, __uint_as_float(xr[c + 2]));
+                mx3 = fmaxf(mx3, __uint_as_float(xr[c + 3]));
+            }
+            const float mt = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * scl;
             float alpha = 1.0f;
             bool resc = false;
             if (mt > m + RESCALE_SLACK) {
@@ -446,17 +454,21 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
                 m = mt;
                 resc = true;
             }
-            const bool none = (m == -INFINITY);
-            float rs = 0.0f;
+            // p = 2^(x * scale - m): one packed FMA per pair, packed row sum.  A row
+            // with nothing visible yet (m = -inf, every x = -inf) gives 2^-inf = 0.
+            const float nm = (m == -INFINITY) ? 0.0f : -m;
+            const float2 sc2 = make_float2(scl, scl), nm2 = make_float2(nm, nm);
+            float2 acc2 = make_float2(0.0f, 0.0f);
             // P packed as BF16 pairs into xr[0..63] (each slot is rewritten only
             // after both of its sources have been read).
 #pragma unroll
             for (int c = 0; c < 128; c += 2) {
-                const float e0 = none ? 0.0f : ex2(__uint_as_float(xr[c]) - m);
-                const float e1 = none ? 0.0f : ex2(__uint_as_float(xr[c + 1]) - m);
-                rs += e0 + e1;
-                xr[c >> 1] = pack_bf16x2(e0, e1);
+                const float2 t = ffma2(make_float2(__uint_as_float(xr[c]), __uint_as_float(xr[c + 1])), sc2, nm2);
+                const float2 e = make_float2(ex2(t.x), ex2(t.y));
+                acc2 = fadd2(acc2, e);
+                xr[c >> 1] = pack_bf16x2(e.x, e.y);
             }
+            const float rs = acc2.x + acc2.y;
             l = l * alpha + rs;
             // S_j(i) complete implies PV_j(i-1) complete (MMAs of one issuer
             // retire in order), so O_j is stable and S_j's columns may take P_j(i).

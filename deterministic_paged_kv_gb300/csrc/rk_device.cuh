@@ -321,6 +321,16 @@ __device__ __forceinline__ float2 fmul2(float2 a, float2 b) {
     return d;
 }
 
+__device__ __forceinline__ float2 fadd2(float2 a, float2 b) {
+    float2 d;
+    asm("{\n\t.reg .b64 ra, rb, rd;\n\t"
+        "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t"
+        "add.rn.f32x2 rd, ra, rb;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+        : "=f"(d.x), "=f"(d.y)
+        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+    return d;
+}
+
 // Rotate one chunk pair (8 rotate-half pairs: 16 bf16 at lo_ptr / hi_ptr) in FP32
 // and write FP16 in place.  c2 / s2 hold the cos / sin of pairs (2k, 2k+1).
 // Returns the running max of the |input| bf16 bit patterns (FP16 range check).
