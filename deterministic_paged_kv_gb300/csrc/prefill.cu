@@ -81,12 +81,50 @@ static_assert(PF_SMEM_BYTES <= 232448, "prefill shared memory above the 227 KiB 
 __device__ __forceinline__ uint32_t sw_off(int row, int chunk) { return sw128_off(row, chunk); }
 
 // K-major 128-byte-swizzled operand: k-step ks (16 elements) of a 128x128 tile.
-__device__ __forceinline__ uint64_t kmajor_desc(uint32_t tile, int ks) {
-    return smem_desc(tile + (ks >> 2) * 16384 + (ks & 3) * 32, 16, 1024, 2);
+// Shared-memory descriptors of this kernel's operands differ only in their low
+// word (start address >> 4 in bits 0..13, leading byte offset >> 4 in bits
+// 16..29); the high word holds SBO = 1024 B (bits 32..45), the fixed version
+// bit 46 and the 128-byte swizzle mode (bits 61..63).
+constexpr uint32_t DESC_HI = (1024u >> 4) | (1u << 14) | (2u << 29);
+__device__ __forceinline__ uint32_t desc_lo(uint32_t saddr, uint32_t lbo_bytes) {
+    return ((saddr & 0x3FFFFu) >> 4) | ((lbo_bytes >> 4) << 16);
 }
-// MN-major 128-byte-swizzled operand ([token][64 dims] blocks): k-step = 16 tokens.
-__device__ __forceinline__ uint64_t mnmajor_desc(uint32_t tile, int ks) {
-    return smem_desc(tile + ks * 2048, 16384, 1024, 2);
+// k-step offsets added to the start-address field (no carry: every operand
+// lies in the CTA's shared memory, below 256 KiB).
+__host__ __device__ constexpr uint32_t kmajor_step(int ks) { return (uint32_t)(((ks >> 2) * 16384 + (ks & 3) * 32) >> 4); }
+__host__ __device__ constexpr uint32_t mnmajor_step(int ks) { return (uint32_t)(ks * (2048 >> 4)); }
+constexpr uint32_t TILE_DESC = PF_TILE_BYTES >> 4;  // one 32 KiB tile in descriptor address units
+
+// D[tmem] (+)= A[smem] * B[smem] at k-step KS: the descriptors are given by
+// the low words of their k-step-0 values and the step offset is added inside
+// the asm, so the compiler keeps only the two base words live.
+template <int KS>
+__device__ __forceinline__ void mma_ss_step(uint32_t d, uint32_t a_lo, uint32_t b_lo, uint32_t idesc) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t.reg .b32 al, bl;\n\t.reg .b64 da, db;\n\t"
+        "add.u32 al, %1, %5;\n\tadd.u32 bl, %2, %5;\n\t"
+        "mov.b64 da, {al, %4};\n\tmov.b64 db, {bl, %4};\n\t"
+        "setp.ne.b32 p, %6, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %3, p;\n\t}" ::"r"(d),
+        "r"(a_lo), "r"(b_lo), "r"(idesc), "r"(DESC_HI), "n"(kmajor_step(KS)), "n"(KS > 0 ? 1 : 0)
+        : "memory");
+    if constexpr (KS + 1 < 8) mma_ss_step<KS + 1>(d, a_lo, b_lo, idesc);
+}
+// D[tmem] (+)= A[tmem] * B[smem] at k-step KS (A: 8 columns of packed BF16
+// pairs per k-step); accumulates from k-step 1 on, and at k-step 0 iff acc0.
+template <int KS>
+__device__ __forceinline__ void mma_ts_step(uint32_t d, uint32_t a_tmem, uint32_t b_lo, uint32_t idesc,
+                                            uint32_t acc0) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t.reg .b32 at, bl;\n\t.reg .b64 db;\n\t"
+        "add.u32 at, %1, %5;\n\tadd.u32 bl, %2, %6;\n\t"
+        "mov.b64 db, {bl, %4};\n\t"
+        "setp.ne.b32 p, %7, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [at], db, %3, p;\n\t}" ::"r"(d),
+        "r"(a_tmem), "r"(b_lo), "r"(idesc), "r"(DESC_HI), "n"(KS * 8), "n"(mnmajor_step(KS)),
+        "r"(KS > 0 ? 1u : acc0)
+        : "memory");
+    if constexpr (KS + 1 < 8) mma_ts_step<KS + 1>(d, a_tmem, b_lo, idesc, acc0);
 }
 
 struct TileInfo {
@@ -286,25 +324,34 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
             // scores: FP16 A and B (format 0), FP32 accumulate, K-major both
             const uint32_t idS = (1u << 4) | ((uint32_t)(PF_BN >> 3) << 17) | ((uint32_t)(PF_BM >> 4) << 24);
             const uint32_t idO = idesc_bf16_f32(PF_BM, HEAD_DIM, 0, 1);
+            // k-step 0 descriptors of stage 0; stages and k-steps are added to the
+            // address field.  Each group of 8 MMAs is unrolled with constant offsets so
+            // that the single issuing thread keeps up with the tensor pipe.
+            const uint32_t dQ0 = desc_lo(s_base + OFF_Q, 16);
+            const uint32_t dK0 = desc_lo(s_base + OFF_K, 16);
+            const uint32_t dV0 = desc_lo(s_base + OFF_V, 16384);
             bool ok = mbar_wait(smem_u32(&bars->q_ready), 0, abort);
+            int v_seen = -1;  // last V tile whose arrival (and tail zeroing) was observed
             auto issue_pv = [&](int j, int i) -> bool {  // O_j += P_j(i) V(i)
                 if (!mbar_wait(smem_u32(&bars->p_ready[j]), (uint32_t)(i & 1), abort)) return false;
-                if (!mbar_wait(smem_u32(&bars->v_full[i % VSTAGES]), (uint32_t)((i / VSTAGES) & 1), abort))
-                    return false;
-                if (has_tail && i == n_tiles - 1 && !mbar_wait(smem_u32(&bars->v_tail), 0, abort)) return false;
+                if (v_seen != i) {
+                    if (!mbar_wait(smem_u32(&bars->v_full[i % VSTAGES]), (uint32_t)((i / VSTAGES) & 1), abort))
+                        return false;
+                    if (has_tail && i == n_tiles - 1 && !mbar_wait(smem_u32(&bars->v_tail), 0, abort)) return false;
+                    v_seen = i;
+                }
                 tc_fence_after();
-                const uint32_t vt = s_base + OFF_V + (i % VSTAGES) * PF_TILE_BYTES;
-                const uint32_t pt = tmem + j * 128;
-#pragma unroll 1
-                for (int ks = 0; ks < 8; ++ks)
-                    umma_ts(tmem + 256 + j * 128, pt + ks * 8, mnmajor_desc(vt, ks), idO,
-                            (i > 0 || ks > 0) ? 1u : 0u);
+                const uint32_t dv = dV0 + (uint32_t)(i % VSTAGES) * TILE_DESC;
+                const uint32_t d = tmem + 256 + j * 128, pt = tmem + j * 128;
+                mma_ts_step<0>(d, pt, dv, idO, i > 0 ? 1u : 0u);
                 return true;
             };
             for (int i = 0; i < n_tiles && ok; ++i) {
                 const int k = i % KSTAGES;
                 bool k_in = false;
-                for (int j = 0; j < 2 && ok; ++j) {
+#pragma unroll
+                for (int j = 0; j < 2; ++j) {
+                    if (!ok) break;
                     if (i < ti[j].n_tiles) {
                         if (i > 0 && !(ok = issue_pv(j, i - 1))) break;
                         if (!k_in) {
@@ -313,12 +360,9 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
                             tc_fence_after();
                             k_in = true;
                         }
-                        const uint32_t kt = s_base + OFF_K + k * PF_TILE_BYTES;
-                        const uint32_t qt = s_base + OFF_Q + j * PF_TILE_BYTES;
-#pragma unroll 1
-                        for (int ks = 0; ks < 8; ++ks)
-                            umma_ss(tmem + j * 128, kmajor_desc(qt, ks), kmajor_desc(kt, ks), idS,
-                                    ks > 0 ? 1u : 0u);
+                        const uint32_t dk = dK0 + (uint32_t)k * TILE_DESC, dq = dQ0 + (uint32_t)j * TILE_DESC;
+                        const uint32_t d = tmem + j * 128;
+                        mma_ss_step<0>(d, dq, dk, idS);
                         umma_commit(smem_u32(&bars->s_full[j]));
                     } else if (i == ti[j].n_tiles && i > 0) {
                         if (!(ok = issue_pv(j, i - 1))) break;
@@ -329,8 +373,9 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
                 umma_commit(smem_u32(&bars->k_empty[k]));                       // K(i) read by S(i)
                 if (i > 0) umma_commit(smem_u32(&bars->v_empty[(i - 1) % VSTAGES]));  // V(i-1) read by PV(i-1)
             }
-            for (int j = 0; j < 2 && ok; ++j) {
-                if (ti[j].n_tiles == n_tiles) {
+#pragma unroll
+            for (int j = 0; j < 2; ++j) {
+                if (ok && ti[j].n_tiles == n_tiles) {
                     if (!(ok = issue_pv(j, n_tiles - 1))) break;
                     umma_commit(smem_u32(&bars->o_done[j]));
                 }
