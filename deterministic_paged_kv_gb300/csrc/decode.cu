@@ -233,7 +233,9 @@ __global__ void __launch_bounds__(DEC_THREADS, 1)
         if (lane == 0) {
             const uint32_t idS = idesc_f16_f32(DEC_BN, NH);
             const uint32_t idO = idesc_bf16_f32(HEAD_DIM, NH, 1, 0);
-            const uint32_t qt = s_base + OFF_QT, pt = s_base + OFF_PT;
+            constexpr uint32_t TILE_DESC = DEC_TILE_BYTES >> 4;  // one 32 KiB tile in descriptor address units
+            const uint32_t dK0 = desc_lo(s_base + OFF_K, 16), dV0 = desc_lo(s_base + OFF_V, 16384);
+            const uint32_t dQT = desc_lo(s_base + OFF_QT, 16), dPT = desc_lo(s_base + OFF_PT, 16);
             bool ok = mbar_wait(smem_u32(&ctl->q_ready), 0, abort);
             // Event-driven issue: the next score MMA and the next PV MMA are
             // started as soon as their own inputs are ready, so neither waits
@@ -247,12 +249,8 @@ __global__ void __launch_bounds__(DEC_THREADS, 1)
                     if (mbar_test(smem_u32(&ctl->k_ready[k]), (uint32_t)((i / DEC_KSTAGES) & 1)) &&
                         (i < 2 || mbar_test(smem_u32(&ctl->s_free[sb]), (uint32_t)(((i >> 1) - 1) & 1)))) {
                         tc_fence_after();
-                        const uint32_t kt = s_base + OFF_K + k * DEC_TILE_BYTES;
-#pragma unroll 1
-                        for (int ks = 0; ks < 8; ++ks)
-                            umma_ss(tmem + sb * NH, smem_desc(kt + (ks >> 2) * 16384 + (ks & 3) * 32, 16, 1024, 2),
-                                    smem_desc(qt + (ks >> 2) * 2048 + (ks & 3) * 32, 16, 1024, 2), idS,
-                                    ks > 0 ? 1u : 0u);
+                        mma_ss_steps<0, 8, K_MAJOR_128, K_MAJOR_16>(tmem + sb * NH, dK0 + (uint32_t)k * TILE_DESC,
+                                                                    dQT, idS, 0u);
                         umma_commit(smem_u32(&ctl->s_full[sb]));
                         umma_commit(smem_u32(&ctl->k_empty[k]));
                         ++next_s;
@@ -265,12 +263,8 @@ __global__ void __launch_bounds__(DEC_THREADS, 1)
                         mbar_test(smem_u32(&ctl->v_full[i % DEC_VSTAGES]), (uint32_t)((i / DEC_VSTAGES) & 1)) &&
                         (!(has_tail && i == n_tiles - 1) || mbar_test(smem_u32(&ctl->v_tail), 0))) {
                         tc_fence_after();
-                        const uint32_t vt = s_base + OFF_V + (i % DEC_VSTAGES) * DEC_TILE_BYTES;
-#pragma unroll 1
-                        for (int ks = 0; ks < 8; ++ks)
-                            umma_ss(tO, smem_desc(vt + ks * 2048, 16384, 1024, 2),
-                                    smem_desc(pt + (ks >> 2) * 2048 + (ks & 3) * 32, 16, 1024, 2), idO,
-                                    (i > 0 || ks > 0) ? 1u : 0u);
+                        mma_ss_steps<0, 8, MN_MAJOR, K_MAJOR_16>(tO, dV0 + (uint32_t)(i % DEC_VSTAGES) * TILE_DESC,
+                                                                 dPT, idO, i > 0 ? 1u : 0u);
                         umma_commit(smem_u32(&ctl->pv_done));
                         umma_commit(smem_u32(&ctl->v_empty[i % DEC_VSTAGES]));
                         ++next_pv;

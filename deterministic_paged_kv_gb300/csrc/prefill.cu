@@ -80,53 +80,6 @@ static_assert(PF_SMEM_BYTES <= 232448, "prefill shared memory above the 227 KiB 
 
 __device__ __forceinline__ uint32_t sw_off(int row, int chunk) { return sw128_off(row, chunk); }
 
-// K-major 128-byte-swizzled operand: k-step ks (16 elements) of a 128x128 tile.
-// Shared-memory descriptors of this kernel's operands differ only in their low
-// word (start address >> 4 in bits 0..13, leading byte offset >> 4 in bits
-// 16..29); the high word holds SBO = 1024 B (bits 32..45), the fixed version
-// bit 46 and the 128-byte swizzle mode (bits 61..63).
-constexpr uint32_t DESC_HI = (1024u >> 4) | (1u << 14) | (2u << 29);
-__device__ __forceinline__ uint32_t desc_lo(uint32_t saddr, uint32_t lbo_bytes) {
-    return ((saddr & 0x3FFFFu) >> 4) | ((lbo_bytes >> 4) << 16);
-}
-// k-step offsets added to the start-address field (no carry: every operand
-// lies in the CTA's shared memory, below 256 KiB).
-__host__ __device__ constexpr uint32_t kmajor_step(int ks) { return (uint32_t)(((ks >> 2) * 16384 + (ks & 3) * 32) >> 4); }
-__host__ __device__ constexpr uint32_t mnmajor_step(int ks) { return (uint32_t)(ks * (2048 >> 4)); }
-constexpr uint32_t TILE_DESC = PF_TILE_BYTES >> 4;  // one 32 KiB tile in descriptor address units
-
-// D[tmem] (+)= A[smem] * B[smem] at k-step KS: the descriptors are given by
-// the low words of their k-step-0 values and the step offset is added inside
-// the asm, so the compiler keeps only the two base words live.
-template <int KS>
-__device__ __forceinline__ void mma_ss_step(uint32_t d, uint32_t a_lo, uint32_t b_lo, uint32_t idesc) {
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t.reg .b32 al, bl;\n\t.reg .b64 da, db;\n\t"
-        "add.u32 al, %1, %5;\n\tadd.u32 bl, %2, %5;\n\t"
-        "mov.b64 da, {al, %4};\n\tmov.b64 db, {bl, %4};\n\t"
-        "setp.ne.b32 p, %6, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %3, p;\n\t}" ::"r"(d),
-        "r"(a_lo), "r"(b_lo), "r"(idesc), "r"(DESC_HI), "n"(kmajor_step(KS)), "n"(KS > 0 ? 1 : 0)
-        : "memory");
-    if constexpr (KS + 1 < 8) mma_ss_step<KS + 1>(d, a_lo, b_lo, idesc);
-}
-// D[tmem] (+)= A[tmem] * B[smem] at k-step KS (A: 8 columns of packed BF16
-// pairs per k-step); accumulates from k-step 1 on, and at k-step 0 iff acc0.
-template <int KS>
-__device__ __forceinline__ void mma_ts_step(uint32_t d, uint32_t a_tmem, uint32_t b_lo, uint32_t idesc,
-                                            uint32_t acc0) {
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t.reg .b32 at, bl;\n\t.reg .b64 db;\n\t"
-        "add.u32 at, %1, %5;\n\tadd.u32 bl, %2, %6;\n\t"
-        "mov.b64 db, {bl, %4};\n\t"
-        "setp.ne.b32 p, %7, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], [at], db, %3, p;\n\t}" ::"r"(d),
-        "r"(a_tmem), "r"(b_lo), "r"(idesc), "r"(DESC_HI), "n"(KS * 8), "n"(mnmajor_step(KS)),
-        "r"(KS > 0 ? 1u : acc0)
-        : "memory");
-    if constexpr (KS + 1 < 8) mma_ts_step<KS + 1>(d, a_tmem, b_lo, idesc, acc0);
-}
-
 struct TileInfo {
     int s0;       // first query index of the q-tile
     int n_keys;   // keys any of its rows may see
@@ -327,6 +280,7 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
             // k-step 0 descriptors of stage 0; stages and k-steps are added to the
             // address field.  Each group of 8 MMAs is unrolled with constant offsets so
             // that the single issuing thread keeps up with the tensor pipe.
+            constexpr uint32_t TILE_DESC = PF_TILE_BYTES >> 4;  // one 32 KiB tile in descriptor address units
             const uint32_t dQ0 = desc_lo(s_base + OFF_Q, 16);
             const uint32_t dK0 = desc_lo(s_base + OFF_K, 16);
             const uint32_t dV0 = desc_lo(s_base + OFF_V, 16384);
@@ -343,7 +297,7 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
                 tc_fence_after();
                 const uint32_t dv = dV0 + (uint32_t)(i % VSTAGES) * TILE_DESC;
                 const uint32_t d = tmem + 256 + j * 128, pt = tmem + j * 128;
-                mma_ts_step<0>(d, pt, dv, idO, i > 0 ? 1u : 0u);
+                mma_ts_steps<0, 8, MN_MAJOR>(d, pt, dv, idO, i > 0 ? 1u : 0u);
                 return true;
             };
             for (int i = 0; i < n_tiles && ok; ++i) {
@@ -362,7 +316,7 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
                         }
                         const uint32_t dk = dK0 + (uint32_t)k * TILE_DESC, dq = dQ0 + (uint32_t)j * TILE_DESC;
                         const uint32_t d = tmem + j * 128;
-                        mma_ss_step<0>(d, dq, dk, idS);
+                        mma_ss_steps<0, 8, K_MAJOR_128, K_MAJOR_128>(d, dq, dk, idS, 0u);
                         umma_commit(smem_u32(&bars->s_full[j]));
                     } else if (i == ti[j].n_tiles && i > 0) {
                         if (!(ok = issue_pv(j, i - 1))) break;

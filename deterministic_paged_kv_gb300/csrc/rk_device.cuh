@@ -188,6 +188,63 @@ __device__ __forceinline__ void umma_commit(uint32_t bar) {
         : "memory");
 }
 
+// Unrolled MMA groups.  Every operand of these kernels is a 128-byte-swizzled
+// tile in the CTA's shared memory whose descriptor has SBO = 1024 B, version
+// bit 46 and swizzle mode 2, so descriptors differ only in their low word
+// (start address >> 4 in bits 0..13, leading byte offset >> 4 in bits 16..29).
+// The k-step offset of each MMA is an immediate added inside the asm: the
+// issuing thread keeps two base words live and issues one MMA after another
+// without recomputing descriptors, which a single thread must do to keep up
+// with the tensor pipe.
+constexpr uint32_t DESC_HI = (1024u >> 4) | (1u << 14) | (2u << 29);
+__device__ __forceinline__ uint32_t desc_lo(uint32_t saddr, uint32_t lbo_bytes) {
+    return ((saddr & 0x3FFFFu) >> 4) | ((lbo_bytes >> 4) << 16);
+}
+// Operand layouts and their k-step (16 elements) offsets in descriptor units
+// (no carry into bit 14: all operands lie below 256 KiB of shared memory).
+enum OperandLayout : int {
+    K_MAJOR_128 = 0,  // [128 rows][2 x 64 elements] K-major: 64-element blocks 16 KiB apart
+    K_MAJOR_16 = 1,   // [16 rows][2 x 64 elements] K-major: blocks 2 KiB apart
+    MN_MAJOR = 2      // [K rows][2 x 64 MN elements]: a k-step is 16 rows = 2 KiB
+};
+__host__ __device__ constexpr uint32_t kstep_off(int layout, int ks) {
+    return layout == K_MAJOR_128 ? (uint32_t)(((ks >> 2) * 16384 + (ks & 3) * 32) >> 4)
+           : layout == K_MAJOR_16 ? (uint32_t)(((ks >> 2) * 2048 + (ks & 3) * 32) >> 4)
+                                  : (uint32_t)(ks * (2048 >> 4));
+}
+// D[tmem] (+)= A[smem] * B[smem], k-steps KS..END-1 of operands with the given
+// layouts; accumulates from k-step 1 on, and at k-step 0 iff acc0.
+template <int KS, int END, int LA, int LB>
+__device__ __forceinline__ void mma_ss_steps(uint32_t d, uint32_t a_lo, uint32_t b_lo, uint32_t idesc,
+                                             uint32_t acc0) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t.reg .b32 al, bl;\n\t.reg .b64 da, db;\n\t"
+        "add.u32 al, %1, %5;\n\tadd.u32 bl, %2, %6;\n\t"
+        "mov.b64 da, {al, %4};\n\tmov.b64 db, {bl, %4};\n\t"
+        "setp.ne.b32 p, %7, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %3, p;\n\t}" ::"r"(d),
+        "r"(a_lo), "r"(b_lo), "r"(idesc), "r"(DESC_HI), "n"(kstep_off(LA, KS)), "n"(kstep_off(LB, KS)),
+        "r"(KS > 0 ? 1u : acc0)
+        : "memory");
+    if constexpr (KS + 1 < END) mma_ss_steps<KS + 1, END, LA, LB>(d, a_lo, b_lo, idesc, acc0);
+}
+// D[tmem] (+)= A[tmem] * B[smem], k-steps KS..END-1; A holds 8 columns of
+// packed 16-bit pairs per k-step.
+template <int KS, int END, int LB>
+__device__ __forceinline__ void mma_ts_steps(uint32_t d, uint32_t a_tmem, uint32_t b_lo, uint32_t idesc,
+                                             uint32_t acc0) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t.reg .b32 at, bl;\n\t.reg .b64 db;\n\t"
+        "add.u32 at, %1, %5;\n\tadd.u32 bl, %2, %6;\n\t"
+        "mov.b64 db, {bl, %4};\n\t"
+        "setp.ne.b32 p, %7, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [at], db, %3, p;\n\t}" ::"r"(d),
+        "r"(a_tmem), "r"(b_lo), "r"(idesc), "r"(DESC_HI), "n"(KS * 8), "n"(kstep_off(LB, KS)),
+        "r"(KS > 0 ? 1u : acc0)
+        : "memory");
+    if constexpr (KS + 1 < END) mma_ts_steps<KS + 1, END, LB>(d, a_tmem, b_lo, idesc, acc0);
+}
+
 // Shared-memory matrix descriptor (tcgen05): start address, leading and
 // stride byte offsets, fixed version bits 46..48 = 0b001, swizzle mode in
 // bits 61..63 (2 = 128-byte swizzle).
