@@ -10,16 +10,20 @@
 // One CTA per (row b, KV head); all G = Hq/Hkv query heads of the group are
 // served by one pass over the row's pages (GQA packing: every K/V byte is
 // read once).  The row's tokens are swept in ascending tiles of 128 (8 pages):
-//   warps 12 / 14 TMA producers: K pages (3-stage ring) and V pages (2-stage
-//                 ring) as 16-token x 64-dim boxes with 128-byte swizzle, i.e.
-//                 already in the UMMA operand layout; the V producer zeroes
-//                 cache rows past kv_len in a partial last page;
+//   warps 12 / 14 TMA producers: K pages (4-stage ring) as two 16-token x
+//                 64-dim boxes each, V pages (2-stage ring) as one 4 KiB box
+//                 each ([64-dim half][16 tokens], read by the PV MMA one page
+//                 per k-step), 128-byte swizzled, i.e. already in UMMA operand
+//                 layout; fewer, larger boxes keep more bytes in flight per SM
+//                 (the TMA unit holds a bounded number of boxes); the V
+//                 producer zeroes cache rows past kv_len in a partial last page;
 //   warps 0-7     transform: rotate each K row in FP32 (angles from an exact
 //                 fixed-point anchor plus 32-position steps) and store it as
 //                 FP16 in place; rotate the G query rows once (FP16 Q^T);
-//   warp 13       MMA issuer: S^T = K Q^T (M = 128 tokens, N = 16 >= G heads,
-//                 FP16 operands, FP32 in TMEM, double-buffered) and
-//                 O^T += V^T P^T (M = 128 dims, N = 16, BF16, FP32 in TMEM);
+//   warp 13       score MMA issuer: S^T = K Q^T (M = 128 tokens, N = 16 >= G
+//                 heads, FP16 operands, FP32 in TMEM, double-buffered);
+//   warp 15       PV MMA issuer: O^T += V^T P^T (M = 128 dims, N = 16, BF16,
+//                 FP32 in TMEM, P^T double-buffered in shared memory);
 //   warps 8-11    softmax: thread t owns token t of the tile: masks, takes the
 //                 tile max per head over the 128 tokens (xor-butterfly + fixed
 //                 warp order), moves the running max only when it grows by
@@ -45,8 +49,10 @@ constexpr int WARP_SOFTMAX0 = DEC_XFORM_THREADS / 32;  // warps 8-11
 constexpr int WARP_TMA_K = WARP_SOFTMAX0 + 4;
 constexpr int WARP_MMA = WARP_TMA_K + 1;
 constexpr int WARP_TMA_V = WARP_TMA_K + 2;
+constexpr int WARP_PV = WARP_TMA_K + 3;
 constexpr int XF_ROW_STEP = DEC_XFORM_THREADS / 8;      // rows between a thread's K rows
 constexpr int XF_ROWS = DEC_BN / XF_ROW_STEP;           // K rows per transform thread per tile
+constexpr int XF_ANCHOR_TILES = 8;                      // tiles between exact RoPE anchors
 constexpr uint32_t TMEM_COLS = 64;  // S^T buffers [0,16) [16,32), O^T [32,48)
 constexpr float RESCALE_SLACK = 8.0f;
 constexpr int NH = 16;  // N of both MMAs: query heads of the group, zero padded
@@ -54,16 +60,19 @@ constexpr int NH = 16;  // N of both MMAs: query heads of the group, zero padded
 constexpr int OFF_K = 0;
 constexpr int OFF_V = OFF_K + DEC_KSTAGES * DEC_TILE_BYTES;
 constexpr int OFF_QT = OFF_V + DEC_VSTAGES * DEC_TILE_BYTES;  // Q^T: 16 rows x 128 dims FP16
-constexpr int OFF_PT = OFF_QT + NH * HEAD_DIM * 2;            // P^T: 16 rows x 128 tokens BF16
-constexpr int OFF_CTRL = OFF_PT + NH * DEC_BN * 2;
+constexpr int PT_BYTES = NH * DEC_BN * 2;                     // P^T: 16 rows x 128 tokens BF16
+constexpr int OFF_PT = OFF_QT + NH * HEAD_DIM * 2;            // two P^T buffers (tile parity)
+constexpr int OFF_CTRL = OFF_PT + 2 * PT_BYTES;
 static_assert(OFF_CTRL + DEC_CTRL_BYTES == DEC_SMEM_BYTES, "decode shared memory carve");
 
 struct DecCtrl {
     uint64_t q_ready;
     uint64_t k_full[DEC_KSTAGES], k_ready[DEC_KSTAGES], k_empty[DEC_KSTAGES];
     uint64_t v_full[DEC_VSTAGES], v_empty[DEC_VSTAGES], v_tail;
-    uint64_t s_full[2], s_free[2], p_ready, pv_done, o_done;
-    uint64_t red_bar[2];  // the 4 softmax warps' tile maxima are in red[sb]
+    // per tile parity b: S^T buffer (s_full, s_free), P^T buffer (p_ready) and
+    // the PV that read it (pv_done); a buffer is reused two tiles later, after
+    // its previous phase has been observed, so a wait never meets a later phase
+    uint64_t s_full[2], s_free[2], p_ready[2], pv_done[2], o_done;
     uint32_t tmem_base;
     int abort;
     int range_bad;
@@ -133,11 +142,11 @@ __global__ void __launch_bounds__(DEC_THREADS, 1)
             mbar_init(smem_u32(&ctl->s_full[k]), 1);
             mbar_init(smem_u32(&ctl->s_free[k]), 128);
         }
-        mbar_init(smem_u32(&ctl->p_ready), 128);
-        mbar_init(smem_u32(&ctl->pv_done), 1);
+        mbar_init(smem_u32(&ctl->p_ready[0]), 128);
+        mbar_init(smem_u32(&ctl->p_ready[1]), 128);
+        mbar_init(smem_u32(&ctl->pv_done[0]), 1);
+        mbar_init(smem_u32(&ctl->pv_done[1]), 1);
         mbar_init(smem_u32(&ctl->o_done), 1);
-        mbar_init(smem_u32(&ctl->red_bar[0]), 4);
-        mbar_init(smem_u32(&ctl->red_bar[1]), 4);
         fence_mbar_init();
     }
     if (tid < ROPE_PAIRS) {
@@ -198,9 +207,13 @@ __global__ void __launch_bounds__(DEC_THREADS, 1)
             good = __shfl_sync(0xffffffffu, good, 0);
             if (!good) break;
             if (lane < np) {
-                const uint32_t t = s_base + (is_k ? OFF_K : OFF_V) + k * DEC_TILE_BYTES + lane * 2048;
-                tma_load_3d(t, map, fb, 0, kvh, pg * PAGE);
-                tma_load_3d(t + 16384, map, fb, 64, kvh, pg * PAGE);
+                if (is_k) {  // two 16 x 64 boxes per page: the K-major tile layout
+                    const uint32_t t = s_base + OFF_K + k * DEC_TILE_BYTES + lane * 2048;
+                    tma_load_3d(t, map, fb, 0, kvh, pg * PAGE);
+                    tma_load_3d(t + 16384, map, fb, 64, kvh, pg * PAGE);
+                } else {     // one 4 KiB box per page: [page][half][16 rows][128 B]
+                    tma_load_4d(s_base + OFF_V + k * DEC_TILE_BYTES + lane * 4096, map, fb, 0, pg * PAGE, 0, kvh);
+                }
             }
             __syncwarp();
             if (!is_k && has_tail && i == n_tiles - 1) {
@@ -213,8 +226,8 @@ __global__ void __launch_bounds__(DEC_THREADS, 1)
                     uint8_t* vt = sm + OFF_V + k * DEC_TILE_BYTES;
                     for (int idx = lane; idx < (r_end - tail) * 16; idx += 32) {
                         const int rr = tail + (idx >> 4), ch = idx & 15;
-                        *reinterpret_cast<uint4*>(vt + (ch >> 3) * 16384 + rr * 128 + (ch & 7) * 16) =
-                            make_uint4(0, 0, 0, 0);
+                        *reinterpret_cast<uint4*>(vt + (rr >> 4) * 4096 + (ch >> 3) * 2048 + (rr & 15) * 128 +
+                                                  (ch & 7) * 16) = make_uint4(0, 0, 0, 0);
                     }
                     fence_proxy_async_smem();
                     __syncwarp();
@@ -228,59 +241,47 @@ __global__ void __launch_bounds__(DEC_THREADS, 1)
                 mbar_wait_drain(smem_u32(is_k ? &ctl->k_full[i % nst] : &ctl->v_full[i % nst]),
                                 (uint32_t)((i / nst) & 1));
         }
-    } else if (warp == WARP_MMA) {
-        // ============================================= MMA issuer ====
+    } else if (warp == WARP_MMA || warp == WARP_PV) {
+        // ============================================ MMA issuers ====
+        // Two issuing threads: warp 13 issues the score MMAs, warp 15 the PV
+        // MMAs, each waiting only for its own inputs, so the barrier checks of
+        // one overlap the MMAs of the other.  tcgen05.commit covers the MMAs of
+        // the committing thread, which is what each completion barrier tracks.
         if (lane == 0) {
-            const uint32_t idS = idesc_f16_f32(DEC_BN, NH);
-            const uint32_t idO = idesc_bf16_f32(HEAD_DIM, NH, 1, 0);
             constexpr uint32_t TILE_DESC = DEC_TILE_BYTES >> 4;  // one 32 KiB tile in descriptor address units
-            const uint32_t dK0 = desc_lo(s_base + OFF_K, 16), dV0 = desc_lo(s_base + OFF_V, 16384);
-            const uint32_t dQT = desc_lo(s_base + OFF_QT, 16), dPT = desc_lo(s_base + OFF_PT, 16);
-            bool ok = mbar_wait(smem_u32(&ctl->q_ready), 0, abort);
-            // Event-driven issue: the next score MMA and the next PV MMA are
-            // started as soon as their own inputs are ready, so neither waits
-            // behind the other's producer (MMAs still retire in issue order).
-            int next_s = 0, next_pv = 0;
-            uint64_t idle_since = global_timer_ns();
-            while (ok && next_pv < n_tiles) {
-                bool progressed = false;
-                if (next_s < n_tiles) {
-                    const int i = next_s, k = i % DEC_KSTAGES, sb = i & 1;
-                    if (mbar_test(smem_u32(&ctl->k_ready[k]), (uint32_t)((i / DEC_KSTAGES) & 1)) &&
-                        (i < 2 || mbar_test(smem_u32(&ctl->s_free[sb]), (uint32_t)(((i >> 1) - 1) & 1)))) {
-                        tc_fence_after();
-                        mma_ss_steps<0, 8, K_MAJOR_128, K_MAJOR_16>(tmem + sb * NH, dK0 + (uint32_t)k * TILE_DESC,
-                                                                    dQT, idS, 0u);
-                        umma_commit(smem_u32(&ctl->s_full[sb]));
-                        umma_commit(smem_u32(&ctl->k_empty[k]));
-                        ++next_s;
-                        progressed = true;
-                    }
+            bool ok = true;
+            if (warp == WARP_MMA) {
+                const uint32_t idS = idesc_f16_f32(DEC_BN, NH);
+                const uint32_t dK0 = desc_lo(s_base + OFF_K, 16), dQT = desc_lo(s_base + OFF_QT, 16);
+                ok = mbar_wait(smem_u32(&ctl->q_ready), 0, abort);
+                for (int i = 0; i < n_tiles && ok; ++i) {
+                    const int k = i % DEC_KSTAGES, sb = i & 1;
+                    ok = mbar_wait(smem_u32(&ctl->k_ready[k]), (uint32_t)((i / DEC_KSTAGES) & 1), abort) &&
+                         (i < 2 || mbar_wait(smem_u32(&ctl->s_free[sb]), (uint32_t)(((i >> 1) - 1) & 1), abort));
+                    if (!ok) break;
+                    tc_fence_after();
+                    mma_ss_steps<0, 8, K_MAJOR_128, K_MAJOR_16>(tmem + sb * NH, dK0 + (uint32_t)k * TILE_DESC, dQT,
+                                                                idS, 0u);
+                    umma_commit(smem_u32(&ctl->s_full[sb]));
+                    umma_commit(smem_u32(&ctl->k_empty[k]));
                 }
-                if (next_pv < next_s) {
-                    const int i = next_pv;
-                    if (mbar_test(smem_u32(&ctl->p_ready), (uint32_t)(i & 1)) &&
-                        mbar_test(smem_u32(&ctl->v_full[i % DEC_VSTAGES]), (uint32_t)((i / DEC_VSTAGES) & 1)) &&
-                        (!(has_tail && i == n_tiles - 1) || mbar_test(smem_u32(&ctl->v_tail), 0))) {
-                        tc_fence_after();
-                        mma_ss_steps<0, 8, MN_MAJOR, K_MAJOR_16>(tO, dV0 + (uint32_t)(i % DEC_VSTAGES) * TILE_DESC,
-                                                                 dPT, idO, i > 0 ? 1u : 0u);
-                        umma_commit(smem_u32(&ctl->pv_done));
-                        umma_commit(smem_u32(&ctl->v_empty[i % DEC_VSTAGES]));
-                        ++next_pv;
-                        progressed = true;
-                    }
+            } else {
+                const uint32_t idO = idesc_bf16_f32(HEAD_DIM, NH, 1, 0);
+                const uint32_t dV0 = desc_lo(s_base + OFF_V, 2048), dPT = desc_lo(s_base + OFF_PT, 16);
+                for (int i = 0; i < n_tiles && ok; ++i) {
+                    ok = mbar_wait(smem_u32(&ctl->p_ready[i & 1]), (uint32_t)((i >> 1) & 1), abort) &&
+                         mbar_wait(smem_u32(&ctl->v_full[i % DEC_VSTAGES]), (uint32_t)((i / DEC_VSTAGES) & 1), abort) &&
+                         (!(has_tail && i == n_tiles - 1) || mbar_wait(smem_u32(&ctl->v_tail), 0, abort));
+                    if (!ok) break;
+                    tc_fence_after();
+                    mma_ss_steps<0, 8, MN_MAJOR_PAGE, K_MAJOR_16>(tO, dV0 + (uint32_t)(i % DEC_VSTAGES) * TILE_DESC,
+                                                             dPT + (uint32_t)(i & 1) * (PT_BYTES >> 4), idO,
+                                                             i > 0 ? 1u : 0u);
+                    umma_commit(smem_u32(&ctl->pv_done[i & 1]));
+                    umma_commit(smem_u32(&ctl->v_empty[i % DEC_VSTAGES]));
                 }
-                if (progressed) {
-                    idle_since = global_timer_ns();
-                } else if (*abort) {
-                    ok = false;
-                } else if (global_timer_ns() - idle_since > RK_WAIT_LIMIT_NS) {
-                    *abort = 1;
-                    ok = false;
-                }
+                if (ok) umma_commit(smem_u32(&ctl->o_done));
             }
-            if (ok) umma_commit(smem_u32(&ctl->o_done));
             if (!ok) {
                 const uint64_t t0 = global_timer_ns();  // let issued MMAs drain before TMEM is released
                 while (global_timer_ns() - t0 < 1000000ull) {
@@ -323,22 +324,41 @@ __global__ void __launch_bounds__(DEC_THREADS, 1)
             dcs[e] = make_float2(s0.x, s1.x);
             dsn[e] = make_float2(s0.y, s1.y);
         }
+        // (cos, sin) of the thread's current row: re-anchored exactly every
+        // XF_ANCHOR_TILES tiles, advanced by the XF_ROW_STEP recurrence in between
+        // (a thread's rows are XF_ROW_STEP apart and the next tile continues the
+        // sequence), so at most XF_ANCHOR_TILES * XF_ROWS steps follow an anchor.
+        float2 c[4], sn[4];
         for (int i = 0; i < n_tiles; ++i) {
             const int k = i % DEC_KSTAGES;
             if (!mbar_wait(smem_u32(&ctl->k_full[k]), (uint32_t)((i / DEC_KSTAGES) & 1), abort)) break;
             uint8_t* kt = sm + OFF_K + k * DEC_TILE_BYTES;
             const int t0 = i * DEC_BN;
-            float2 c[4], sn[4];
+            if (i % XF_ANCHOR_TILES == 0) {
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                rope_cos_sin((uint32_t)(t0 + r0), ctl->turns[8 * u + 2 * e], c[e].x, sn[e].x);
-                rope_cos_sin((uint32_t)(t0 + r0), ctl->turns[8 * u + 2 * e + 1], c[e].y, sn[e].y);
+                for (int e = 0; e < 4; ++e) {
+                    rope_cos_sin((uint32_t)(t0 + r0), ctl->turns[8 * u + 2 * e], c[e].x, sn[e].x);
+                    rope_cos_sin((uint32_t)(t0 + r0), ctl->turns[8 * u + 2 * e + 1], c[e].y, sn[e].y);
+                }
             }
-#pragma unroll 2
+            // all of the thread's rows are read before any is rotated (the
+            // shared-memory latency is paid once per tile)
+            uint4 lo[XF_ROWS], hi[XF_ROWS];
+#pragma unroll
+            for (int m = 0; m < XF_ROWS; ++m) {
+                const uint32_t off = sw128_off(r0 + XF_ROW_STEP * m, u);
+                lo[m] = *reinterpret_cast<const uint4*>(kt + off);
+                hi[m] = *reinterpret_cast<const uint4*>(kt + 16384 + off);
+            }
+#pragma unroll
             for (int m = 0; m < XF_ROWS; ++m) {
                 const int r = r0 + XF_ROW_STEP * m;
-                const uint32_t off = sw128_off(r, u);
-                if (t0 + r < n_vis) range = rotate_chunk_f16(kt + off, kt + 16384 + off, c, sn, range);
+                if (t0 + r < n_vis) {
+                    range = rotate_regs_f16(lo[m], hi[m], c, sn, range);
+                    const uint32_t off = sw128_off(r, u);
+                    *reinterpret_cast<uint4*>(kt + off) = lo[m];
+                    *reinterpret_cast<uint4*>(kt + 16384 + off) = hi[m];
+                }
                 rope_step(c, sn, dcs, dsn);
             }
             if (range_exceeded(range)) ctl->range_bad = 1;
@@ -358,10 +378,14 @@ __global__ void __launch_bounds__(DEC_THREADS, 1)
             m[h] = -INFINITY;
             lp[h] = 0.0f;
         }
-        bool ok = true;
+        // Every wait result is OR-reduced over the warpgroup at named barrier 1,
+        // so the four warps leave the loop together and never strand one another
+        // at a barrier; a thread whose wait gave up skips its work until then.
+        bool ok = true, failed = false;
         for (int i = 0; i < n_tiles; ++i) {
             const int sb = i & 1;
-            if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&ctl->s_full[sb]), (uint32_t)((i >> 1) & 1), abort))) {
+            const bool got = mbar_wait(smem_u32(&ctl->s_full[sb]), (uint32_t)((i >> 1) & 1), abort);
+            if (named_bar_or(1, 128, failed || !got)) {
                 ok = false;
                 break;
             }
@@ -381,14 +405,10 @@ __global__ void __launch_bounds__(DEC_THREADS, 1)
                 for (int off = 16; off >= 1; off >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, off));
                 if (lane == 0) ctl->red[sb][wq][h] = v;
             }
-            // Exchange the four warps' maxima through an mbarrier (bounded wait,
-            // so a warp that gave up cannot strand the others at a barrier).
-            __syncwarp();
-            if (lane == 0) mbar_arrive(smem_u32(&ctl->red_bar[sb]));
-            if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&ctl->red_bar[sb]), (uint32_t)((i >> 1) & 1), abort))) {
-                ok = false;
-                break;
-            }
+            // The four warps' maxima meet at named barrier 1.  red[] is indexed by
+            // tile parity: a buffer is rewritten two tiles later, after every
+            // thread has passed the next tile's barrier (and so read it).
+            named_bar_sync(1, 128);
             float alpha[8];
             bool resc = false;
 #pragma unroll
@@ -408,32 +428,37 @@ __global__ void __launch_bounds__(DEC_THREADS, 1)
                 p[h] = m[h] == -INFINITY ? 0.0f : ex2(x[h] - m[h]);
                 lp[h] = lp[h] * alpha[h] + p[h];
             }
-            if (i > 0) {
-                // PV(i-1) done: P^T may be overwritten and O^T is stable.
-                if (!__all_sync(0xffffffffu, mbar_wait(smem_u32(&ctl->pv_done), (uint32_t)((i - 1) & 1), abort))) {
-                    ok = false;
-                    break;
-                }
-                tc_fence_after();
-                if (resc) {  // uniform across the warpgroup: every thread saw the same maxima
-                    uint32_t orow[16];
-                    tmem_ld16(tO + lane_addr, orow);
-                    tmem_ld_wait();
-#pragma unroll
-                    for (int h = 0; h < 8; ++h) orow[h] = __float_as_uint(__uint_as_float(orow[h]) * alpha[h]);
-                    tmem_st16(tO + lane_addr, orow);
-                    tmem_st_wait();
-                }
+            // P^T buffer sb was last read by PV(i-2); a rescale of O^T needs PV(i-1)
+            // retired (resc is uniform: every thread saw the same maxima).  One
+            // barrier per buffer parity, so a wait never meets a phase of a later PV.
+            bool w = true;
+            if (i >= 2) w = mbar_wait(smem_u32(&ctl->pv_done[sb]), (uint32_t)(((i - 2) >> 1) & 1), abort);
+            if (w && resc && i >= 1)
+                w = mbar_wait(smem_u32(&ctl->pv_done[sb ^ 1]), (uint32_t)(((i - 1) >> 1) & 1), abort);
+            if (!__all_sync(0xffffffffu, w)) {
+                failed = true;  // leaves at the next barrier, together with the others
+                continue;
             }
-            uint8_t* ptb = sm + OFF_PT + (t >> 6) * 2048 + (t & 7) * 2;
+            tc_fence_after();
+            if (resc && i >= 1) {
+                uint32_t orow[16];
+                tmem_ld16(tO + lane_addr, orow);
+                tmem_ld_wait();
+#pragma unroll
+                for (int h = 0; h < 8; ++h) orow[h] = __float_as_uint(__uint_as_float(orow[h]) * alpha[h]);
+                tmem_st16(tO + lane_addr, orow);
+                tmem_st_wait();
+            }
+            uint8_t* ptb = sm + OFF_PT + sb * PT_BYTES + (t >> 6) * 2048 + (t & 7) * 2;
 #pragma unroll
             for (int h = 0; h < 8; ++h)
                 if (h < G)
                     *reinterpret_cast<__nv_bfloat16*>(ptb + sw128_off(h, (t & 63) >> 3)) = __float2bfloat16_rn(p[h]);
             fence_proxy_async_smem();
             tc_fence_before();
-            mbar_arrive(smem_u32(&ctl->p_ready));
+            mbar_arrive(smem_u32(&ctl->p_ready[sb]));
         }
+        if (ok && named_bar_or(1, 128, failed)) ok = false;
         named_bar_sync(2, DEC_XFORM_THREADS + 128);
         if (ok) ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&ctl->o_done), 0, abort));
         // ---- epilogue: fixed-order reduction of l, out = O / l once, LSE ----

@@ -16,14 +16,17 @@
 //   warpgroup 0  transform: rotate both q-tiles once and each K tile in place
 //                in shared memory (FP32 math; angles from an exact fixed-point
 //                anchor plus 16-position angle-addition steps), store FP16 in
-//                the UMMA operand layout; zero V rows past the last key;
+//                the UMMA operand layout;
 //   warpgroup 1  softmax for q-tile 0, warpgroup 2 softmax for q-tile 1: one
 //                thread per accumulator row reads its S row from TMEM, masks,
 //                runs the online softmax in the log2 domain (the running max
 //                only moves when it grows by more than 8, then the O row in
 //                TMEM is rescaled), writes P as BF16 back into TMEM over S;
 //                epilogue O / l -> BF16 once, LSE -> FP32;
-//   warp 12      TMA producer (Q once; per KV tile 8 pages x {K, V} x 2 halves);
+//   warps 12/14  TMA producers: warp 12 loads Q once and each K page as two
+//                16-token x 64-dim boxes (K-major tile layout), warp 14 each V
+//                page as one 4 KiB box ([64-dim half][16 tokens], one page per
+//                PV k-step) and zeroes V rows past the last key;
 //   warp 13      MMA issuer: S_j = Q_j K^T (FP16 operands, FP32 in TMEM) and
 //                O_j += P_j V (P from TMEM, V from shared memory, BF16).
 // Score precision: rotated Q and K are rounded to FP16 (11-bit mantissa) for
@@ -243,9 +246,14 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
                 good = __shfl_sync(0xffffffffu, good, 0);
                 if (!good) break;
                 if (lane < np) {
-                    const uint32_t t = s_base + (is_k ? OFF_K : OFF_V) + k * PF_TILE_BYTES + lane * 2048;
-                    tma_load_3d(t, map, fb, 0, kvh, pg * PAGE);
-                    tma_load_3d(t + 16384, map, fb, 64, kvh, pg * PAGE);
+                    if (is_k) {  // two 16 x 64 boxes per page: the K-major tile layout
+                        const uint32_t t = s_base + OFF_K + k * PF_TILE_BYTES + lane * 2048;
+                        tma_load_3d(t, map, fb, 0, kvh, pg * PAGE);
+                        tma_load_3d(t + 16384, map, fb, 64, kvh, pg * PAGE);
+                    } else {     // one 4 KiB box per page: [page][half][16 rows][128 B]
+                        tma_load_4d(s_base + OFF_V + k * PF_TILE_BYTES + lane * 4096, map, fb, 0, pg * PAGE, 0,
+                                    kvh);
+                    }
                 }
                 __syncwarp();
                 if (!is_k && has_tail && i == n_tiles - 1) {
@@ -257,8 +265,8 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
                         uint8_t* vt = sm + OFF_V + k * PF_TILE_BYTES;
                         for (int idx = lane; idx < (r_end - tail) * 16; idx += 32) {
                             const int rr = tail + (idx >> 4), ch = idx & 15;
-                            *reinterpret_cast<uint4*>(vt + (ch >> 3) * 16384 + rr * 128 + (ch & 7) * 16) =
-                                make_uint4(0, 0, 0, 0);
+                            *reinterpret_cast<uint4*>(vt + (rr >> 4) * 4096 + (ch >> 3) * 2048 + (rr & 15) * 128 +
+                                                      (ch & 7) * 16) = make_uint4(0, 0, 0, 0);
                         }
                         fence_proxy_async_smem();
                         __syncwarp();
@@ -283,7 +291,7 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
             constexpr uint32_t TILE_DESC = PF_TILE_BYTES >> 4;  // one 32 KiB tile in descriptor address units
             const uint32_t dQ0 = desc_lo(s_base + OFF_Q, 16);
             const uint32_t dK0 = desc_lo(s_base + OFF_K, 16);
-            const uint32_t dV0 = desc_lo(s_base + OFF_V, 16384);
+            const uint32_t dV0 = desc_lo(s_base + OFF_V, 2048);
             bool ok = mbar_wait(smem_u32(&bars->q_ready), 0, abort);
             int v_seen = -1;  // last V tile whose arrival (and tail zeroing) was observed
             auto issue_pv = [&](int j, int i) -> bool {  // O_j += P_j(i) V(i)
@@ -297,7 +305,7 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
                 tc_fence_after();
                 const uint32_t dv = dV0 + (uint32_t)(i % VSTAGES) * TILE_DESC;
                 const uint32_t d = tmem + 256 + j * 128, pt = tmem + j * 128;
-                mma_ts_steps<0, 8, MN_MAJOR>(d, pt, dv, idO, i > 0 ? 1u : 0u);
+                mma_ts_steps<0, 8, MN_MAJOR_PAGE>(d, pt, dv, idO, i > 0 ? 1u : 0u);
                 return true;
             };
             for (int i = 0; i < n_tiles && ok; ++i) {

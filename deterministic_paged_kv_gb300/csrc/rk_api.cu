@@ -190,6 +190,16 @@ int make_cache_map(CUtensorMap* m, const void* cache, int num_pages, int Hkv, in
     return make_map(m, cache, 3, dims, strides, box, swz, what);
 }
 
+// The same cache seen as 4-D (64 dims, token row, 64-dim half, head): one box
+// of (64, 16, 2, 1) copies a whole page of one head (4 KiB) and lands as
+// [half][16 rows][128 B], 128-byte swizzled.
+int make_page_map(CUtensorMap* m, const void* cache, int num_pages, int Hkv, const char* what) {
+    const cuuint64_t dims[4] = {64, (cuuint64_t)(num_pages > 0 ? num_pages : 1) * rk::PAGE, 2, (cuuint64_t)Hkv};
+    const cuuint64_t strides[3] = {(cuuint64_t)Hkv * rk::HEAD_DIM * 2, 128, (cuuint64_t)rk::HEAD_DIM * 2};
+    const cuuint32_t box[4] = {64, (cuuint32_t)rk::PAGE, 2, 1};
+    return make_map(m, cache, 4, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B, what);
+}
+
 bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
 int check_launch_common(const rk_paged_plan_t* plan, const void* q, const void* kc, const void* vc,
@@ -289,8 +299,7 @@ int rk_paged_attn_decode(const rk_paged_plan_t* plan, const void* q, const void*
     if ((rc = make_cache_map(&km, have ? k_cache : q, have ? plan->num_pages : 1, have ? plan->Hkv : 1, 64,
                              CU_TENSOR_MAP_SWIZZLE_128B, "k_cache")))
         return rc;
-    if ((rc = make_cache_map(&vm, have ? v_cache : q, have ? plan->num_pages : 1, have ? plan->Hkv : 1, 64,
-                             CU_TENSOR_MAP_SWIZZLE_128B, "v_cache")))
+    if ((rc = make_page_map(&vm, have ? v_cache : q, have ? plan->num_pages : 1, have ? plan->Hkv : 1, "v_cache")))
         return rc;
     rk::DecodeArgs a;
     std::memset(&a, 0, sizeof a);
@@ -341,8 +350,7 @@ int rk_paged_attn_prefill(const rk_paged_plan_t* plan, const void* q, const void
     if ((rc = make_cache_map(&km, have ? k_cache : q, have ? plan->num_pages : 1, have ? plan->Hkv : 1, 64,
                              CU_TENSOR_MAP_SWIZZLE_128B, "k_cache")))
         return rc;
-    if ((rc = make_cache_map(&vm, have ? v_cache : q, have ? plan->num_pages : 1, have ? plan->Hkv : 1, 64,
-                             CU_TENSOR_MAP_SWIZZLE_128B, "v_cache")))
+    if ((rc = make_page_map(&vm, have ? v_cache : q, have ? plan->num_pages : 1, have ? plan->Hkv : 1, "v_cache")))
         return rc;
     rk::PrefillArgs a;
     std::memset(&a, 0, sizeof a);

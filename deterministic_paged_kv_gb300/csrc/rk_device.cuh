@@ -60,14 +60,17 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t byt
                  : "memory");
 }
 
+// A waiting thread is suspended until the phase completes or the hint time
+// passes, so waiting warps leave the issue slots to the working ones.
+constexpr uint32_t RK_SUSPEND_HINT_NS = 20000;
 __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
     uint32_t ok;
     asm volatile(
         "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
         "selp.u32 %0, 1, 0, p;\n\t}"
         : "=r"(ok)
-        : "r"(bar), "r"(parity)
+        : "r"(bar), "r"(parity), "r"(RK_SUSPEND_HINT_NS)
         : "memory");
     return ok != 0;
 }
@@ -115,6 +118,20 @@ __device__ __forceinline__ void mbar_wait_drain(uint32_t bar, uint32_t parity) {
 // Named barrier among `nthreads` threads (ids 1..15; 0 is __syncthreads).
 __device__ __forceinline__ void named_bar_sync(int id, int nthreads) {
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+
+// Named barrier over nthreads threads that also ORs a predicate across them.
+__device__ __forceinline__ bool named_bar_or(int id, int nthreads, bool v) {
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t"
+        "setp.ne.u32 p, %1, 0;\n\t"
+        "bar.red.or.pred q, %2, %3, p;\n\t"
+        "selp.u32 %0, 1, 0, q;\n\t}"
+        : "=r"(r)
+        : "r"((uint32_t)v), "r"(id), "r"(nthreads)
+        : "memory");
+    return r != 0;
 }
 
 // ---------------------------------------------------------------- TMA ----
@@ -205,12 +222,14 @@ __device__ __forceinline__ uint32_t desc_lo(uint32_t saddr, uint32_t lbo_bytes) 
 enum OperandLayout : int {
     K_MAJOR_128 = 0,  // [128 rows][2 x 64 elements] K-major: 64-element blocks 16 KiB apart
     K_MAJOR_16 = 1,   // [16 rows][2 x 64 elements] K-major: blocks 2 KiB apart
-    MN_MAJOR = 2      // [K rows][2 x 64 MN elements]: a k-step is 16 rows = 2 KiB
+    MN_MAJOR = 2,     // [2 x 64 MN elements][K rows]: a k-step is 16 rows = 2 KiB
+    MN_MAJOR_PAGE = 3 // [page][2 x 64 MN elements][16 rows] (LBO 2 KiB): a k-step is one 4 KiB page
 };
 __host__ __device__ constexpr uint32_t kstep_off(int layout, int ks) {
     return layout == K_MAJOR_128 ? (uint32_t)(((ks >> 2) * 16384 + (ks & 3) * 32) >> 4)
            : layout == K_MAJOR_16 ? (uint32_t)(((ks >> 2) * 2048 + (ks & 3) * 32) >> 4)
-                                  : (uint32_t)(ks * (2048 >> 4));
+           : layout == MN_MAJOR   ? (uint32_t)(ks * (2048 >> 4))
+                                  : (uint32_t)(ks * (4096 >> 4));
 }
 // D[tmem] (+)= A[smem] * B[smem], k-steps KS..END-1 of operands with the given
 // layouts; accumulates from k-step 1 on, and at k-step 0 iff acc0.
@@ -391,10 +410,8 @@ __device__ __forceinline__ float2 fadd2(float2 a, float2 b) {
 // Rotate one chunk pair (8 rotate-half pairs: 16 bf16 at lo_ptr / hi_ptr) in FP32
 // and write FP16 in place.  c2 / s2 hold the cos / sin of pairs (2k, 2k+1).
 // Returns the running max of the |input| bf16 bit patterns (FP16 range check).
-__device__ __forceinline__ uint32_t rotate_chunk_f16(uint8_t* lo_ptr, uint8_t* hi_ptr, const float2 (&c2)[4],
-                                                     const float2 (&s2)[4], uint32_t range) {
-    const uint4 a = *reinterpret_cast<const uint4*>(lo_ptr);
-    const uint4 b = *reinterpret_cast<const uint4*>(hi_ptr);
+__device__ __forceinline__ uint32_t rotate_regs_f16(uint4& a, uint4& b, const float2 (&c2)[4], const float2 (&s2)[4],
+                                                    uint32_t range) {
     const uint32_t aw[4] = {a.x, a.y, a.z, a.w};
     const uint32_t bw[4] = {b.x, b.y, b.z, b.w};
     uint32_t ow[4], pw[4];
@@ -410,8 +427,17 @@ __device__ __forceinline__ uint32_t rotate_chunk_f16(uint8_t* lo_ptr, uint8_t* h
         ow[k] = pack_f16x2(x.x, x.y);
         pw[k] = pack_f16x2(y.x, y.y);
     }
-    *reinterpret_cast<uint4*>(lo_ptr) = make_uint4(ow[0], ow[1], ow[2], ow[3]);
-    *reinterpret_cast<uint4*>(hi_ptr) = make_uint4(pw[0], pw[1], pw[2], pw[3]);
+    a = make_uint4(ow[0], ow[1], ow[2], ow[3]);
+    b = make_uint4(pw[0], pw[1], pw[2], pw[3]);
+    return range;
+}
+__device__ __forceinline__ uint32_t rotate_chunk_f16(uint8_t* lo_ptr, uint8_t* hi_ptr, const float2 (&c2)[4],
+                                                     const float2 (&s2)[4], uint32_t range) {
+    uint4 a = *reinterpret_cast<const uint4*>(lo_ptr);
+    uint4 b = *reinterpret_cast<const uint4*>(hi_ptr);
+    range = rotate_regs_f16(a, b, c2, s2, range);
+    *reinterpret_cast<uint4*>(lo_ptr) = a;
+    *reinterpret_cast<uint4*>(hi_ptr) = b;
     return range;
 }
 

@@ -17,14 +17,14 @@ constexpr int ROPE_PAIRS = HEAD_DIM / 2;
 // warpgroup, K and V TMA producer warps and one MMA warp (15 warps).  Tiles
 // of 128 tokens.
 constexpr int DEC_XFORM_THREADS = 256;
-constexpr int DEC_THREADS = 15 * 32;
+constexpr int DEC_THREADS = 16 * 32;
 constexpr int DEC_BN = 128;                           // tokens per KV tile (8 pages)
 constexpr int DEC_KSTAGES = 4;
 constexpr int DEC_VSTAGES = 2;
 constexpr int DEC_TILE_BYTES = DEC_BN * HEAD_DIM * 2;  // 32 KiB
 constexpr int DEC_CTRL_BYTES = 2048;                   // barriers, RoPE tables, reductions
 constexpr int DEC_SMEM_BYTES = (DEC_KSTAGES + DEC_VSTAGES) * DEC_TILE_BYTES + 16 * HEAD_DIM * 2 +
-                               16 * DEC_BN * 2 + DEC_CTRL_BYTES;
+                               2 * 16 * DEC_BN * 2 + DEC_CTRL_BYTES;
 
 struct DecodeArgs {
     const void* q;                // bf16 [B, Hq, 1, D]
