@@ -276,6 +276,44 @@ def measure_prefill(args, dev, stream, world, tf_burst, peak_kind):
     return prefill
 
 
+def measure_decode_long(args, dev, stream, hbm, peak_kind, split_tokens=2048):
+    """Time decode_long (B=1, kv 32768: 8 CTAs without splitting) through the
+    split-free entry point and the fixed-split entry point; L2 flushed between
+    launches.  Returns the "decode_long" object."""
+    import torch
+
+    from deterministic_paged_kv_gb300 import binding, workloads
+    names = ("q", "k_cache", "v_cache", "block_table", "kv_lens", "position_ids")
+    w = workloads.decode_long()
+    d = {k: getattr(w, k).to(dev) for k in names}
+    p = binding.plan(w.B, 1, w.Hq, w.Hkv, w.D, 16, w.num_pages, w.W, w.block_table, w.kv_lens,
+                     w.position_ids, w.rope_theta, w.rope_scale)
+    out = torch.empty_like(d["q"])
+    lse = torch.empty((w.B, w.Hq, 1), dtype=torch.float32, device=dev)
+    scratch = torch.empty(binding.decode_split_scratch_bytes(p, split_tokens), dtype=torch.uint8, device=dev)
+    args_d = (d["q"], d["k_cache"], d["v_cache"], d["block_table"], d["kv_lens"], d["position_ids"], out, lse)
+
+    def free():
+        binding.attn_decode(p, *args_d, stream=stream)
+
+    def split():
+        binding.attn_decode_split(p, split_tokens, *args_d, scratch, stream=stream)
+
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    byt = decode_alg_bytes(w)
+    res = {"config": {"workload": w.name + " page=16", "l2": "flushed (256 MB write) between launches",
+                      "alg_bytes_per_launch": byt, "split_tokens": split_tokens}}
+    for name, fn in (("split_free", free), ("split_%d" % split_tokens, split)):
+        for _ in range(max(3, args.warmup)):
+            fn()
+        torch.cuda.synchronize()
+        t = time_launches(fn, 20, stream, flush=flush)
+        ms = sum(t) / len(t)
+        res[name] = {"value": byt / (ms * 1e-3) / 1e9, "unit": "GB/s", "ms_per_launch": ms,
+                     "frac_of_peak": byt / (ms * 1e-3) / 1e9 / hbm, "peak_kind": peak_kind}
+    return res
+
+
 def run_ours(args):
     import torch
     import torch.distributed as dist
@@ -377,6 +415,7 @@ def run_ours(args):
     d2h = h_out.numel() * 2 + h_lse.numel() * 4
 
     prefill = None if args.no_prefill else measure_prefill(args, dev, stream, world, tf_burst, peak_kind)
+    dlong = None if args.no_long else measure_decode_long(args, dev, stream, hbm, peak_kind)
 
     clk.__exit__(None, None, None)
     cpu = None
@@ -405,6 +444,7 @@ def run_ours(args):
             "clocks": clocks,
             "wall_s_timed_region": wall,
             "prefill": prefill,
+            "decode_long": dlong,
         }
         if args.no_e2e:
             line["e2e"] = line["e2e_resident_cache"] = None
@@ -423,6 +463,8 @@ def main():
     ap.add_argument("--cpu-budget", type=float, default=15.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-long", action="store_true",
+                    help="skip the decode_long object (split-free vs fixed-split decode)")
     ap.add_argument("--no-prefill", action="store_true",
                     help="skip the prefill object (profiling runs of the decode kernel)")
     ap.add_argument("--prefill-only", action="store_true",

@@ -8,8 +8,9 @@ missing, every call raises.
 
 Names mirror the C ABI in ``include/rk_paged.h``:
 ``plan`` (rk_paged_plan), ``attn_decode`` (rk_paged_attn_decode),
-``attn_prefill`` (rk_paged_attn_prefill), ``last_error``, ``policy``,
-``abi_version``.
+``attn_prefill`` (rk_paged_attn_prefill), ``decode_split_scratch_bytes``
+(rk_paged_decode_split_scratch_bytes), ``attn_decode_split``
+(rk_paged_attn_decode_split), ``last_error``, ``policy``, ``abi_version``.
 """
 from __future__ import annotations
 
@@ -75,6 +76,12 @@ def load(path: str | None = None):
             f = getattr(lib, name)
             f.restype = ctypes.c_int
             f.argtypes = [ctypes.POINTER(Plan)] + [vp] * 10
+        lib.rk_paged_decode_split_scratch_bytes.restype = ctypes.c_int
+        lib.rk_paged_decode_split_scratch_bytes.argtypes = [ctypes.POINTER(Plan), ctypes.c_int32,
+                                                            ctypes.POINTER(ctypes.c_uint64)]
+        lib.rk_paged_attn_decode_split.restype = ctypes.c_int
+        lib.rk_paged_attn_decode_split.argtypes = [ctypes.POINTER(Plan), ctypes.c_int32] + [vp] * 9 + \
+            [ctypes.c_uint64, vp, vp]
         lib.rk_last_error.restype = ctypes.c_char_p
         lib.rk_last_error.argtypes = []
         lib.rk_paged_policy.restype = ctypes.c_char_p
@@ -183,9 +190,38 @@ def attn_prefill(p: Plan, q, k_cache, v_cache, block_table, kv_lens, position_id
             position_ids, out, lse, status, stream)
 
 
+def decode_split_scratch_bytes(p: Plan, split_tokens: int) -> int:
+    """rk_paged_decode_split_scratch_bytes: device scratch bytes of the split decode."""
+    n = ctypes.c_uint64(0)
+    _check(load().rk_paged_decode_split_scratch_bytes(ctypes.byref(p), int(split_tokens), ctypes.byref(n)))
+    return int(n.value)
+
+
+def attn_decode_split(p: Plan, split_tokens, q, k_cache, v_cache, block_table, kv_lens, position_ids,
+                      out, lse, scratch, status=None, stream=None):
+    """rk_paged_attn_decode_split on device tensors; ``scratch`` is a CUDA tensor
+    of at least ``decode_split_scratch_bytes`` bytes (any dtype)."""
+    import torch
+    for t, dt, name in ((q, torch.bfloat16, "q"), (k_cache, torch.bfloat16, "k_cache"),
+                        (v_cache, torch.bfloat16, "v_cache"), (out, torch.bfloat16, "out"),
+                        (lse, torch.float32, "lse"), (block_table, torch.int32, "block_table"),
+                        (kv_lens, torch.int32, "kv_lens"), (position_ids, torch.int32, "position_ids")):
+        if t.dtype != dt:
+            raise TypeError("%s must be %s (got %s)" % (name, dt, t.dtype))
+    if status is not None and status.dtype != torch.int32:
+        raise TypeError("status must be int32")
+    nbytes = scratch.numel() * scratch.element_size()
+    rc = load().rk_paged_attn_decode_split(
+        ctypes.byref(p), int(split_tokens), _dptr(q), _dptr(k_cache), _dptr(v_cache), _dptr(block_table),
+        _dptr(kv_lens), _dptr(position_ids), _dptr(out), _dptr(lse), _dptr(scratch), nbytes, _dptr(status),
+        _stream(stream))
+    _check(rc)
+
+
 def run(mode: str, q, k_cache, v_cache, block_table, kv_lens, position_ids, plan_obj=None,
-        rope_theta=1e6, rope_scale=1.0, status=None, stream=None):
-    """Allocate out / lse with torch and launch decode or prefill.
+        rope_theta=1e6, rope_scale=1.0, status=None, stream=None, split_tokens=0):
+    """Allocate out / lse (and the split scratch) with torch and launch decode,
+    split decode (``mode="decode"`` with ``split_tokens`` > 0) or prefill.
 
     ``plan_obj`` defaults to a shape-only plan; pass one built from host
     metadata to have the contents validated first.
@@ -198,6 +234,12 @@ def run(mode: str, q, k_cache, v_cache, block_table, kv_lens, position_ids, plan
                         rope_theta=rope_theta, rope_scale=rope_scale)
     out = torch.empty_like(q)
     lse = torch.empty((B, Hq, Sq), dtype=torch.float32, device=q.device)
+    if mode == "decode" and split_tokens:
+        scratch = torch.empty(decode_split_scratch_bytes(plan_obj, split_tokens), dtype=torch.uint8,
+                              device=q.device)
+        attn_decode_split(plan_obj, split_tokens, q, k_cache, v_cache, block_table, kv_lens, position_ids,
+                          out, lse, scratch, status=status, stream=stream)
+        return out, lse
     fn = attn_decode if mode == "decode" else attn_prefill
     fn(plan_obj, q, k_cache, v_cache, block_table, kv_lens, position_ids, out, lse,
        status=status, stream=stream)

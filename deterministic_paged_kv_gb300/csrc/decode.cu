@@ -83,7 +83,18 @@ struct DecCtrl {
 };
 static_assert(sizeof(DecCtrl) <= DEC_CTRL_BYTES, "decode control block exceeds its reservation");
 
-__device__ __forceinline__ void write_empty_row(const DecodeArgs& a, int b, int h0, float lse_val) {
+// out = 0 and lse = lse_val for the G heads of (b, kv head); in split mode the
+// same for this split's partial (the merge turns NaN / -inf partials into the
+// row's NaN / empty result).
+__device__ __forceinline__ void write_empty_row(const DecodeArgs& a, int b, int h0, int split, float lse_val) {
+    if (a.split_tiles > 0) {
+        for (int i = threadIdx.x; i < a.G * HEAD_DIM; i += blockDim.x) {
+            const int hh = i / HEAD_DIM, d = i % HEAD_DIM;
+            a.o_part[(((size_t)b * a.Hq + h0 + hh) * a.n_splits + split) * HEAD_DIM + d] = 0.0f;
+        }
+        if (threadIdx.x < a.G) a.lse_part[((size_t)b * a.Hq + h0 + threadIdx.x) * a.n_splits + split] = lse_val;
+        return;
+    }
     __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(a.out);
     for (int i = threadIdx.x; i < a.G * HEAD_DIM; i += blockDim.x) {
         const int hh = i / HEAD_DIM, d = i % HEAD_DIM;
@@ -99,7 +110,10 @@ __global__ void __launch_bounds__(DEC_THREADS, 1)
     DecCtrl* ctl = reinterpret_cast<DecCtrl*>(sm + OFF_CTRL);
     const uint32_t s_base = smem_u32(sm);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int kvh = blockIdx.x % a.Hkv, b = blockIdx.x / a.Hkv;
+    // work unit: (split, row, KV head), split-major; split = 0 without splitting
+    const int rows_heads = a.B * a.Hkv;
+    const int split = (int)(blockIdx.x / rows_heads), unit = (int)(blockIdx.x % rows_heads);
+    const int kvh = unit % a.Hkv, b = unit / a.Hkv;
     const int G = a.G, h0 = kvh * G;
     if (s_base & 1023u) {  // the swizzled operand layout needs a 1024-byte aligned base
         if (tid == 0 && a.status) atomicOr(a.status, RK_STATUS_TIMEOUT);
@@ -115,12 +129,18 @@ __global__ void __launch_bounds__(DEC_THREADS, 1)
     const int n_vis = bad ? 0 : (qpos >= kv_len ? kv_len : qpos + 1);
     const int n_pages = (n_vis + PAGE - 1) / PAGE;
     const int n_tiles = (n_vis + DEC_BN - 1) / DEC_BN;
+    // This CTA's KV tiles [i0, i0 + n_loc): the whole row, or one fixed split.
+    const int i0 = a.split_tiles > 0 ? split * a.split_tiles : 0;
+    const int n_loc = a.split_tiles > 0 ? max(0, min(n_tiles, i0 + a.split_tiles) - i0) : n_tiles;
+    constexpr int PPT = DEC_BN / PAGE;  // pages per tile
     // Last page partly filled and inside the visible range: its rows past
-    // kv_len hold arbitrary bits and are zeroed in V after the copy lands.
-    const bool has_tail = n_vis == kv_len && (kv_len & (PAGE - 1)) != 0;
+    // kv_len hold arbitrary bits and are zeroed in V after the copy lands
+    // (by the CTA that holds the row's last tile).
+    const bool has_tail = n_vis == kv_len && (kv_len & (PAGE - 1)) != 0 && n_loc > 0 && i0 + n_loc == n_tiles;
     const int32_t* bt = a.block_table + (size_t)b * a.W;
     int oob = 0;
-    for (int i = tid; i < n_pages; i += DEC_THREADS) {
+    const int pg_end = min(n_pages, (i0 + n_loc) * PPT);  // the pages this CTA reads
+    for (int i = i0 * PPT + tid; i < pg_end; i += DEC_THREADS) {
         const int pg = __ldg(bt + i);
         oob |= (pg < 0) | (pg >= a.num_pages);
     }
@@ -162,11 +182,11 @@ __global__ void __launch_bounds__(DEC_THREADS, 1)
     if (__syncthreads_or(oob)) bad |= RK_STATUS_PAGE_OOB;
     if (bad) {
         if (tid == 0 && a.status) atomicOr(a.status, bad);
-        write_empty_row(a, b, h0, __int_as_float(0x7fc00000));
+        write_empty_row(a, b, h0, split, __int_as_float(0x7fc00000));
         return;
     }
-    if (n_vis == 0) {
-        write_empty_row(a, b, h0, -INFINITY);
+    if (n_loc == 0) {
+        write_empty_row(a, b, h0, split, -INFINITY);
         return;
     }
 
@@ -186,17 +206,18 @@ __global__ void __launch_bounds__(DEC_THREADS, 1)
         const bool is_k = warp == WARP_TMA_K;
         const CUtensorMap* map = is_k ? &kmap : &vmap;
         const int nst = is_k ? DEC_KSTAGES : DEC_VSTAGES;
-        constexpr int PPT = DEC_BN / PAGE;  // pages per tile
         if (lane == 0) prefetch_tmap(map);
         int issued = 0;
-        int pg_next = lane < min(PPT, n_pages) ? __ldg(bt + lane) : 0;
-        for (int i = 0; i < n_tiles; ++i) {
-            const int k = i % nst;
-            const uint32_t use = (uint32_t)(i / nst);
+        int pg_next = lane < min(PPT, n_pages - i0 * PPT) ? __ldg(bt + i0 * PPT + lane) : 0;
+        // it: the CTA's own tile count (stages, phases); i: the row's tile index
+        for (int it = 0; it < n_loc; ++it) {
+            const int i = i0 + it;
+            const int k = it % nst;
+            const uint32_t use = (uint32_t)(it / nst);
             const int np = min(PPT, n_pages - i * PPT);
             const int pg = pg_next;
             const int nxt = (i + 1) * PPT + lane;  // the next tile's page ids, loaded ahead
-            pg_next = (i + 1 < n_tiles && lane < PPT && nxt < n_pages) ? __ldg(bt + nxt) : 0;
+            pg_next = (it + 1 < n_loc && lane < PPT && nxt < n_pages) ? __ldg(bt + nxt) : 0;
             const uint32_t eb = smem_u32(is_k ? &ctl->k_empty[k] : &ctl->v_empty[k]);
             const uint32_t fb = smem_u32(is_k ? &ctl->k_full[k] : &ctl->v_full[k]);
             int good = 1;
@@ -216,7 +237,7 @@ __global__ void __launch_bounds__(DEC_THREADS, 1)
                 }
             }
             __syncwarp();
-            if (!is_k && has_tail && i == n_tiles - 1) {
+            if (!is_k && has_tail && it == n_loc - 1) {
                 // this warp armed the phase it waits for: no parity aliasing
                 const int landed =
                     __shfl_sync(0xffffffffu, lane == 0 ? (int)mbar_wait(fb, use & 1u, abort) : 0, 0);
@@ -254,10 +275,10 @@ __global__ void __launch_bounds__(DEC_THREADS, 1)
                 const uint32_t idS = idesc_f16_f32(DEC_BN, NH);
                 const uint32_t dK0 = desc_lo(s_base + OFF_K, 16), dQT = desc_lo(s_base + OFF_QT, 16);
                 ok = mbar_wait(smem_u32(&ctl->q_ready), 0, abort);
-                for (int i = 0; i < n_tiles && ok; ++i) {
-                    const int k = i % DEC_KSTAGES, sb = i & 1;
-                    ok = mbar_wait(smem_u32(&ctl->k_ready[k]), (uint32_t)((i / DEC_KSTAGES) & 1), abort) &&
-                         (i < 2 || mbar_wait(smem_u32(&ctl->s_free[sb]), (uint32_t)(((i >> 1) - 1) & 1), abort));
+                for (int it = 0; it < n_loc && ok; ++it) {
+                    const int k = it % DEC_KSTAGES, sb = it & 1;
+                    ok = mbar_wait(smem_u32(&ctl->k_ready[k]), (uint32_t)((it / DEC_KSTAGES) & 1), abort) &&
+                         (it < 2 || mbar_wait(smem_u32(&ctl->s_free[sb]), (uint32_t)(((it >> 1) - 1) & 1), abort));
                     if (!ok) break;
                     tc_fence_after();
                     mma_ss_steps<0, 8, K_MAJOR_128, K_MAJOR_16>(tmem + sb * NH, dK0 + (uint32_t)k * TILE_DESC, dQT,
@@ -268,17 +289,17 @@ __global__ void __launch_bounds__(DEC_THREADS, 1)
             } else {
                 const uint32_t idO = idesc_bf16_f32(HEAD_DIM, NH, 1, 0);
                 const uint32_t dV0 = desc_lo(s_base + OFF_V, 2048), dPT = desc_lo(s_base + OFF_PT, 16);
-                for (int i = 0; i < n_tiles && ok; ++i) {
-                    ok = mbar_wait(smem_u32(&ctl->p_ready[i & 1]), (uint32_t)((i >> 1) & 1), abort) &&
-                         mbar_wait(smem_u32(&ctl->v_full[i % DEC_VSTAGES]), (uint32_t)((i / DEC_VSTAGES) & 1), abort) &&
-                         (!(has_tail && i == n_tiles - 1) || mbar_wait(smem_u32(&ctl->v_tail), 0, abort));
+                for (int it = 0; it < n_loc && ok; ++it) {
+                    ok = mbar_wait(smem_u32(&ctl->p_ready[it & 1]), (uint32_t)((it >> 1) & 1), abort) &&
+                         mbar_wait(smem_u32(&ctl->v_full[it % DEC_VSTAGES]), (uint32_t)((it / DEC_VSTAGES) & 1), abort) &&
+                         (!(has_tail && it == n_loc - 1) || mbar_wait(smem_u32(&ctl->v_tail), 0, abort));
                     if (!ok) break;
                     tc_fence_after();
-                    mma_ss_steps<0, 8, MN_MAJOR_PAGE, K_MAJOR_16>(tO, dV0 + (uint32_t)(i % DEC_VSTAGES) * TILE_DESC,
-                                                             dPT + (uint32_t)(i & 1) * (PT_BYTES >> 4), idO,
-                                                             i > 0 ? 1u : 0u);
-                    umma_commit(smem_u32(&ctl->pv_done[i & 1]));
-                    umma_commit(smem_u32(&ctl->v_empty[i % DEC_VSTAGES]));
+                    mma_ss_steps<0, 8, MN_MAJOR_PAGE, K_MAJOR_16>(tO, dV0 + (uint32_t)(it % DEC_VSTAGES) * TILE_DESC,
+                                                             dPT + (uint32_t)(it & 1) * (PT_BYTES >> 4), idO,
+                                                             it > 0 ? 1u : 0u);
+                    umma_commit(smem_u32(&ctl->pv_done[it & 1]));
+                    umma_commit(smem_u32(&ctl->v_empty[it % DEC_VSTAGES]));
                 }
                 if (ok) umma_commit(smem_u32(&ctl->o_done));
             }
@@ -329,12 +350,12 @@ __global__ void __launch_bounds__(DEC_THREADS, 1)
         // (a thread's rows are XF_ROW_STEP apart and the next tile continues the
         // sequence), so at most XF_ANCHOR_TILES * XF_ROWS steps follow an anchor.
         float2 c[4], sn[4];
-        for (int i = 0; i < n_tiles; ++i) {
-            const int k = i % DEC_KSTAGES;
-            if (!mbar_wait(smem_u32(&ctl->k_full[k]), (uint32_t)((i / DEC_KSTAGES) & 1), abort)) break;
+        for (int it = 0; it < n_loc; ++it) {
+            const int i = i0 + it, k = it % DEC_KSTAGES;
+            if (!mbar_wait(smem_u32(&ctl->k_full[k]), (uint32_t)((it / DEC_KSTAGES) & 1), abort)) break;
             uint8_t* kt = sm + OFF_K + k * DEC_TILE_BYTES;
             const int t0 = i * DEC_BN;
-            if (i % XF_ANCHOR_TILES == 0) {
+            if (it == 0 || i % XF_ANCHOR_TILES == 0) {
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
                     rope_cos_sin((uint32_t)(t0 + r0), ctl->turns[8 * u + 2 * e], c[e].x, sn[e].x);
@@ -382,9 +403,9 @@ __global__ void __launch_bounds__(DEC_THREADS, 1)
         // so the four warps leave the loop together and never strand one another
         // at a barrier; a thread whose wait gave up skips its work until then.
         bool ok = true, failed = false;
-        for (int i = 0; i < n_tiles; ++i) {
-            const int sb = i & 1;
-            const bool got = mbar_wait(smem_u32(&ctl->s_full[sb]), (uint32_t)((i >> 1) & 1), abort);
+        for (int it = 0; it < n_loc; ++it) {
+            const int i = i0 + it, sb = it & 1;
+            const bool got = mbar_wait(smem_u32(&ctl->s_full[sb]), (uint32_t)((it >> 1) & 1), abort);
             if (named_bar_or(1, 128, failed || !got)) {
                 ok = false;
                 break;
@@ -432,15 +453,15 @@ __global__ void __launch_bounds__(DEC_THREADS, 1)
             // retired (resc is uniform: every thread saw the same maxima).  One
             // barrier per buffer parity, so a wait never meets a phase of a later PV.
             bool w = true;
-            if (i >= 2) w = mbar_wait(smem_u32(&ctl->pv_done[sb]), (uint32_t)(((i - 2) >> 1) & 1), abort);
-            if (w && resc && i >= 1)
-                w = mbar_wait(smem_u32(&ctl->pv_done[sb ^ 1]), (uint32_t)(((i - 1) >> 1) & 1), abort);
+            if (it >= 2) w = mbar_wait(smem_u32(&ctl->pv_done[sb]), (uint32_t)(((it - 2) >> 1) & 1), abort);
+            if (w && resc && it >= 1)
+                w = mbar_wait(smem_u32(&ctl->pv_done[sb ^ 1]), (uint32_t)(((it - 1) >> 1) & 1), abort);
             if (!__all_sync(0xffffffffu, w)) {
                 failed = true;  // leaves at the next barrier, together with the others
                 continue;
             }
             tc_fence_after();
-            if (resc && i >= 1) {
+            if (resc && it >= 1) {
                 uint32_t orow[16];
                 tmem_ld16(tO + lane_addr, orow);
                 tmem_ld_wait();
@@ -475,7 +496,28 @@ __global__ void __launch_bounds__(DEC_THREADS, 1)
         for (int h = 0; h < 8; ++h) L[h] = ((ctl->lred[0][h] + ctl->lred[1][h]) + ctl->lred[2][h]) + ctl->lred[3][h];
         const bool range_bad = ctl->range_bad != 0;
         __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(a.out);
-        if (ok) {
+        if (a.split_tiles > 0) {
+            // split partial: O / l in FP32 and m + log2(l) (log2 domain); the
+            // merge rescales and sums the splits in ascending order
+            uint32_t orow[16];
+            if (ok) {
+                tc_fence_after();
+                tmem_ld16(tO + lane_addr, orow);
+                tmem_ld_wait();
+            }
+#pragma unroll
+            for (int h = 0; h < 8; ++h) {
+                if (h < G) {
+                    const size_t ph = ((size_t)b * a.Hq + h0 + h) * a.n_splits + split;
+                    const float o = (!ok || range_bad || !(L[h] > 0.0f)) ? 0.0f : __uint_as_float(orow[h]) / L[h];
+                    a.o_part[ph * HEAD_DIM + t] = o;
+                    if (t == h)
+                        a.lse_part[ph] = (!ok || range_bad) ? __int_as_float(0x7fc00000)
+                                                            : (L[h] > 0.0f ? m[h] + log2f(L[h]) : -INFINITY);
+                }
+            }
+            if (t == 0 && a.status && (!ok || range_bad)) atomicOr(a.status, ok ? RK_STATUS_RANGE : RK_STATUS_TIMEOUT);
+        } else if (ok) {
             tc_fence_after();
             uint32_t orow[16];
             tmem_ld16(tO + lane_addr, orow);
@@ -508,6 +550,40 @@ __global__ void __launch_bounds__(DEC_THREADS, 1)
     }
 }
 
+// Ordered merge of the split partials of one (row, query head); thread d owns
+// output dim d.  With M the largest partial LSE (log2 domain), w_s =
+// 2^(lse_s - M), out = sum_s w_s o_s / sum_s w_s and lse = M + log2(sum_s w_s),
+// both sums taken in ascending split order.  A NaN partial (unsafe metadata,
+// FP16 range, timeout) makes the row out = 0, lse = NaN; no visible key at
+// all gives out = 0, lse = -inf.
+__global__ void __launch_bounds__(HEAD_DIM) decode_merge_kernel(const __grid_constant__ DecodeArgs a) {
+    const size_t bh = blockIdx.x;  // b * Hq + h
+    const int d = threadIdx.x;
+    const float* lp = a.lse_part + bh * a.n_splits;
+    const float* op = a.o_part + bh * a.n_splits * HEAD_DIM + d;
+    float M = -INFINITY;
+    bool bad = false;
+    for (int s = 0; s < a.n_splits; ++s) {
+        const float v = lp[s];
+        bad |= v != v;
+        M = fmaxf(M, v);
+    }
+    __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(a.out) + bh * HEAD_DIM;
+    if (bad || M == -INFINITY) {
+        out[d] = __float2bfloat16_rn(0.0f);
+        if (d == 0) a.lse[bh] = bad ? __int_as_float(0x7fc00000) : -INFINITY;
+        return;
+    }
+    float wsum = 0.0f, acc = 0.0f;
+    for (int s = 0; s < a.n_splits; ++s) {
+        const float w = ex2(lp[s] - M);  // 0 for an empty split
+        wsum += w;
+        acc = fmaf(w, op[(size_t)s * HEAD_DIM], acc);
+    }
+    out[d] = __float2bfloat16_rn(acc / wsum);
+    if (d == 0) a.lse[bh] = (M + log2f(wsum)) * 0.693147180559945309f;
+}
+
 }  // namespace
 
 cudaError_t launch_decode(const CUtensorMap& km, const CUtensorMap& vm, const DecodeArgs& a,
@@ -522,10 +598,13 @@ cudaError_t launch_decode(const CUtensorMap& km, const CUtensorMap& vm, const De
         if (e != cudaSuccess) return e;
         configured.fetch_or(bit);
     }
-    const long long grid = (long long)a.B * a.Hkv;
+    const long long grid = (long long)a.B * a.Hkv * (a.split_tiles > 0 ? a.n_splits : 1);
     if (grid <= 0) return cudaSuccess;
     if (grid > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
     decode_kernel<<<(unsigned)grid, DEC_THREADS, DEC_SMEM_BYTES, stream>>>(km, vm, a);
+    e = cudaGetLastError();
+    if (e != cudaSuccess || a.split_tiles <= 0) return e;
+    decode_merge_kernel<<<(unsigned)((long long)a.B * a.Hq), HEAD_DIM, 0, stream>>>(a);
     return cudaGetLastError();
 }
 

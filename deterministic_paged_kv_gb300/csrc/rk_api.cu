@@ -237,7 +237,8 @@ const char* rk_paged_policy(void) {
            "rotary_dim=head_dim;gqa=contiguous_groups;decode_tile=kv128,score_mma=fp16_operands_fp32_acc,"
            "pv_mma=bf16_operands_fp32_acc,l_merge=fixed_tree;"
            "prefill_tile=2xq128xkv128,score_mma=fp16_operands_fp32_acc,pv_mma=bf16_operands_fp32_acc;"
-           "batch_invariant=1;page_size=16;head_dim=128";
+           "batch_invariant=1;page_size=16;head_dim=128;"
+           "decode_split_entry=fixed_splits_of_1024k_tokens,ordered_fp32_merge,separate_policy";
 }
 
 int rk_paged_plan(rk_paged_plan_t* plan, int32_t B, int32_t Sq, int32_t Hq, int32_t Hkv, int32_t D,
@@ -284,15 +285,42 @@ int rk_paged_plan(rk_paged_plan_t* plan, int32_t B, int32_t Sq, int32_t Hq, int3
     return RK_OK;
 }
 
-int rk_paged_attn_decode(const rk_paged_plan_t* plan, const void* q, const void* k_cache,
-                         const void* v_cache, const int32_t* block_table_d, const int32_t* kv_lens_d,
-                         const int32_t* position_ids_d, void* out, float* lse, int32_t* status_d,
-                         rk_stream_t stream) {
+namespace {
+
+// Splits of a row's KV range for split_tokens per split: enough for the
+// widest row the table allows (W pages), at least one.
+int64_t split_count(const rk_paged_plan_t* plan, int32_t split_tokens) {
+    const int64_t cap = (int64_t)plan->W * rk::PAGE;
+    return cap > 0 ? (cap + split_tokens - 1) / split_tokens : 1;
+}
+
+int64_t split_scratch_need(const rk_paged_plan_t* plan, int32_t split_tokens) {
+    const int64_t n = (int64_t)plan->B * plan->Hq * split_count(plan, split_tokens);
+    return n * rk::HEAD_DIM * 4 + n * 4;  // o_part then lse_part
+}
+
+// Shared by the split-free and the split entry points (split_tokens = 0: none).
+int decode_common(const rk_paged_plan_t* plan, int32_t split_tokens, const void* q, const void* k_cache,
+                  const void* v_cache, const int32_t* block_table_d, const int32_t* kv_lens_d,
+                  const int32_t* position_ids_d, void* out, float* lse, void* scratch, uint64_t scratch_bytes,
+                  int32_t* status_d, rk_stream_t stream) {
     g_err.clear();
     int rc = check_launch_common(plan, q, k_cache, v_cache, block_table_d, kv_lens_d, position_ids_d,
                                  out, lse);
     if (rc) return rc;
     if (plan->Sq != 1) return fail(RK_E_ARG, "decode needs a plan with Sq == 1 (got %d)", plan->Sq);
+    if (split_tokens < 0 || (split_tokens > 0 && split_tokens % rk::DEC_SPLIT_GRAIN != 0))
+        return fail(RK_E_ARG, "split_tokens must be a positive multiple of %d (got %d)", rk::DEC_SPLIT_GRAIN,
+                    split_tokens);
+    if (split_tokens > 0) {
+        const int64_t need = split_scratch_need(plan, split_tokens);
+        if (!scratch || !aligned(scratch, 16))
+            return fail(RK_E_ARG, "split decode scratch must be a non-null 16-byte aligned device pointer");
+        if ((uint64_t)need > scratch_bytes)
+            return fail(RK_E_ARG, "split decode scratch too small: %lld bytes needed, %llu given", (long long)need,
+                        (unsigned long long)scratch_bytes);
+        if (split_count(plan, split_tokens) > 0x7fffffffLL) return fail(RK_E_ARG, "too many splits");
+    }
     if (plan->B == 0) return RK_OK;
     const bool have = plan->num_pages > 0;
     CUtensorMap km, vm;
@@ -317,10 +345,51 @@ int rk_paged_attn_decode(const rk_paged_plan_t* plan, const void* q, const void*
     a.W = plan->W;
     a.num_pages = plan->num_pages;
     a.qk_scale_log2 = (float)((1.0 / std::sqrt((double)plan->D)) * 1.4426950408889634074);
+    if (split_tokens > 0) {
+        const int64_t n = (int64_t)plan->B * plan->Hq * split_count(plan, split_tokens);
+        a.split_tiles = split_tokens / rk::DEC_BN;
+        a.n_splits = (int32_t)split_count(plan, split_tokens);
+        a.o_part = static_cast<float*>(scratch);
+        a.lse_part = static_cast<float*>(scratch) + n * rk::HEAD_DIM;
+    }
     std::memcpy(a.rope_turns, plan->rope_turns, sizeof a.rope_turns);
     cudaError_t e = rk::launch_decode(km, vm, a, reinterpret_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return fail(RK_E_CUDA, "decode launch: %s", cudaGetErrorString(e));
     return RK_OK;
+}
+
+}  // namespace
+
+int rk_paged_attn_decode(const rk_paged_plan_t* plan, const void* q, const void* k_cache,
+                         const void* v_cache, const int32_t* block_table_d, const int32_t* kv_lens_d,
+                         const int32_t* position_ids_d, void* out, float* lse, int32_t* status_d,
+                         rk_stream_t stream) {
+    return decode_common(plan, 0, q, k_cache, v_cache, block_table_d, kv_lens_d, position_ids_d, out, lse,
+                         nullptr, 0, status_d, stream);
+}
+
+int rk_paged_decode_split_scratch_bytes(const rk_paged_plan_t* plan, int32_t split_tokens, uint64_t* bytes) {
+    g_err.clear();
+    if (!plan || !bytes) return fail(RK_E_ARG, "plan and bytes must be non-null");
+    if (plan->abi != RK_PAGED_ABI_VERSION) return fail(RK_E_ARG, "plan ABI %u != %u", plan->abi, RK_PAGED_ABI_VERSION);
+    if (split_tokens <= 0 || split_tokens % rk::DEC_SPLIT_GRAIN != 0)
+        return fail(RK_E_ARG, "split_tokens must be a positive multiple of %d (got %d)", rk::DEC_SPLIT_GRAIN,
+                    split_tokens);
+    *bytes = (uint64_t)split_scratch_need(plan, split_tokens);
+    return RK_OK;
+}
+
+int rk_paged_attn_decode_split(const rk_paged_plan_t* plan, int32_t split_tokens, const void* q,
+                               const void* k_cache, const void* v_cache, const int32_t* block_table_d,
+                               const int32_t* kv_lens_d, const int32_t* position_ids_d, void* out, float* lse,
+                               void* scratch, uint64_t scratch_bytes, int32_t* status_d, rk_stream_t stream) {
+    if (split_tokens <= 0) {
+        g_err.clear();
+        return fail(RK_E_ARG, "split_tokens must be a positive multiple of %d (got %d)", rk::DEC_SPLIT_GRAIN,
+                    split_tokens);
+    }
+    return decode_common(plan, split_tokens, q, k_cache, v_cache, block_table_d, kv_lens_d, position_ids_d, out,
+                         lse, scratch, scratch_bytes, status_d, stream);
 }
 
 int rk_paged_attn_prefill(const rk_paged_plan_t* plan, const void* q, const void* k_cache,

@@ -163,6 +163,51 @@ int rk_paged_attn_prefill(const rk_paged_plan_t *plan, const void *q, const void
                           const int32_t *kv_lens_d, const int32_t *position_ids_d, void *out,
                           float *lse, int32_t *status_d, rk_stream_t stream);
 
+/*
+ * Fixed-split decode (a separate arithmetic policy, not bitwise equal to
+ * rk_paged_attn_decode): each row's KV range is cut at fixed logical token
+ * offsets s * split_tokens, every split is reduced by its own CTA in
+ * ascending KV order (FP32 partial O / l and partial LSE), and the partials
+ * are merged in ascending split order in FP32 before the single BF16 write.
+ * The boundaries depend only on the token index, so results stay bitwise
+ * identical across batch composition, table width and graph replay for a
+ * given split_tokens.  Gives a long row more CTAs than its Hkv heads.
+ * Follows "Add FlashInfer RoPE-fused paged attention scaffold", boundary
+ * table (Split-K row: fixed num_splits, merge order fixed by the global block
+ * index) and "flashinfer_fa2 backend for Ada (SM89)", the no-split vs split
+ * kernel table (the cost of disabling splits on long, low-batch rows).
+ *
+ *   split_tokens  a positive multiple of 1024 (RK_E_ARG otherwise).
+ *   n_splits      = ceil(W * page_size / split_tokens), at least 1.
+ *
+ * rk_paged_decode_split_scratch_bytes -- *bytes = the device scratch the
+ * split entry point needs for this plan and split_tokens:
+ * B * Hq * n_splits * (D + 1) * 4.  Host only.
+ */
+int rk_paged_decode_split_scratch_bytes(const rk_paged_plan_t *plan, int32_t split_tokens, uint64_t *bytes);
+
+/*
+ * rk_paged_attn_decode_split -- as rk_paged_attn_decode, plus:
+ *   scratch        DEVICE memory owned by the caller, 16-byte aligned, at
+ *                  least rk_paged_decode_split_scratch_bytes bytes; holds the
+ *                  FP32 partials ([B, Hq, n_splits, D] O / l, then
+ *                  [B, Hq, n_splits] log2-domain LSE).  Nothing in it needs
+ *                  initialising: every partial the merge reads is written
+ *                  first by the same call.  Two calls in flight at once must
+ *                  not share a scratch buffer.
+ *   scratch_bytes  its size.
+ * Two kernel launches on `stream` (splits, then merge).  A split that meets
+ * unsafe metadata or the FP16 range limit makes its row out = 0, lse = NaN
+ * and sets the status bit, as in rk_paged_attn_decode.
+ * Returns RK_E_ARG for a bad split_tokens or a missing / small / misaligned
+ * scratch, otherwise as rk_paged_attn_decode.
+ */
+int rk_paged_attn_decode_split(const rk_paged_plan_t *plan, int32_t split_tokens, const void *q,
+                               const void *k_cache, const void *v_cache, const int32_t *block_table_d,
+                               const int32_t *kv_lens_d, const int32_t *position_ids_d, void *out,
+                               float *lse, void *scratch, uint64_t scratch_bytes, int32_t *status_d,
+                               rk_stream_t stream);
+
 /* Message of the last failing call on this thread ("" if none).  The
  * pointer stays valid until the next library call on the same thread. */
 const char *rk_last_error(void);

@@ -12,8 +12,9 @@ def to_dev(w, device="cuda"):
             ("q", "k_cache", "v_cache", "block_table", "kv_lens", "position_ids")}
 
 
-def run_gpu(w, mode=None, validate=True, status=None, stream=None):
-    """Launch through the C ABI; returns device (out, lse)."""
+def run_gpu(w, mode=None, validate=True, status=None, stream=None, split_tokens=0):
+    """Launch through the C ABI; returns device (out, lse).  split_tokens > 0
+    selects the fixed-split decode entry point."""
     from deterministic_paged_kv_gb300 import binding
     mode = mode or w.mode
     d = to_dev(w)
@@ -23,7 +24,7 @@ def run_gpu(w, mode=None, validate=True, status=None, stream=None):
                          w.kv_lens, w.position_ids, w.rope_theta, w.rope_scale)
     return binding.run(mode, d["q"], d["k_cache"], d["v_cache"], d["block_table"], d["kv_lens"],
                        d["position_ids"], plan_obj=p, rope_theta=w.rope_theta,
-                       rope_scale=w.rope_scale, status=status, stream=stream)
+                       rope_scale=w.rope_scale, status=status, stream=stream, split_tokens=split_tokens)
 
 
 def oracle_ref(w, row_mask=None):
