@@ -10,7 +10,8 @@ Names mirror the C ABI in ``include/rk_paged.h``:
 ``plan`` (rk_paged_plan), ``attn_decode`` (rk_paged_attn_decode),
 ``attn_prefill`` (rk_paged_attn_prefill), ``decode_split_scratch_bytes``
 (rk_paged_decode_split_scratch_bytes), ``attn_decode_split``
-(rk_paged_attn_decode_split), ``last_error``, ``policy``, ``abi_version``.
+(rk_paged_attn_decode_split), ``attn_decode_split_static``
+(rk_paged_attn_decode_split_static), ``last_error``, ``policy``, ``abi_version``.
 """
 from __future__ import annotations
 
@@ -29,6 +30,7 @@ ERRORS = {
 CODES = {v: k for k, v in ERRORS.items()}
 STATUS_PAGE_OOB, STATUS_KVLEN, STATUS_POSITION, STATUS_TIMEOUT, STATUS_RANGE = 1, 2, 4, 8, 16
 ABI_VERSION = 1
+SPLIT_STATIC_SCRATCH_BYTES = 16 << 20  # RK_PAGED_SPLIT_STATIC_SCRATCH_BYTES
 
 
 class RkError(RuntimeError):
@@ -82,6 +84,8 @@ def load(path: str | None = None):
         lib.rk_paged_attn_decode_split.restype = ctypes.c_int
         lib.rk_paged_attn_decode_split.argtypes = [ctypes.POINTER(Plan), ctypes.c_int32] + [vp] * 9 + \
             [ctypes.c_uint64, vp, vp]
+        lib.rk_paged_attn_decode_split_static.restype = ctypes.c_int
+        lib.rk_paged_attn_decode_split_static.argtypes = [ctypes.POINTER(Plan), ctypes.c_int32] + [vp] * 10
         lib.rk_last_error.restype = ctypes.c_char_p
         lib.rk_last_error.argtypes = []
         lib.rk_paged_policy.restype = ctypes.c_char_p
@@ -216,6 +220,14 @@ def attn_decode_split(p: Plan, split_tokens, q, k_cache, v_cache, block_table, k
         _dptr(kv_lens), _dptr(position_ids), _dptr(out), _dptr(lse), _dptr(scratch), nbytes, _dptr(status),
         _stream(stream))
     _check(rc)
+
+
+def attn_decode_split_static(p: Plan, split_tokens, q, k_cache, v_cache, block_table, kv_lens,
+                             position_ids, out, lse, status=None, stream=None):
+    """rk_paged_attn_decode_split_static: the split decode with the library's own
+    static device scratch (no allocation; calls overlapping in time race)."""
+    _launch(lambda pp, *r: load().rk_paged_attn_decode_split_static(pp, int(split_tokens), *r), p, q,
+            k_cache, v_cache, block_table, kv_lens, position_ids, out, lse, status, stream)
 
 
 def run(mode: str, q, k_cache, v_cache, block_table, kv_lens, position_ids, plan_obj=None,

@@ -392,6 +392,60 @@ int rk_paged_attn_decode_split(const rk_paged_plan_t* plan, int32_t split_tokens
                          lse, scratch, scratch_bytes, status_d, stream);
 }
 
+namespace {
+
+// Scratch of rk_paged_attn_decode_split_static: one file-scope device array
+// shared by every call on a device (the library allocates nothing).
+static __device__ __align__(256) unsigned char g_split_scratch[RK_PAGED_SPLIT_STATIC_SCRATCH_BYTES];
+
+// Its device address, looked up once per device (with that device current).
+std::atomic<uintptr_t> g_split_scratch_addr[64];
+
+int split_static_scratch(void** p) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return fail(RK_E_CUDA, "cudaGetDevice: %s", cudaGetErrorString(e));
+    if (dev >= 0 && dev < 64) {
+        const uintptr_t a = g_split_scratch_addr[dev].load();
+        if (a) {
+            *p = reinterpret_cast<void*>(a);
+            return RK_OK;
+        }
+    }
+    void* a = nullptr;
+    e = cudaGetSymbolAddress(&a, g_split_scratch);
+    if (e != cudaSuccess || !a)
+        return fail(RK_E_CUDA, "cudaGetSymbolAddress(split scratch): %s", cudaGetErrorString(e));
+    if (dev >= 0 && dev < 64) g_split_scratch_addr[dev].store(reinterpret_cast<uintptr_t>(a));
+    *p = a;
+    return RK_OK;
+}
+
+}  // namespace
+
+int rk_paged_attn_decode_split_static(const rk_paged_plan_t* plan, int32_t split_tokens, const void* q,
+                                      const void* k_cache, const void* v_cache, const int32_t* block_table_d,
+                                      const int32_t* kv_lens_d, const int32_t* position_ids_d, void* out,
+                                      float* lse, int32_t* status_d, rk_stream_t stream) {
+    g_err.clear();
+    if (!plan) return fail(RK_E_ARG, "plan must be non-null");
+    if (split_tokens <= 0 || split_tokens % rk::DEC_SPLIT_GRAIN != 0)
+        return fail(RK_E_ARG, "split_tokens must be a positive multiple of %d (got %d)", rk::DEC_SPLIT_GRAIN,
+                    split_tokens);
+    if (plan->abi != RK_PAGED_ABI_VERSION) return fail(RK_E_ARG, "plan ABI %u != %u", plan->abi, RK_PAGED_ABI_VERSION);
+    const int64_t need = split_scratch_need(plan, split_tokens);
+    if (need > (int64_t)RK_PAGED_SPLIT_STATIC_SCRATCH_BYTES)
+        return fail(RK_E_ARG, "split partials need %lld bytes, above the %llu-byte static scratch", (long long)need,
+                    (unsigned long long)RK_PAGED_SPLIT_STATIC_SCRATCH_BYTES);
+    void* scratch = nullptr;
+    int rc = split_static_scratch(&scratch);
+    if (rc) return rc;
+    // Nothing in the scratch has to start at zero: the split kernel writes every
+    // partial the merge reads, in the same call, so nothing is cleared here.
+    return decode_common(plan, split_tokens, q, k_cache, v_cache, block_table_d, kv_lens_d, position_ids_d, out,
+                         lse, scratch, RK_PAGED_SPLIT_STATIC_SCRATCH_BYTES, status_d, stream);
+}
+
 int rk_paged_attn_prefill(const rk_paged_plan_t* plan, const void* q, const void* k_cache,
                           const void* v_cache, const int32_t* block_table_d, const int32_t* kv_lens_d,
                           const int32_t* position_ids_d, void* out, float* lse, int32_t* status_d,

@@ -208,6 +208,30 @@ int rk_paged_attn_decode_split(const rk_paged_plan_t *plan, int32_t split_tokens
                                float *lse, void *scratch, uint64_t scratch_bytes, int32_t *status_d,
                                rk_stream_t stream);
 
+/*
+ * rk_paged_attn_decode_split_static -- rk_paged_attn_decode_split without a
+ * caller scratch buffer and without any allocation: the partials live in one
+ * file-scope device array of RK_PAGED_SPLIT_STATIC_SCRATCH_BYTES inside the
+ * library (its address is looked up once per device, with that device
+ * current).  Arguments, results and errors as rk_paged_attn_decode_split,
+ * and in addition:
+ *   RK_E_ARG   rk_paged_decode_split_scratch_bytes(plan, split_tokens) is
+ *              above RK_PAGED_SPLIT_STATIC_SCRATCH_BYTES (nothing launched);
+ *   RK_E_CUDA  the device address of the array could not be obtained.
+ * Nothing in the array needs to start at zero (each call writes every partial
+ * it reads), so nothing is cleared.  The array is shared by every call on the
+ * device: two calls whose kernels overlap in time (different streams, or
+ * different host threads on the same device) race on it and may return wrong
+ * results; serialise such calls or use rk_paged_attn_decode_split with a
+ * scratch buffer per stream.
+ */
+#define RK_PAGED_SPLIT_STATIC_SCRATCH_BYTES (16ull << 20)
+int rk_paged_attn_decode_split_static(const rk_paged_plan_t *plan, int32_t split_tokens, const void *q,
+                                      const void *k_cache, const void *v_cache,
+                                      const int32_t *block_table_d, const int32_t *kv_lens_d,
+                                      const int32_t *position_ids_d, void *out, float *lse,
+                                      int32_t *status_d, rk_stream_t stream);
+
 /* Message of the last failing call on this thread ("" if none).  The
  * pointer stays valid until the next library call on the same thread. */
 const char *rk_last_error(void);
