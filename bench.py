@@ -314,6 +314,41 @@ def measure_decode_long(args, dev, stream, hbm, peak_kind, split_tokens=2048):
     return res
 
 
+def measure_append(args, dev, stream, hbm, peak_kind):
+    """Time rk_paged_kv_append for the prefill-chunk shape (4 rows x 512 new
+    tokens) and the decode-step shape (64 rows x 1 token); L2 flushed between
+    launches.  Bytes = new K and V read once and written once."""
+    import torch
+
+    from deterministic_paged_kv_gb300 import binding, workloads
+    res = {}
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    for name, w, n_new in (("prefill_chunk_append", workloads.prefill_chunk(), 512),
+                           ("decode_step_append", workloads.decode_throughput(), 1)):
+        p = binding.plan(w.B, 1, w.Hq, w.Hkv, w.D, 16, w.num_pages, w.W, w.block_table, w.kv_lens,
+                         w.kv_lens[:, None].clone(), w.rope_theta, w.rope_scale)
+        kc, vc = w.k_cache.to(dev), w.v_cache.to(dev)
+        g = torch.Generator().manual_seed(7)
+        k_new = torch.randn((w.B, n_new, w.Hkv, w.D), generator=g).to(torch.bfloat16).to(dev)
+        v_new = torch.randn((w.B, n_new, w.Hkv, w.D), generator=g).to(torch.bfloat16).to(dev)
+        bt, kl = w.block_table.to(dev), w.kv_lens.to(dev)
+
+        def fn():
+            binding.kv_append(p, n_new, k_new, v_new, bt, kl, kc, vc, stream=stream)
+
+        for _ in range(max(3, args.warmup)):
+            fn()
+        torch.cuda.synchronize()
+        t = time_launches(fn, 20, stream, flush=flush)
+        ms = sum(t) / len(t)
+        byt = 2 * 2 * k_new.numel() * 2
+        res[name] = {"rows": w.B, "new_tokens_per_row": n_new, "bytes_per_launch": byt, "ms_per_launch": ms,
+                     "value": byt / (ms * 1e-3) / 1e9, "unit": "GB/s", "frac_of_peak": byt / (ms * 1e-3) / 1e9 / hbm,
+                     "peak_kind": peak_kind}
+        del kc, vc
+    return res
+
+
 def run_ours(args):
     import torch
     import torch.distributed as dist
@@ -416,6 +451,7 @@ def run_ours(args):
 
     prefill = None if args.no_prefill else measure_prefill(args, dev, stream, world, tf_burst, peak_kind)
     dlong = None if args.no_long else measure_decode_long(args, dev, stream, hbm, peak_kind)
+    append = None if args.no_long else measure_append(args, dev, stream, hbm, peak_kind)
 
     clk.__exit__(None, None, None)
     cpu = None
@@ -445,6 +481,7 @@ def run_ours(args):
             "wall_s_timed_region": wall,
             "prefill": prefill,
             "decode_long": dlong,
+            "kv_append": append,
         }
         if args.no_e2e:
             line["e2e"] = line["e2e_resident_cache"] = None
@@ -464,7 +501,7 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-long", action="store_true",
-                    help="skip the decode_long object (split-free vs fixed-split decode)")
+                    help="skip the decode_long (split-free vs fixed-split decode) and kv_append objects")
     ap.add_argument("--no-prefill", action="store_true",
                     help="skip the prefill object (profiling runs of the decode kernel)")
     ap.add_argument("--prefill-only", action="store_true",

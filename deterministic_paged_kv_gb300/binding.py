@@ -11,7 +11,8 @@ Names mirror the C ABI in ``include/rk_paged.h``:
 ``attn_prefill`` (rk_paged_attn_prefill), ``decode_split_scratch_bytes``
 (rk_paged_decode_split_scratch_bytes), ``attn_decode_split``
 (rk_paged_attn_decode_split), ``attn_decode_split_static``
-(rk_paged_attn_decode_split_static), ``last_error``, ``policy``, ``abi_version``.
+(rk_paged_attn_decode_split_static), ``kv_append`` (rk_paged_kv_append),
+``last_error``, ``policy``, ``abi_version``.
 """
 from __future__ import annotations
 
@@ -86,6 +87,8 @@ def load(path: str | None = None):
             [ctypes.c_uint64, vp, vp]
         lib.rk_paged_attn_decode_split_static.restype = ctypes.c_int
         lib.rk_paged_attn_decode_split_static.argtypes = [ctypes.POINTER(Plan), ctypes.c_int32] + [vp] * 10
+        lib.rk_paged_kv_append.restype = ctypes.c_int
+        lib.rk_paged_kv_append.argtypes = [ctypes.POINTER(Plan), ctypes.c_int32] + [vp] * 8
         lib.rk_last_error.restype = ctypes.c_char_p
         lib.rk_last_error.argtypes = []
         lib.rk_paged_policy.restype = ctypes.c_char_p
@@ -228,6 +231,24 @@ def attn_decode_split_static(p: Plan, split_tokens, q, k_cache, v_cache, block_t
     static device scratch (no allocation; calls overlapping in time race)."""
     _launch(lambda pp, *r: load().rk_paged_attn_decode_split_static(pp, int(split_tokens), *r), p, q,
             k_cache, v_cache, block_table, kv_lens, position_ids, out, lse, status, stream)
+
+
+def kv_append(p: Plan, n_new, k_new, v_new, block_table, kv_lens, k_cache, v_cache, status=None,
+              stream=None):
+    """rk_paged_kv_append: write k_new / v_new (bf16 [B, n_new, Hkv, D]) into the
+    pages of positions kv_len - n_new .. kv_len - 1 (kv_lens after the append)."""
+    import torch
+    for t, dt, name in ((k_new, torch.bfloat16, "k_new"), (v_new, torch.bfloat16, "v_new"),
+                        (k_cache, torch.bfloat16, "k_cache"), (v_cache, torch.bfloat16, "v_cache"),
+                        (block_table, torch.int32, "block_table"), (kv_lens, torch.int32, "kv_lens")):
+        if t.dtype != dt:
+            raise TypeError("%s must be %s (got %s)" % (name, dt, t.dtype))
+    if status is not None and status.dtype != torch.int32:
+        raise TypeError("status must be int32")
+    rc = load().rk_paged_kv_append(ctypes.byref(p), int(n_new), _dptr(k_new), _dptr(v_new), _dptr(block_table),
+                                   _dptr(kv_lens), _dptr(k_cache), _dptr(v_cache), _dptr(status),
+                                   _stream(stream))
+    _check(rc)
 
 
 def run(mode: str, q, k_cache, v_cache, block_table, kv_lens, position_ids, plan_obj=None,

@@ -22,6 +22,7 @@ cudaError_t launch_decode(const CUtensorMap& km, const CUtensorMap& vm, const De
                           cudaStream_t stream);
 cudaError_t launch_prefill(const CUtensorMap& qm, const CUtensorMap& km, const CUtensorMap& vm,
                            const PrefillArgs& a, cudaStream_t stream);
+cudaError_t launch_kv_append(const AppendArgs& a, cudaStream_t stream);
 }  // namespace rk
 
 namespace {
@@ -444,6 +445,46 @@ int rk_paged_attn_decode_split_static(const rk_paged_plan_t* plan, int32_t split
     // partial the merge reads, in the same call, so nothing is cleared here.
     return decode_common(plan, split_tokens, q, k_cache, v_cache, block_table_d, kv_lens_d, position_ids_d, out,
                          lse, scratch, RK_PAGED_SPLIT_STATIC_SCRATCH_BYTES, status_d, stream);
+}
+
+int rk_paged_kv_append(const rk_paged_plan_t* plan, int32_t n_new, const void* k_new, const void* v_new,
+                       const int32_t* block_table_d, const int32_t* kv_lens_d, void* k_cache, void* v_cache,
+                       int32_t* status_d, rk_stream_t stream) {
+    g_err.clear();
+    if (!plan) return fail(RK_E_ARG, "plan is NULL");
+    if (plan->abi != RK_PAGED_ABI_VERSION)
+        return fail(RK_E_ARG, "plan ABI %u does not match library ABI %u (plan not filled by rk_paged_plan?)",
+                    plan->abi, RK_PAGED_ABI_VERSION);
+    int rc = check_shape(plan->B, plan->Sq, plan->Hq, plan->Hkv, plan->D, plan->page_size, plan->num_pages,
+                         plan->W, plan->rope_theta, plan->rope_scale);
+    if (rc) return rc;
+    if (n_new < 0) return fail(RK_E_ARG, "n_new must be >= 0 (got %d)", n_new);
+    if (plan->B == 0 || n_new == 0) return RK_OK;
+    if (plan->W == 0 || plan->num_pages == 0)
+        return fail(RK_E_KVLEN, "appending %d tokens needs a non-empty block table and page pool", n_new);
+    if (!k_new || !v_new || !block_table_d || !kv_lens_d || !k_cache || !v_cache)
+        return fail(RK_E_ARG, "null device pointer");
+    if (!aligned(k_new, 16) || !aligned(v_new, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16))
+        return fail(RK_E_ARG, "k_new, v_new, k_cache and v_cache must be 16-byte aligned");
+    if (!aligned(block_table_d, 4) || !aligned(kv_lens_d, 4)) return fail(RK_E_ARG, "metadata must be 4-byte aligned");
+    if ((rc = check_device())) return rc;
+    rk::AppendArgs a;
+    std::memset(&a, 0, sizeof a);
+    a.k_new = k_new;
+    a.v_new = v_new;
+    a.block_table = block_table_d;
+    a.kv_lens = kv_lens_d;
+    a.k_cache = k_cache;
+    a.v_cache = v_cache;
+    a.status = status_d;
+    a.B = plan->B;
+    a.n_new = n_new;
+    a.Hkv = plan->Hkv;
+    a.W = plan->W;
+    a.num_pages = plan->num_pages;
+    cudaError_t e = rk::launch_kv_append(a, reinterpret_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return fail(RK_E_CUDA, "append launch: %s", cudaGetErrorString(e));
+    return RK_OK;
 }
 
 int rk_paged_attn_prefill(const rk_paged_plan_t* plan, const void* q, const void* k_cache,

@@ -70,4 +70,17 @@ struct PrefillArgs {
     uint64_t rope_turns[ROPE_PAIRS];
 };
 
+// ------------------------------------------------------------ append ----
+// Write n_new tokens per row into the page cache (kv_lens after the append).
+struct AppendArgs {
+    const void* k_new;            // bf16 [B, n_new, Hkv, D]
+    const void* v_new;            // bf16 [B, n_new, Hkv, D]
+    const int32_t* block_table;   // [B, W]
+    const int32_t* kv_lens;       // [B], lengths including the new tokens
+    void* k_cache;                // bf16 [num_pages, 16, Hkv, D]
+    void* v_cache;
+    int32_t* status;
+    int32_t B, n_new, Hkv, W, num_pages;
+};
+
 }  // namespace rk

@@ -232,6 +232,34 @@ int rk_paged_attn_decode_split_static(const rk_paged_plan_t *plan, int32_t split
                                       const int32_t *position_ids_d, void *out, float *lse,
                                       int32_t *status_d, rk_stream_t stream);
 
+/*
+ * rk_paged_kv_append -- write new tokens' K and V into their pages, as the
+ * cache holds them: pre-RoPE (the attention calls rotate K when they read
+ * it; "WS2 PR7 ...", "FlashInfer RoPE Fusion").  The page walk is the one of
+ * the attention calls: position t of row b is slot t % 16 of page
+ * block_table_d[b, t / 16].
+ *   n_new         tokens per row (>= 0; 0 is a no-op).
+ *   k_new, v_new  bf16 [B, n_new, Hkv, D] DEVICE, contiguous, 16-byte aligned.
+ *   kv_lens_d     [B] lengths AFTER the append: the new tokens of row b take
+ *                 positions kv_len - n_new .. kv_len - 1 (a prefill chunk's
+ *                 K/V is in the cache before its attention runs).  The caller
+ *                 updates kv_lens and allocates the pages first; a plan built
+ *                 on those host values validates them.
+ *   k_cache, v_cache  bf16 [num_pages, 16, Hkv, D] DEVICE, written in place.
+ *   status_d      RK_STATUS_KVLEN when kv_len < n_new or > W * 16,
+ *                 RK_STATUS_PAGE_OOB when a target page id is outside
+ *                 [0, num_pages): that token is not written (never out of
+ *                 bounds).  May be NULL.
+ * Plan: only B, Hkv, D, page_size, W, num_pages are used (Sq is ignored).
+ * One launch on `stream`, no allocation, no host synchronisation.  Errors:
+ * RK_E_ARG (null / misaligned pointer, n_new < 0, plan mismatch),
+ * RK_E_KVLEN (tokens to append but an empty table or pool), RK_E_DEVICE,
+ * RK_E_CUDA.
+ */
+int rk_paged_kv_append(const rk_paged_plan_t *plan, int32_t n_new, const void *k_new, const void *v_new,
+                       const int32_t *block_table_d, const int32_t *kv_lens_d, void *k_cache,
+                       void *v_cache, int32_t *status_d, rk_stream_t stream);
+
 /* Message of the last failing call on this thread ("" if none).  The
  * pointer stays valid until the next library call on the same thread. */
 const char *rk_last_error(void);
