@@ -349,6 +349,40 @@ def measure_append(args, dev, stream, hbm, peak_kind):
     return res
 
 
+def measure_ragged(args, dev, stream):
+    """Time one mixed serving step through rk_paged_attn_ragged: 60 decode rows
+    (one query, kv 2048) and 4 prefill chunks (512 queries at 1536..2047) packed
+    in one call; L2 flushed between launches."""
+    import torch
+
+    from deterministic_paged_kv_gb300 import binding, workloads
+    q_lens = [1] * 60 + [512] * 4
+    w = workloads.ragged_case(q_lens, [2048] * 64, seed=1007)
+    q, ind, pos = workloads.pack_ragged(w)
+    p, mq = binding.plan_ragged(w.B, q.shape[0], w.Hq, w.Hkv, w.D, 16, w.num_pages, w.W, ind, w.block_table,
+                                w.kv_lens, pos, w.rope_theta, w.rope_scale)
+    kc, vc, bt, kl = w.k_cache.to(dev), w.v_cache.to(dev), w.block_table.to(dev), w.kv_lens.to(dev)
+    dq, dind, dpos = q.to(dev), ind.to(dev), pos.to(dev)
+    out = torch.empty((q.shape[0], w.Hq, w.D), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((q.shape[0], w.Hq), dtype=torch.float32, device=dev)
+
+    def fn():
+        binding.attn_ragged(p, mq, dind, dq, kc, vc, bt, kl, dpos, out, lse, stream=stream)
+
+    for _ in range(max(3, args.warmup)):
+        fn()
+    torch.cuda.synchronize()
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    t = time_launches(fn, 20, stream, flush=flush)
+    ms = sum(t) / len(t)
+    dec_bytes = 60 * 2048 * w.Hkv * w.D * 2 * 2
+    pf_flops = 4.0 * w.D * w.Hq * 4 * sum(1536 + s + 1 for s in range(512))
+    return {"workload": "ragged step: 60 decode rows (kv 2048) + 4 prefill chunks (512 at 1536..2047)",
+            "l2": "flushed (256 MB write) between launches", "ms_per_launch": ms,
+            "decode_rows_kv_bytes": dec_bytes, "prefill_rows_flops": pf_flops,
+            "note": "one call, two launches (decode rows, prefill rows)"}
+
+
 def run_ours(args):
     import torch
     import torch.distributed as dist
@@ -452,6 +486,7 @@ def run_ours(args):
     prefill = None if args.no_prefill else measure_prefill(args, dev, stream, world, tf_burst, peak_kind)
     dlong = None if args.no_long else measure_decode_long(args, dev, stream, hbm, peak_kind)
     append = None if args.no_long else measure_append(args, dev, stream, hbm, peak_kind)
+    ragged = None if args.no_long else measure_ragged(args, dev, stream)
 
     clk.__exit__(None, None, None)
     cpu = None
@@ -482,6 +517,7 @@ def run_ours(args):
             "prefill": prefill,
             "decode_long": dlong,
             "kv_append": append,
+            "ragged_step": ragged,
         }
         if args.no_e2e:
             line["e2e"] = line["e2e_resident_cache"] = None
@@ -501,7 +537,7 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-long", action="store_true",
-                    help="skip the decode_long (split-free vs fixed-split decode) and kv_append objects")
+                    help="skip the decode_long (split-free vs fixed-split decode), kv_append and ragged_step objects")
     ap.add_argument("--no-prefill", action="store_true",
                     help="skip the prefill object (profiling runs of the decode kernel)")
     ap.add_argument("--prefill-only", action="store_true",

@@ -12,6 +12,7 @@ Names mirror the C ABI in ``include/rk_paged.h``:
 (rk_paged_decode_split_scratch_bytes), ``attn_decode_split``
 (rk_paged_attn_decode_split), ``attn_decode_split_static``
 (rk_paged_attn_decode_split_static), ``kv_append`` (rk_paged_kv_append),
+``plan_ragged`` (rk_paged_plan_ragged), ``attn_ragged`` (rk_paged_attn_ragged),
 ``last_error``, ``policy``, ``abi_version``.
 """
 from __future__ import annotations
@@ -89,6 +90,11 @@ def load(path: str | None = None):
         lib.rk_paged_attn_decode_split_static.argtypes = [ctypes.POINTER(Plan), ctypes.c_int32] + [vp] * 10
         lib.rk_paged_kv_append.restype = ctypes.c_int
         lib.rk_paged_kv_append.argtypes = [ctypes.POINTER(Plan), ctypes.c_int32] + [vp] * 8
+        lib.rk_paged_plan_ragged.restype = ctypes.c_int
+        lib.rk_paged_plan_ragged.argtypes = [ctypes.POINTER(Plan)] + [ctypes.c_int32] * 8 + \
+            [i32p, i32p, i32p, i32p, ctypes.c_double, ctypes.c_double, ctypes.POINTER(ctypes.c_int32)]
+        lib.rk_paged_attn_ragged.restype = ctypes.c_int
+        lib.rk_paged_attn_ragged.argtypes = [ctypes.POINTER(Plan), ctypes.c_int32] + [vp] * 11
         lib.rk_last_error.restype = ctypes.c_char_p
         lib.rk_last_error.argtypes = []
         lib.rk_paged_policy.restype = ctypes.c_char_p
@@ -249,6 +255,31 @@ def kv_append(p: Plan, n_new, k_new, v_new, block_table, kv_lens, k_cache, v_cac
                                    _dptr(kv_lens), _dptr(k_cache), _dptr(v_cache), _dptr(status),
                                    _stream(stream))
     _check(rc)
+
+
+def plan_ragged(B, total_q, Hq, Hkv, D, page_size, num_pages, W, qo_indptr, block_table=None, kv_lens=None,
+                position_ids=None, rope_theta=1e6, rope_scale=1.0):
+    """rk_paged_plan_ragged on HOST metadata; returns (plan, max_q_len)."""
+    lib = load()
+    p = Plan()
+    mq = ctypes.c_int32(0)
+    keep = [_host_i32(x) for x in (qo_indptr, block_table, kv_lens, position_ids)]
+    rc = lib.rk_paged_plan_ragged(ctypes.byref(p), int(B), int(total_q), int(Hq), int(Hkv), int(D),
+                                  int(page_size), int(num_pages), int(W), keep[0][1], keep[1][1], keep[2][1],
+                                  keep[3][1], float(rope_theta), float(rope_scale), ctypes.byref(mq))
+    _check(rc)
+    return p, int(mq.value)
+
+
+def attn_ragged(p: Plan, max_q_len, qo_indptr, q, k_cache, v_cache, block_table, kv_lens, position_ids, out,
+                lse, status=None, stream=None):
+    """rk_paged_attn_ragged on device tensors: q / out [total_q, Hq, D],
+    lse [total_q, Hq], position_ids [total_q], qo_indptr [B + 1]."""
+    import torch
+    if qo_indptr.dtype != torch.int32:
+        raise TypeError("qo_indptr must be int32")
+    _launch(lambda pp, *r: load().rk_paged_attn_ragged(pp, int(max_q_len), _dptr(qo_indptr), *r), p, q,
+            k_cache, v_cache, block_table, kv_lens, position_ids, out, lse, status, stream)
 
 
 def run(mode: str, q, k_cache, v_cache, block_table, kv_lens, position_ids, plan_obj=None,

@@ -86,7 +86,8 @@ static_assert(sizeof(DecCtrl) <= DEC_CTRL_BYTES, "decode control block exceeds i
 // out = 0 and lse = lse_val for the G heads of (b, kv head); in split mode the
 // same for this split's partial (the merge turns NaN / -inf partials into the
 // row's NaN / empty result).
-__device__ __forceinline__ void write_empty_row(const DecodeArgs& a, int b, int h0, int split, float lse_val) {
+__device__ __forceinline__ void write_empty_row(const DecodeArgs& a, int b, int tq, int h0, int split,
+                                                float lse_val) {
     if (a.split_tiles > 0) {
         for (int i = threadIdx.x; i < a.G * HEAD_DIM; i += blockDim.x) {
             const int hh = i / HEAD_DIM, d = i % HEAD_DIM;
@@ -98,9 +99,9 @@ __device__ __forceinline__ void write_empty_row(const DecodeArgs& a, int b, int 
     __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(a.out);
     for (int i = threadIdx.x; i < a.G * HEAD_DIM; i += blockDim.x) {
         const int hh = i / HEAD_DIM, d = i % HEAD_DIM;
-        out[((size_t)b * a.Hq + h0 + hh) * HEAD_DIM + d] = __float2bfloat16_rn(0.0f);
+        out[((size_t)tq * a.Hq + h0 + hh) * HEAD_DIM + d] = __float2bfloat16_rn(0.0f);
     }
-    if (threadIdx.x < a.G) a.lse[(size_t)b * a.Hq + h0 + threadIdx.x] = lse_val;
+    if (threadIdx.x < a.G) a.lse[(size_t)tq * a.Hq + h0 + threadIdx.x] = lse_val;
 }
 
 __global__ void __launch_bounds__(DEC_THREADS, 1)
@@ -121,8 +122,18 @@ __global__ void __launch_bounds__(DEC_THREADS, 1)
     }
 
     // ---- row metadata (device copy) and memory-safety checks ----
+    int tq = b;  // the row's query: padded row b, or its packed row in a ragged batch
+    if (a.qo_indptr) {
+        const int qs = a.qo_indptr[b], qe = a.qo_indptr[b + 1];
+        if (qs < 0 || qe < qs || qe > a.total_q) {  // unsafe: nowhere safe to write
+            if (tid == 0 && a.status) atomicOr(a.status, RK_STATUS_POSITION);
+            return;
+        }
+        if (qe - qs != 1) return;  // no query, or a prefill row
+        tq = qs;
+    }
     const int kv_len = a.kv_lens[b];
-    const int qpos = a.position_ids[b];
+    const int qpos = a.position_ids[tq];
     int bad = 0;
     if (kv_len < 0 || kv_len > a.W * PAGE) bad |= RK_STATUS_KVLEN;
     if (qpos < 0) bad |= RK_STATUS_POSITION;
@@ -182,11 +193,11 @@ __global__ void __launch_bounds__(DEC_THREADS, 1)
     if (__syncthreads_or(oob)) bad |= RK_STATUS_PAGE_OOB;
     if (bad) {
         if (tid == 0 && a.status) atomicOr(a.status, bad);
-        write_empty_row(a, b, h0, split, __int_as_float(0x7fc00000));
+        write_empty_row(a, b, tq, h0, split, __int_as_float(0x7fc00000));
         return;
     }
     if (n_loc == 0) {
-        write_empty_row(a, b, h0, split, -INFINITY);
+        write_empty_row(a, b, tq, h0, split, -INFINITY);
         return;
     }
 
@@ -318,7 +329,7 @@ __global__ void __launch_bounds__(DEC_THREADS, 1)
             if (tid < G * 8) {
                 const int h = tid >> 3, u = tid & 7;
                 const uint4* row = reinterpret_cast<const uint4*>(reinterpret_cast<const __nv_bfloat16*>(a.q) +
-                                                                  ((size_t)b * a.Hq + h0 + h) * HEAD_DIM);
+                                                                  ((size_t)tq * a.Hq + h0 + h) * HEAD_DIM);
                 __align__(16) uint8_t tmp[32];
                 *reinterpret_cast<uint4*>(tmp) = __ldg(row + u);
                 *reinterpret_cast<uint4*>(tmp + 16) = __ldg(row + 8 + u);
@@ -526,13 +537,13 @@ __global__ void __launch_bounds__(DEC_THREADS, 1)
             for (int h = 0; h < 8; ++h) {
                 if (h < G) {
                     const float o = (range_bad || !(L[h] > 0.0f)) ? 0.0f : __uint_as_float(orow[h]) / L[h];
-                    out[((size_t)b * a.Hq + h0 + h) * HEAD_DIM + t] = __float2bfloat16_rn(o);
+                    out[((size_t)tq * a.Hq + h0 + h) * HEAD_DIM + t] = __float2bfloat16_rn(o);
                 }
             }
 #pragma unroll
             for (int h = 0; h < 8; ++h)
                 if (t == h && h < G)
-                    a.lse[(size_t)b * a.Hq + h0 + h] =
+                    a.lse[(size_t)tq * a.Hq + h0 + h] =
                         range_bad ? __int_as_float(0x7fc00000)
                                   : (L[h] > 0.0f ? (m[h] + log2f(L[h])) * 0.693147180559945309f : -INFINITY);
             if (range_bad && t == 0 && a.status) atomicOr(a.status, RK_STATUS_RANGE);

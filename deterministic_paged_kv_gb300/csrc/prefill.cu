@@ -89,16 +89,27 @@ struct TileInfo {
     int n_tiles;  // KV tiles it needs
 };
 
-__device__ __forceinline__ void write_rows(const PrefillArgs& a, int b, int kvh, int s0, float lse_val) {
+// Where a row's queries live: padded rows (s of row b at [b, h, s]) or a
+// ragged batch (packed rows qbase .. qbase + qn - 1 at [qbase + s, h]).
+struct RowMap {
+    int b, qn, qbase;
+    bool ragged;
+    // index of (query s, head h) in lse; times HEAD_DIM in out
+    __device__ __forceinline__ size_t at(const PrefillArgs& a, int h, int s) const {
+        return ragged ? (size_t)(qbase + s) * a.Hq + h : ((size_t)b * a.Hq + h) * a.Sq + s;
+    }
+};
+
+__device__ __forceinline__ void write_rows(const PrefillArgs& a, const RowMap& rm, int kvh, int s0, float lse_val) {
     __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(a.out);
     const int rph = a.rows_per_head;
     for (int r = threadIdx.x; r < PF_BM; r += blockDim.x) {
         const int g = r / rph, s = s0 + r % rph;
-        if (s >= a.Sq) continue;
+        if (s >= rm.qn) continue;
         const int h = kvh * a.G + g;
-        uint4* o = reinterpret_cast<uint4*>(out + (((size_t)b * a.Hq + h) * a.Sq + s) * HEAD_DIM);
+        uint4* o = reinterpret_cast<uint4*>(out + rm.at(a, h, s) * HEAD_DIM);
         for (int d = 0; d < HEAD_DIM / 8; ++d) o[d] = make_uint4(0, 0, 0, 0);
-        a.lse[((size_t)b * a.Hq + h) * a.Sq + s] = lse_val;
+        a.lse[rm.at(a, h, s)] = lse_val;
     }
 }
 
@@ -124,8 +135,20 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
     const int rph = a.rows_per_head;
 
     // ---- row metadata (device copy) and memory-safety checks ----
+    RowMap rm{b, a.Sq, b * a.Sq, a.qo_indptr != nullptr};
+    if (rm.ragged) {
+        const int qs = a.qo_indptr[b], qe = a.qo_indptr[b + 1];
+        if (qs < 0 || qe < qs || qe > a.total_q || qe - qs > a.n_qtiles * rph) {
+            // unsafe, or more queries than the grid covers: nothing written
+            if (threadIdx.x == 0 && a.status) atomicOr(a.status, RK_STATUS_POSITION);
+            return;
+        }
+        if (qe - qs < 2) return;  // no query, or a single-query row (decode kernel)
+        rm.qn = qe - qs;
+        rm.qbase = qs;
+    }
     const int kv_len = a.kv_lens[b];
-    const int32_t* pos_row = a.position_ids + (size_t)b * a.Sq;
+    const int32_t* pos_row = a.position_ids + rm.qbase;
     int bad = 0;
     if (kv_len < 0 || kv_len > a.W * PAGE) bad |= RK_STATUS_KVLEN;
     TileInfo ti[2];
@@ -133,7 +156,7 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
     for (int j = 0; j < 2; ++j) {
         ti[j].s0 = (2 * pair + j) * rph;
         int pmax = -1;
-        for (int s = ti[j].s0; s < min(ti[j].s0 + rph, a.Sq); ++s) {
+        for (int s = ti[j].s0; s < min(ti[j].s0 + rph, rm.qn); ++s) {
             const int p = pos_row[s];
             if (p < 0) bad |= RK_STATUS_POSITION;
             pmax = max(pmax, p);
@@ -191,8 +214,8 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
     if (bad || n_tiles == 0) {
         if (bad && tid == 0 && a.status) atomicOr(a.status, bad);
         const float lv = bad ? __int_as_float(0x7fc00000) : -INFINITY;
-        write_rows(a, b, kvh, ti[0].s0, lv);
-        write_rows(a, b, kvh, ti[1].s0, lv);
+        write_rows(a, rm, kvh, ti[0].s0, lv);
+        write_rows(a, rm, kvh, ti[1].s0, lv);
         return;
     }
 
@@ -222,9 +245,14 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
                     const uint32_t qb = smem_u32(&bars->q_full);
                     mbar_arrive_expect_tx(qb, 2 * PF_TILE_BYTES);
                     for (int j = 0; j < 2; ++j) {
-                        tma_load_4d(s_base + OFF_Q + j * PF_TILE_BYTES, &qmap, qb, 0, ti[j].s0, kvh * a.G, b);
-                        tma_load_4d(s_base + OFF_Q + j * PF_TILE_BYTES + 16384, &qmap, qb, 64, ti[j].s0,
-                                    kvh * a.G, b);
+                        const uint32_t dq = s_base + OFF_Q + j * PF_TILE_BYTES;
+                        if (rm.ragged) {  // packed q seen as (d, token, head): rows past the row's end are masked
+                            tma_load_3d(dq, &qmap, qb, 0, rm.qbase + ti[j].s0, kvh * a.G);
+                            tma_load_3d(dq + 16384, &qmap, qb, 64, rm.qbase + ti[j].s0, kvh * a.G);
+                        } else {
+                            tma_load_4d(dq, &qmap, qb, 0, ti[j].s0, kvh * a.G, b);
+                            tma_load_4d(dq + 16384, &qmap, qb, 64, ti[j].s0, kvh * a.G, b);
+                        }
                     }
                 }
             }
@@ -361,7 +389,7 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
             for (int j = 0; j < 2 && got; ++j) {
                 const int r = tid;
                 const int s = ti[j].s0 + r % rph;
-                const int p = s < a.Sq ? pos_row[s] : 0;
+                const int p = s < rm.qn ? pos_row[s] : 0;
                 uint8_t* qt = sm + OFF_Q + j * PF_TILE_BYTES;
 #pragma unroll 1
                 for (int u = 0; u < 8; ++u) {
@@ -372,7 +400,10 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
                         rope_cos_sin((uint32_t)p, bars->turns[8 * u + 2 * e + 1], c[e].y, sn[e].y);
                     }
                     const uint32_t off = sw_off(r, u);
-                    range = rotate_chunk_f16(qt + off, qt + 16384 + off, c, sn, range);
+                    // only the row's own queries count for the range check (in a
+                    // ragged batch the rows past its end hold the next row's queries)
+                    const uint32_t nr = rotate_chunk_f16(qt + off, qt + 16384 + off, c, sn, range);
+                    if (s < rm.qn) range = nr;
                 }
             }
             if (range_exceeded(range)) bars->range_bad = 1;
@@ -420,7 +451,7 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
         const uint32_t lane_addr = (uint32_t)((warp & 3) * 32) << 16;
         const uint32_t tS = tmem + j * 128, tO = tmem + 256 + j * 128;
         const int g = r / rph, s = ti[j].s0 + r % rph;
-        const bool valid = s < a.Sq;
+        const bool valid = s < rm.qn;
         const int p = valid ? pos_row[s] : -1;
         const int n_vis = valid ? (p >= kv_len ? kv_len : p + 1) : 0;
         const float scl = a.qk_scale_log2;
@@ -502,7 +533,7 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
         const bool range_bad = bars->range_bad != 0;
         __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(a.out);
         const int h = kvh * a.G + g;
-        uint4* o = reinterpret_cast<uint4*>(out + (((size_t)b * a.Hq + h) * a.Sq + (valid ? s : 0)) * HEAD_DIM);
+        uint4* o = reinterpret_cast<uint4*>(out + rm.at(a, h, valid ? s : 0) * HEAD_DIM);
         if (ok && nt > 0) {
             tc_fence_after();
             const bool zero = range_bad || !(l > 0.0f);
@@ -524,13 +555,13 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
                 }
             }
             if (valid)
-                a.lse[((size_t)b * a.Hq + h) * a.Sq + s] =
+                a.lse[rm.at(a, h, s)] =
                     range_bad ? __int_as_float(0x7fc00000)
                               : (l > 0.0f ? (m + log2f(l)) * 0.693147180559945309f : -INFINITY);
             if (range_bad && r == 0 && a.status) atomicOr(a.status, RK_STATUS_RANGE);
         } else if (nt == 0 && valid) {
             for (int d = 0; d < HEAD_DIM / 8; ++d) o[d] = make_uint4(0, 0, 0, 0);
-            a.lse[((size_t)b * a.Hq + h) * a.Sq + s] = -INFINITY;
+            a.lse[rm.at(a, h, s)] = -INFINITY;
         } else if (!ok && r == 0 && a.status) {
             atomicOr(a.status, RK_STATUS_TIMEOUT);
         }

@@ -66,8 +66,10 @@ int check_shape(int32_t B, int32_t Sq, int32_t Hq, int32_t Hkv, int32_t D, int32
     return RK_OK;
 }
 
+// Row b's queries are pos[b * Sq .. b * Sq + Sq) (qo == nullptr), or the
+// packed range pos[qo[b] .. qo[b + 1]) of a ragged batch (rows may be empty).
 int check_metadata(int32_t B, int32_t Sq, int32_t num_pages, int32_t W, const int32_t* bt,
-                   const int32_t* kv, const int32_t* pos, int32_t* max_kv) {
+                   const int32_t* kv, const int32_t* pos, int32_t* max_kv, const int32_t* qo = nullptr) {
     *max_kv = 0;
     for (int b = 0; b < B; ++b) {
         const int n = kv[b];
@@ -100,18 +102,20 @@ int check_metadata(int32_t B, int32_t Sq, int32_t num_pages, int32_t W, const in
         }
     }
     for (int b = 0; b < B; ++b) {
-        const int32_t* p = pos + (size_t)b * Sq;
-        for (int s = 0; s < Sq; ++s) {
+        const int32_t* p = qo ? pos + qo[b] : pos + (size_t)b * Sq;
+        const int nq = qo ? qo[b + 1] - qo[b] : Sq;
+        if (nq == 0) continue;  // a ragged row with no query this step
+        for (int s = 0; s < nq; ++s) {
             if (p[s] < 0) return fail(RK_E_POSITION, "row %d: position_ids[%d] = %d < 0", b, s, p[s]);
             if (s > 0 && p[s] != p[s - 1] + 1)
                 return fail(RK_E_POSITION, "row %d: positions not contiguous ascending at %d", b, s);
         }
         const int n = kv[b];
-        const int last = p[Sq - 1];
+        const int last = p[nq - 1];
         if (n == 0) {
-            if (Sq > 1)
+            if (nq > 1)
                 return fail(RK_E_POSITION,
-                            "row %d: empty row with %d queries (only decode rows may be empty)", b, Sq);
+                            "row %d: empty row with %d queries (only decode rows may be empty)", b, nq);
         } else if (last != n - 1 && last != n) {
             return fail(RK_E_POSITION,
                         "row %d: last query position %d is neither kv_len-1 = %d nor kv_len = %d", b,
@@ -283,6 +287,49 @@ int rk_paged_plan(rk_paged_plan_t* plan, int32_t B, int32_t Sq, int32_t Hq, int3
         const double fx = std::ldexp(w, 64);
         plan->rope_turns[i] = fx >= 18446744073709551615.0 ? ~0ull : (uint64_t)fx;
     }
+    return RK_OK;
+}
+
+int rk_paged_plan_ragged(rk_paged_plan_t* plan, int32_t B, int32_t total_q, int32_t Hq, int32_t Hkv, int32_t D,
+                         int32_t page_size, int32_t num_pages, int32_t W, const int32_t* qo_indptr_h,
+                         const int32_t* block_table_h, const int32_t* kv_lens_h, const int32_t* position_ids_h,
+                         double rope_theta, double rope_scale, int32_t* max_q_len) {
+    g_err.clear();
+    if (!plan || !qo_indptr_h || !max_q_len) return fail(RK_E_ARG, "plan, qo_indptr and max_q_len must be non-null");
+    std::memset(plan, 0, sizeof *plan);
+    if (B < 0 || total_q < 1) return fail(RK_E_ARG, "bad sizes: B=%d total_q=%d (need B >= 0, total_q >= 1)", B, total_q);
+    if (qo_indptr_h[0] != 0 || qo_indptr_h[B] != total_q)
+        return fail(RK_E_ARG, "qo_indptr must start at 0 and end at total_q = %d (got %d .. %d)", total_q,
+                    qo_indptr_h[0], qo_indptr_h[B]);
+    int32_t mq = 0;
+    for (int b = 0; b < B; ++b) {
+        const int32_t n = qo_indptr_h[b + 1] - qo_indptr_h[b];
+        if (n < 0) return fail(RK_E_ARG, "qo_indptr decreases at row %d", b);
+        mq = n > mq ? n : mq;
+    }
+    // shapes as a padded plan of Sq = total_q (the packed q has total_q tokens)
+    int rc = rk_paged_plan(plan, B, total_q, Hq, Hkv, D, page_size, num_pages, W, nullptr, nullptr, nullptr,
+                           rope_theta, rope_scale);
+    if (rc) return rc;
+    const bool any = block_table_h || kv_lens_h || position_ids_h;
+    const bool check = kv_lens_h && position_ids_h && (block_table_h || W == 0);
+    if (any && !check) {
+        std::memset(plan, 0, sizeof *plan);
+        return fail(RK_E_ARG, "pass all three host metadata arrays, or none for a shape-only plan");
+    }
+    if (check && B > 0) {
+        static const int32_t kEmpty = -1;
+        int32_t max_kv = 0;
+        rc = check_metadata(B, total_q, num_pages, W, block_table_h ? block_table_h : &kEmpty, kv_lens_h,
+                            position_ids_h, &max_kv, qo_indptr_h);
+        if (rc) {
+            std::memset(plan, 0, sizeof *plan);
+            return rc;
+        }
+        plan->max_kv_len = max_kv;
+        plan->validated = 1;
+    }
+    *max_q_len = mq;
     return RK_OK;
 }
 
@@ -537,6 +584,96 @@ int rk_paged_attn_prefill(const rk_paged_plan_t* plan, const void* q, const void
     std::memcpy(a.rope_turns, plan->rope_turns, sizeof a.rope_turns);
     cudaError_t e = rk::launch_prefill(qm, km, vm, a, reinterpret_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return fail(RK_E_CUDA, "prefill launch: %s", cudaGetErrorString(e));
+    return RK_OK;
+}
+
+int rk_paged_attn_ragged(const rk_paged_plan_t* plan, int32_t max_q_len, const int32_t* qo_indptr_d, const void* q,
+                         const void* k_cache, const void* v_cache, const int32_t* block_table_d,
+                         const int32_t* kv_lens_d, const int32_t* position_ids_d, void* out, float* lse,
+                         int32_t* status_d, rk_stream_t stream) {
+    g_err.clear();
+    int rc = check_launch_common(plan, q, k_cache, v_cache, block_table_d, kv_lens_d, position_ids_d, out, lse);
+    if (rc) return rc;
+    if (plan->B == 0) return RK_OK;
+    const int32_t total_q = plan->Sq;
+    if (max_q_len < 1 || max_q_len > total_q)
+        return fail(RK_E_ARG, "max_q_len %d outside [1, total_q = %d]", max_q_len, total_q);
+    if (!qo_indptr_d || !aligned(qo_indptr_d, 4)) return fail(RK_E_ARG, "qo_indptr must be a 4-byte aligned device pointer");
+    const int G = plan->Hq / plan->Hkv;
+    const int rph = rk::PF_BM / G;
+    const bool have = plan->num_pages > 0;
+    const float qk = (float)((1.0 / std::sqrt((double)plan->D)) * 1.4426950408889634074);
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    // single-query rows: the decode kernel
+    {
+        CUtensorMap km, vm;
+        if ((rc = make_cache_map(&km, have ? k_cache : q, have ? plan->num_pages : 1, have ? plan->Hkv : 1, 64,
+                                 CU_TENSOR_MAP_SWIZZLE_128B, "k_cache")))
+            return rc;
+        if ((rc = make_page_map(&vm, have ? v_cache : q, have ? plan->num_pages : 1, have ? plan->Hkv : 1,
+                                "v_cache")))
+            return rc;
+        rk::DecodeArgs a;
+        std::memset(&a, 0, sizeof a);
+        a.q = q;
+        a.block_table = block_table_d;
+        a.kv_lens = kv_lens_d;
+        a.position_ids = position_ids_d;
+        a.out = out;
+        a.lse = lse;
+        a.status = status_d;
+        a.B = plan->B;
+        a.Hq = plan->Hq;
+        a.Hkv = plan->Hkv;
+        a.G = G;
+        a.W = plan->W;
+        a.num_pages = plan->num_pages;
+        a.qk_scale_log2 = qk;
+        a.qo_indptr = qo_indptr_d;
+        a.total_q = total_q;
+        std::memcpy(a.rope_turns, plan->rope_turns, sizeof a.rope_turns);
+        cudaError_t e = rk::launch_decode(km, vm, a, st);
+        if (e != cudaSuccess) return fail(RK_E_CUDA, "ragged decode launch: %s", cudaGetErrorString(e));
+    }
+    if (max_q_len < 2) return RK_OK;
+    // rows of two or more queries: the prefill kernel; packed q [total_q, Hq, D]
+    // seen as (d, token, head) so that a box (64, 128/G tokens, G heads) lands
+    // head-major like the padded layout's q-tile
+    CUtensorMap qm, km, vm;
+    {
+        const cuuint64_t dims[3] = {(cuuint64_t)rk::HEAD_DIM, (cuuint64_t)total_q, (cuuint64_t)plan->Hq};
+        const cuuint64_t strides[2] = {(cuuint64_t)plan->Hq * rk::HEAD_DIM * 2, (cuuint64_t)rk::HEAD_DIM * 2};
+        const cuuint32_t box[3] = {64, (cuuint32_t)rph, (cuuint32_t)G};
+        if ((rc = make_map(&qm, q, 3, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B, "q (packed)"))) return rc;
+    }
+    if ((rc = make_cache_map(&km, have ? k_cache : q, have ? plan->num_pages : 1, have ? plan->Hkv : 1, 64,
+                             CU_TENSOR_MAP_SWIZZLE_128B, "k_cache")))
+        return rc;
+    if ((rc = make_page_map(&vm, have ? v_cache : q, have ? plan->num_pages : 1, have ? plan->Hkv : 1, "v_cache")))
+        return rc;
+    rk::PrefillArgs a;
+    std::memset(&a, 0, sizeof a);
+    a.block_table = block_table_d;
+    a.kv_lens = kv_lens_d;
+    a.position_ids = position_ids_d;
+    a.out = out;
+    a.lse = lse;
+    a.status = status_d;
+    a.B = plan->B;
+    a.Sq = total_q;
+    a.Hq = plan->Hq;
+    a.Hkv = plan->Hkv;
+    a.G = G;
+    a.W = plan->W;
+    a.num_pages = plan->num_pages;
+    a.rows_per_head = rph;
+    a.n_qtiles = (max_q_len + rph - 1) / rph;
+    a.qk_scale_log2 = qk;
+    a.qo_indptr = qo_indptr_d;
+    a.total_q = total_q;
+    std::memcpy(a.rope_turns, plan->rope_turns, sizeof a.rope_turns);
+    cudaError_t e = rk::launch_prefill(qm, km, vm, a, st);
+    if (e != cudaSuccess) return fail(RK_E_CUDA, "ragged prefill launch: %s", cudaGetErrorString(e));
     return RK_OK;
 }
 

@@ -44,6 +44,13 @@ struct DecodeArgs {
     int32_t n_splits;
     float* o_part;
     float* lse_part;
+    // Ragged batch (qo_indptr != null): q / out [total_q, Hq, D], lse
+    // [total_q, Hq], position_ids [total_q]; row b's queries are packed rows
+    // qo_indptr[b] .. qo_indptr[b + 1] - 1 and this kernel serves the rows
+    // with exactly one query.
+    const int32_t* qo_indptr;
+    int32_t total_q;
+    int32_t pad1;
     uint64_t rope_turns[ROPE_PAIRS];
 };
 constexpr int DEC_SPLIT_GRAIN = 1024;  // split lengths are multiples of this many tokens (8 KV tiles)
@@ -65,8 +72,14 @@ struct PrefillArgs {
     int32_t* status;
     int32_t B, Sq, Hq, Hkv, G, W, num_pages;
     int32_t rows_per_head;        // 128 / G positions per q-tile
-    int32_t n_qtiles;             // ceil(Sq / rows_per_head)
+    int32_t n_qtiles;             // ceil(Sq / rows_per_head) (ragged: ceil(max_q_len / rows_per_head))
     float qk_scale_log2;
+    // Ragged batch (qo_indptr != null): packed q / out [total_q, Hq, D], lse
+    // [total_q, Hq], position_ids [total_q]; this kernel serves the rows with
+    // two or more queries (single-query rows go to the decode kernel).
+    const int32_t* qo_indptr;
+    int32_t total_q;
+    int32_t pad0;
     uint64_t rope_turns[ROPE_PAIRS];
 };
 

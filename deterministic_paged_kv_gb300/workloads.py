@@ -111,6 +111,42 @@ def build(name, B, Sq, Hq, Hkv, D, kv_lens, num_pages, W, seed, mode,
                     pos, mode, rope_theta, rope_scale)
 
 
+def ragged_case(q_lens, kv_lens, seed, Hq=32, Hkv=8, D=128, extra_pages=3):
+    """A ragged batch, kept padded to max(q_lens) queries per row (the pack
+    step below gives the packed layout).  Row b has q_lens[b] queries: one
+    query sits at position kv_len (a decode row), longer rows take the
+    trailing positions kv_len - q_len .. kv_len - 1 (a prefill chunk); padding
+    entries repeat the row's last position and are never read."""
+    B = len(q_lens)
+    mq = max(list(q_lens) + [1])
+    need = sum((int(n) + PAGE - 1) // PAGE for n in kv_lens)
+    W = max([(int(n) + PAGE - 1) // PAGE for n in kv_lens] + [1])
+    w = build("ragged", B, mq, Hq, Hkv, D, kv_lens, need + extra_pages, W, seed, "prefill")
+    pos = torch.zeros((B, mq), dtype=torch.int32)
+    for b, n in enumerate(q_lens):
+        n = int(n)
+        if n == 0:
+            continue
+        start = max(int(kv_lens[b]) - n + (1 if n == 1 else 0), 0)
+        pos[b, :n] = torch.arange(start, start + n, dtype=torch.int32)
+        pos[b, n:] = start + n - 1
+    w.position_ids = pos
+    w.meta["q_lens"] = [int(n) for n in q_lens]
+    return w
+
+
+def pack_ragged(w):
+    """(q [total_q, Hq, D], qo_indptr [B + 1], position_ids [total_q]) of a
+    ragged_case workload: row b's first q_lens[b] queries, rows in order."""
+    ql = w.meta["q_lens"]
+    indptr = [0]
+    for n in ql:
+        indptr.append(indptr[-1] + n)
+    q = torch.cat([w.q[b, :, :n].transpose(0, 1) for b, n in enumerate(ql)], 0).contiguous()
+    pos = torch.cat([w.position_ids[b, :n] for b, n in enumerate(ql)]).contiguous()
+    return q, torch.tensor(indptr, dtype=torch.int32), pos
+
+
 def decode_small():
     """B=2, q_len 1, kv_len 128, query at 128; 16 pages shuffled."""
     return build("decode_small: B=2 kv=128 Hq=32 Hkv=8 d=128", 2, 1, 32, 8, 128,

@@ -260,6 +260,53 @@ int rk_paged_kv_append(const rk_paged_plan_t *plan, int32_t n_new, const void *k
                        const int32_t *block_table_d, const int32_t *kv_lens_d, void *k_cache,
                        void *v_cache, int32_t *status_d, rk_stream_t stream);
 
+/*
+ * Ragged batches: rows with different numbers of queries this step (prefill
+ * chunks of any length next to single-query decode rows), queries packed
+ * along one axis as in FlashInfer's ragged NHD layout (qo_indptr).  Each row
+ * is computed exactly as the padded entry points compute it (the same
+ * validation list, the same per-row reduction): single-query rows by the
+ * decode kernel, longer rows by the prefill kernel, a choice made by the
+ * row's own query count, so results stay batch-invariant.
+ *   qo_indptr     int32 [B + 1]: row b's queries are packed rows
+ *                 qo_indptr[b] .. qo_indptr[b + 1] - 1 (0 = no query).
+ *   q, out        bf16 [total_q, Hq, D];  lse  fp32 [total_q, Hq];
+ *   position_ids  int32 [total_q] (contiguous ascending per row, trailing).
+ *
+ * rk_paged_plan_ragged -- rk_paged_plan for a ragged batch: validates
+ * qo_indptr (starts at 0, non-decreasing, ends at total_q >= 1; RK_E_ARG),
+ * then shapes and, when all three metadata arrays are given, the same list
+ * as rk_paged_plan per row (rows with no query are skipped by the position
+ * rules).  The plan holds Sq = total_q.  *max_q_len receives the largest
+ * per-row query count (the prefill grid is sized by it).  Host only.
+ */
+int rk_paged_plan_ragged(rk_paged_plan_t *plan, int32_t B, int32_t total_q, int32_t Hq, int32_t Hkv,
+                         int32_t D, int32_t page_size, int32_t num_pages, int32_t W,
+                         const int32_t *qo_indptr_h, const int32_t *block_table_h,
+                         const int32_t *kv_lens_h, const int32_t *position_ids_h, double rope_theta,
+                         double rope_scale, int32_t *max_q_len);
+
+/*
+ * rk_paged_attn_ragged -- causal attention for a ragged batch (plan from
+ * rk_paged_plan_ragged, or a shape-only rk_paged_plan with Sq = total_q).
+ *   max_q_len     1 <= max_q_len <= total_q: bound of every row's query count
+ *                 this call may see (the grid is sized by it; a row above it
+ *                 is not computed and sets RK_STATUS_POSITION).
+ *   qo_indptr_d   DEVICE int32 [B + 1].  Other buffers as above, DEVICE,
+ *                 q / out / caches 16-byte aligned.
+ * Two launches on `stream` (decode rows, then prefill rows), no allocation,
+ * no host synchronisation: metadata is read on the device, so a captured
+ * graph replays with new contents that respect max_q_len.  A row whose
+ * qo_indptr entries are out of range or decreasing is not written and sets
+ * RK_STATUS_POSITION.  Errors as rk_paged_attn_prefill, plus RK_E_ARG for
+ * max_q_len or qo_indptr_d.
+ */
+int rk_paged_attn_ragged(const rk_paged_plan_t *plan, int32_t max_q_len, const int32_t *qo_indptr_d,
+                         const void *q, const void *k_cache, const void *v_cache,
+                         const int32_t *block_table_d, const int32_t *kv_lens_d,
+                         const int32_t *position_ids_d, void *out, float *lse, int32_t *status_d,
+                         rk_stream_t stream);
+
 /* Message of the last failing call on this thread ("" if none).  The
  * pointer stays valid until the next library call on the same thread. */
 const char *rk_last_error(void);

@@ -198,3 +198,23 @@ def test_split_decode_scratch_bytes_host_only(rk):
         with pytest.raises(rk.RkError) as e:
             rk.decode_split_scratch_bytes(p, bad)
         assert e.value.name == "RK_E_ARG"
+
+
+def test_ragged_plan_validation_host_only(rk):
+    """rk_paged_plan_ragged: qo_indptr must start at 0, not decrease and end at
+    total_q; per-row positions follow the padded rules; max_q_len returned."""
+    from deterministic_paged_kv_gb300 import workloads
+    w = workloads.ragged_case([1, 0, 5, 3], [40, 10, 60, 20], seed=3)
+    q, ind, pos = workloads.pack_ragged(w)
+    T = q.shape[0]
+    p, mq = rk.plan_ragged(w.B, T, 32, 8, 128, 16, w.num_pages, w.W, ind, w.block_table, w.kv_lens, pos)
+    assert mq == 5 and p.Sq == T and p.validated == 1
+    for bad_ind in ([1, 1, 1, 6, 9], [0, 1, 0, 6, 9], [0, 1, 1, 6, 8]):
+        with pytest.raises(rk.RkError) as e:
+            rk.plan_ragged(w.B, T, 32, 8, 128, 16, w.num_pages, w.W, bad_ind, w.block_table, w.kv_lens, pos)
+        assert e.value.name == "RK_E_ARG"
+    bad_pos = pos.clone()
+    bad_pos[1 + 2] += 1  # row 2 no longer contiguous
+    with pytest.raises(rk.RkError) as e:
+        rk.plan_ragged(w.B, T, 32, 8, 128, 16, w.num_pages, w.W, ind, w.block_table, w.kv_lens, bad_pos)
+    assert e.value.name == "RK_E_POSITION"
