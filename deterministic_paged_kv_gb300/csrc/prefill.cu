@@ -77,6 +77,8 @@ struct PfBars {
     int range_bad;
     uint64_t turns[ROPE_PAIRS];
     float2 step16[ROPE_PAIRS];  // cos/sin of a 16-position turn per pair
+    int pre_max[PF_THREADS / 32];    // per-warp largest query position (prologue)
+    int pre_flags[PF_THREADS / 32];  // per-warp unsafe flags: 1 position, 2 page id
 };
 static_assert(sizeof(PfBars) <= PF_CTRL_BYTES, "prefill control block exceeds its reservation");
 static_assert(PF_SMEM_BYTES <= 232448, "prefill shared memory above the 227 KiB opt-in limit");
@@ -151,32 +153,31 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
     const int32_t* pos_row = a.position_ids + rm.qbase;
     int bad = 0;
     if (kv_len < 0 || kv_len > a.W * PAGE) bad |= RK_STATUS_KVLEN;
-    TileInfo ti[2];
-#pragma unroll
-    for (int j = 0; j < 2; ++j) {
-        ti[j].s0 = (2 * pair + j) * rph;
-        int pmax = -1;
-        for (int s = ti[j].s0; s < min(ti[j].s0 + rph, rm.qn); ++s) {
-            const int p = pos_row[s];
-            if (p < 0) bad |= RK_STATUS_POSITION;
-            pmax = max(pmax, p);
-        }
-        ti[j].n_keys = (bad || pmax < 0) ? 0 : (pmax >= kv_len ? kv_len : pmax + 1);
-        ti[j].n_tiles = (ti[j].n_keys + PF_BN - 1) / PF_BN;
-    }
-    const int n_keys = max(ti[0].n_keys, ti[1].n_keys);
-    const int n_tiles = max(ti[0].n_tiles, ti[1].n_tiles);
-    const int n_pages = (n_keys + PAGE - 1) / PAGE;
-    // The row's last page is in this CTA's last tile and is only partly
-    // filled: its cache rows past kv_len hold arbitrary bits and are zeroed in
-    // V after the copy lands (they meet P = 0, which would not cancel a
-    // non-finite value).
-    const bool has_tail = n_keys == kv_len && (kv_len & (PAGE - 1)) != 0;
     const int32_t* bt = a.block_table + (size_t)b * a.W;
-    int oob = 0;
-    for (int i = tid; i < n_pages; i += PF_THREADS) {
+    // One query position per thread (threads 0..255: q-tile tid / 128, row
+    // tid % 128) and every page id of the row's keys (kv_len, not just the keys
+    // this pair sees, so all CTAs of a row agree on unsafe pages), loaded
+    // together and reduced at the barrier below.
+    int p_mine = -1, flags = 0;
+    if (tid < 256) {
+        const int rr = tid & 127, s = (2 * pair + (tid >> 7)) * rph + rr;
+        if (rr < rph && s < rm.qn) {
+            p_mine = pos_row[s];
+            if (p_mine < 0) flags |= 1;
+        }
+    }
+    const int row_pages = (bad & RK_STATUS_KVLEN) ? 0 : (kv_len + PAGE - 1) / PAGE;
+    for (int i = tid; i < row_pages; i += PF_THREADS) {
         const int pg = __ldg(bt + i);
-        oob |= (pg < 0) | (pg >= a.num_pages);
+        if ((pg < 0) | (pg >= a.num_pages)) flags |= 2;
+    }
+    {
+        const int wmax = __reduce_max_sync(0xffffffffu, p_mine);
+        const int wflags = __reduce_or_sync(0xffffffffu, (unsigned)flags);
+        if (lane == 0) {
+            bars->pre_max[warp] = wmax;
+            bars->pre_flags[warp] = wflags;
+        }
     }
     if (tid == 0) {
         bars->abort = 0;
@@ -210,7 +211,30 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
         rope_cos_sin((uint32_t)PAGE, a.rope_turns[tid], c, s);
         bars->step16[tid] = make_float2(c, s);
     }
-    if (__syncthreads_or(oob)) bad |= RK_STATUS_PAGE_OOB;
+    __syncthreads();
+    {
+        int f = 0;
+        for (int w = 0; w < PF_THREADS / 32; ++w) f |= bars->pre_flags[w];
+        if (f & 1) bad |= RK_STATUS_POSITION;
+        if (f & 2) bad |= RK_STATUS_PAGE_OOB;
+    }
+    TileInfo ti[2];
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {  // warps 4j .. 4j+3 loaded q-tile j's positions
+        ti[j].s0 = (2 * pair + j) * rph;
+        const int pmax = max(max(bars->pre_max[4 * j], bars->pre_max[4 * j + 1]),
+                             max(bars->pre_max[4 * j + 2], bars->pre_max[4 * j + 3]));
+        ti[j].n_keys = (bad || pmax < 0) ? 0 : (pmax >= kv_len ? kv_len : pmax + 1);
+        ti[j].n_tiles = (ti[j].n_keys + PF_BN - 1) / PF_BN;
+    }
+    const int n_keys = max(ti[0].n_keys, ti[1].n_keys);
+    const int n_tiles = max(ti[0].n_tiles, ti[1].n_tiles);
+    const int n_pages = (n_keys + PAGE - 1) / PAGE;
+    // The row's last page is in this CTA's last tile and is only partly
+    // filled: its cache rows past kv_len hold arbitrary bits and are zeroed in
+    // V after the copy lands (they meet P = 0, which would not cancel a
+    // non-finite value).
+    const bool has_tail = n_keys == kv_len && (kv_len & (PAGE - 1)) != 0;
     if (bad || n_tiles == 0) {
         if (bad && tid == 0 && a.status) atomicOr(a.status, bad);
         const float lv = bad ? __int_as_float(0x7fc00000) : -INFINITY;
