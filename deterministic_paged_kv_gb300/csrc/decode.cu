@@ -134,6 +134,22 @@ __global__ void __launch_bounds__(DEC_THREADS, 1)
     }
     const int kv_len = a.kv_lens[b];
     const int qpos = a.position_ids[tq];
+    const int32_t* bt = a.block_table + (size_t)b * a.W;
+    constexpr int PPT = DEC_BN / PAGE;  // pages per tile
+    const int i0 = a.split_tiles > 0 ? split * a.split_tiles : 0;
+    // The page ids of the CTA's part of the table are loaded before its length
+    // is known (the metadata costs one round trip, not two) and judged against
+    // the visible range below; the producers' first page ids likewise.
+    const int pg_lo = i0 * PPT;
+    const int pg_cap = a.split_tiles > 0 ? min(a.W, (i0 + a.split_tiles) * PPT) : a.W;
+    constexpr int PRE = 4;  // table entries per thread held from the early load
+    int pre[PRE];
+#pragma unroll
+    for (int e = 0; e < PRE; ++e) {
+        const int i = pg_lo + tid + e * DEC_THREADS;
+        pre[e] = i < pg_cap ? __ldg(bt + i) : 0;
+    }
+    const int first_pg = (lane < PPT && pg_lo + lane < a.W) ? __ldg(bt + pg_lo + lane) : 0;
     int bad = 0;
     if (kv_len < 0 || kv_len > a.W * PAGE) bad |= RK_STATUS_KVLEN;
     if (qpos < 0) bad |= RK_STATUS_POSITION;
@@ -141,17 +157,19 @@ __global__ void __launch_bounds__(DEC_THREADS, 1)
     const int n_pages = (n_vis + PAGE - 1) / PAGE;
     const int n_tiles = (n_vis + DEC_BN - 1) / DEC_BN;
     // This CTA's KV tiles [i0, i0 + n_loc): the whole row, or one fixed split.
-    const int i0 = a.split_tiles > 0 ? split * a.split_tiles : 0;
     const int n_loc = a.split_tiles > 0 ? max(0, min(n_tiles, i0 + a.split_tiles) - i0) : n_tiles;
-    constexpr int PPT = DEC_BN / PAGE;  // pages per tile
     // Last page partly filled and inside the visible range: its rows past
     // kv_len hold arbitrary bits and are zeroed in V after the copy lands
     // (by the CTA that holds the row's last tile).
     const bool has_tail = n_vis == kv_len && (kv_len & (PAGE - 1)) != 0 && n_loc > 0 && i0 + n_loc == n_tiles;
-    const int32_t* bt = a.block_table + (size_t)b * a.W;
     int oob = 0;
     const int pg_end = min(n_pages, (i0 + n_loc) * PPT);  // the pages this CTA reads
-    for (int i = i0 * PPT + tid; i < pg_end; i += DEC_THREADS) {
+#pragma unroll
+    for (int e = 0; e < PRE; ++e) {
+        const int i = pg_lo + tid + e * DEC_THREADS;
+        if (i < pg_end) oob |= (pre[e] < 0) | (pre[e] >= a.num_pages);
+    }
+    for (int i = pg_lo + tid + PRE * DEC_THREADS; i < pg_end; i += DEC_THREADS) {  // very wide rows
         const int pg = __ldg(bt + i);
         oob |= (pg < 0) | (pg >= a.num_pages);
     }
@@ -219,7 +237,7 @@ __global__ void __launch_bounds__(DEC_THREADS, 1)
         const int nst = is_k ? DEC_KSTAGES : DEC_VSTAGES;
         if (lane == 0) prefetch_tmap(map);
         int issued = 0;
-        int pg_next = lane < min(PPT, n_pages - i0 * PPT) ? __ldg(bt + i0 * PPT + lane) : 0;
+        int pg_next = first_pg;  // lanes past the tile's pages never use theirs
         // it: the CTA's own tile count (stages, phases); i: the row's tile index
         for (int it = 0; it < n_loc; ++it) {
             const int i = i0 + it;
