@@ -346,9 +346,12 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
             const uint32_t dV0 = desc_lo(s_base + OFF_V, 2048);
             bool ok = mbar_wait(smem_u32(&bars->q_ready), 0, abort);
             int v_seen = -1;  // last V tile whose arrival (and tail zeroing) was observed
-            auto issue_pv = [&](int j, int i) -> bool {  // O_j += P_j(i) V(i)
+            // O_j += P_j(i) V(i).  implied: P_j(i) was published after K(i+1) was
+            // ready, which the transform published after V(i) landed, so only
+            // P_j(i) is waited for; otherwise (the q-tile's last PV) V(i) too.
+            auto issue_pv = [&](int j, int i, bool implied) -> bool {
                 if (!mbar_wait(smem_u32(&bars->p_ready[j]), (uint32_t)(i & 1), abort)) return false;
-                if (v_seen != i) {
+                if (!implied && v_seen != i) {
                     if (!mbar_wait(smem_u32(&bars->v_full[i % VSTAGES]), (uint32_t)((i / VSTAGES) & 1), abort))
                         return false;
                     if (has_tail && i == n_tiles - 1 && !mbar_wait(smem_u32(&bars->v_tail), 0, abort)) return false;
@@ -367,8 +370,11 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
                 for (int j = 0; j < 2; ++j) {
                     if (!ok) break;
                     if (i < ti[j].n_tiles) {
-                        if (i > 0 && !(ok = issue_pv(j, i - 1))) break;
-                        if (!k_in) {
+                        // for i > 0, K(i) is implied by P_j(i-1) (see issue_pv)
+                        if (i > 0 && !(ok = issue_pv(j, i - 1, true))) break;
+                        if (i > 0) {
+                            k_in = true;
+                        } else if (!k_in) {
                             if (!(ok = mbar_wait(smem_u32(&bars->k_ready[k]), (uint32_t)((i / KSTAGES) & 1), abort)))
                                 break;
                             tc_fence_after();
@@ -379,7 +385,7 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
                         mma_ss_steps<0, 8, K_MAJOR_128, K_MAJOR_128>(d, dq, dk, idS, 0u);
                         umma_commit(smem_u32(&bars->s_full[j]));
                     } else if (i == ti[j].n_tiles && i > 0) {
-                        if (!(ok = issue_pv(j, i - 1))) break;
+                        if (!(ok = issue_pv(j, i - 1, false))) break;
                         umma_commit(smem_u32(&bars->o_done[j]));
                     }
                 }
@@ -390,7 +396,7 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
 #pragma unroll
             for (int j = 0; j < 2; ++j) {
                 if (ok && ti[j].n_tiles == n_tiles) {
-                    if (!(ok = issue_pv(j, n_tiles - 1))) break;
+                    if (!(ok = issue_pv(j, n_tiles - 1, false))) break;
                     umma_commit(smem_u32(&bars->o_done[j]));
                 }
             }
@@ -463,6 +469,11 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
             }
             if (range_exceeded(range)) bars->range_bad = 1;
             fence_proxy_async_smem();
+            // K(i) is published only once V(i-1) has landed, so whoever has seen
+            // K(i) ready may also read V(i-1) (the MMA issuer relies on it).
+            if (i > 0 && !mbar_wait(smem_u32(&bars->v_full[(i - 1) % VSTAGES]),
+                                    (uint32_t)(((i - 1) / VSTAGES) & 1), abort))
+                break;
             mbar_arrive(smem_u32(&bars->k_ready[k]));
         }
         named_bar_sync(1, 384);  // transform done: the range flag is final for the epilogues
@@ -488,6 +499,13 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
                 break;
             }
             tc_fence_after();
+            // P_j(i) is published only once K(i+1) is ready when S_j(i+1) follows,
+            // so the MMA issuer need not wait for K (or V(i), see the transform).
+            // Probed here, confirmed before the arrive: the latency overlaps the math.
+            const bool need_k = i + 1 < nt;
+            const int kn = (i + 1) % KSTAGES;
+            const uint32_t kpar = (uint32_t)(((i + 1) / KSTAGES) & 1);
+            const bool k_seen = !need_k || mbar_test(smem_u32(&bars->k_ready[kn]), kpar);
             uint32_t xr[128];
 #pragma unroll
             for (int c4 = 0; c4 < 4; ++c4)
@@ -548,6 +566,10 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
             tmem_st32(tS + lane_addr, *reinterpret_cast<uint32_t(*)[32]>(&xr[0]));
             tmem_st32(tS + lane_addr + 32, *reinterpret_cast<uint32_t(*)[32]>(&xr[32]));
             tmem_st_wait();
+            if (!__all_sync(0xffffffffu, k_seen || mbar_wait(smem_u32(&bars->k_ready[kn]), kpar, abort))) {
+                ok = false;
+                break;
+            }
             tc_fence_before();
             mbar_arrive(smem_u32(&bars->p_ready[j]));
         }
