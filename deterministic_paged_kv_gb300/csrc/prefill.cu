@@ -85,11 +85,6 @@ static_assert(PF_SMEM_BYTES <= 232448, "prefill shared memory above the 227 KiB 
 
 __device__ __forceinline__ uint32_t sw_off(int row, int chunk) { return sw128_off(row, chunk); }
 
-struct TileInfo {
-    int s0;       // first query index of the q-tile
-    int n_keys;   // keys any of its rows may see
-    int n_tiles;  // KV tiles it needs
-};
 
 // Where a row's queries live: padded rows (s of row b at [b, h, s]) or a
 // ragged batch (packed rows qbase .. qbase + qn - 1 at [qbase + s, h]).
@@ -218,17 +213,18 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
         if (f & 1) bad |= RK_STATUS_POSITION;
         if (f & 2) bad |= RK_STATUS_PAGE_OOB;
     }
-    TileInfo ti[2];
-#pragma unroll
-    for (int j = 0; j < 2; ++j) {  // warps 4j .. 4j+3 loaded q-tile j's positions
-        ti[j].s0 = (2 * pair + j) * rph;
+    // q-tile j: first query (2 pair + j) * rph; keys and KV tiles it needs (scalars,
+    // so nothing indexed at run time lands in local memory)
+    auto qt_keys = [&](int j) {  // warps 4j .. 4j+3 loaded q-tile j's positions
         const int pmax = max(max(bars->pre_max[4 * j], bars->pre_max[4 * j + 1]),
                              max(bars->pre_max[4 * j + 2], bars->pre_max[4 * j + 3]));
-        ti[j].n_keys = (bad || pmax < 0) ? 0 : (pmax >= kv_len ? kv_len : pmax + 1);
-        ti[j].n_tiles = (ti[j].n_keys + PF_BN - 1) / PF_BN;
-    }
-    const int n_keys = max(ti[0].n_keys, ti[1].n_keys);
-    const int n_tiles = max(ti[0].n_tiles, ti[1].n_tiles);
+        return (bad || pmax < 0) ? 0 : (pmax >= kv_len ? kv_len : pmax + 1);
+    };
+    const int nk0 = qt_keys(0), nk1 = qt_keys(1);
+    const int nt0 = (nk0 + PF_BN - 1) / PF_BN, nt1 = (nk1 + PF_BN - 1) / PF_BN;
+    const int s00 = 2 * pair * rph;  // first query of q-tile 0; q-tile 1 starts rph later
+    const int n_keys = max(nk0, nk1);
+    const int n_tiles = max(nt0, nt1);
     const int n_pages = (n_keys + PAGE - 1) / PAGE;
     // The row's last page is in this CTA's last tile and is only partly
     // filled: its cache rows past kv_len hold arbitrary bits and are zeroed in
@@ -238,8 +234,8 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
     if (bad || n_tiles == 0) {
         if (bad && tid == 0 && a.status) atomicOr(a.status, bad);
         const float lv = bad ? __int_as_float(0x7fc00000) : -INFINITY;
-        write_rows(a, rm, kvh, ti[0].s0, lv);
-        write_rows(a, rm, kvh, ti[1].s0, lv);
+        write_rows(a, rm, kvh, s00, lv);
+        write_rows(a, rm, kvh, s00 + rph, lv);
         return;
     }
 
@@ -271,11 +267,11 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
                     for (int j = 0; j < 2; ++j) {
                         const uint32_t dq = s_base + OFF_Q + j * PF_TILE_BYTES;
                         if (rm.ragged) {  // packed q seen as (d, token, head): rows past the row's end are masked
-                            tma_load_3d(dq, &qmap, qb, 0, rm.qbase + ti[j].s0, kvh * a.G);
-                            tma_load_3d(dq + 16384, &qmap, qb, 64, rm.qbase + ti[j].s0, kvh * a.G);
+                            tma_load_3d(dq, &qmap, qb, 0, rm.qbase + s00 + j * rph, kvh * a.G);
+                            tma_load_3d(dq + 16384, &qmap, qb, 64, rm.qbase + s00 + j * rph, kvh * a.G);
                         } else {
-                            tma_load_4d(dq, &qmap, qb, 0, ti[j].s0, kvh * a.G, b);
-                            tma_load_4d(dq + 16384, &qmap, qb, 64, ti[j].s0, kvh * a.G, b);
+                            tma_load_4d(dq, &qmap, qb, 0, s00 + j * rph, kvh * a.G, b);
+                            tma_load_4d(dq + 16384, &qmap, qb, 64, s00 + j * rph, kvh * a.G, b);
                         }
                     }
                 }
@@ -369,7 +365,7 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
 #pragma unroll
                 for (int j = 0; j < 2; ++j) {
                     if (!ok) break;
-                    if (i < ti[j].n_tiles) {
+                    if (i < (j ? nt1 : nt0)) {
                         // for i > 0, K(i) is implied by P_j(i-1) (see issue_pv)
                         if (i > 0 && !(ok = issue_pv(j, i - 1, true))) break;
                         if (i > 0) {
@@ -384,7 +380,7 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
                         const uint32_t d = tmem + j * 128;
                         mma_ss_steps<0, 8, K_MAJOR_128, K_MAJOR_128>(d, dq, dk, idS, 0u);
                         umma_commit(smem_u32(&bars->s_full[j]));
-                    } else if (i == ti[j].n_tiles && i > 0) {
+                    } else if (i == (j ? nt1 : nt0) && i > 0) {
                         if (!(ok = issue_pv(j, i - 1, false))) break;
                         umma_commit(smem_u32(&bars->o_done[j]));
                     }
@@ -395,7 +391,7 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
             }
 #pragma unroll
             for (int j = 0; j < 2; ++j) {
-                if (ok && ti[j].n_tiles == n_tiles) {
+                if (ok && (j ? nt1 : nt0) == n_tiles) {
                     if (!(ok = issue_pv(j, n_tiles - 1, false))) break;
                     umma_commit(smem_u32(&bars->o_done[j]));
                 }
@@ -418,7 +414,7 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
             const bool got = mbar_wait(smem_u32(&bars->q_full), 0, abort);
             for (int j = 0; j < 2 && got; ++j) {
                 const int r = tid;
-                const int s = ti[j].s0 + r % rph;
+                const int s = s00 + j * rph + r % rph;
                 const int p = s < rm.qn ? pos_row[s] : 0;
                 uint8_t* qt = sm + OFF_Q + j * PF_TILE_BYTES;
 #pragma unroll 1
@@ -485,12 +481,12 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
         const int r = tid - 128 * wg;  // accumulator row == TMEM lane
         const uint32_t lane_addr = (uint32_t)((warp & 3) * 32) << 16;
         const uint32_t tS = tmem + j * 128, tO = tmem + 256 + j * 128;
-        const int g = r / rph, s = ti[j].s0 + r % rph;
+        const int g = r / rph, s = s00 + j * rph + r % rph;
         const bool valid = s < rm.qn;
         const int p = valid ? pos_row[s] : -1;
         const int n_vis = valid ? (p >= kv_len ? kv_len : p + 1) : 0;
         const float scl = a.qk_scale_log2;
-        const int nt = ti[j].n_tiles;
+        const int nt = j ? nt1 : nt0;
         float m = -INFINITY, l = 0.0f;
         bool ok = true;
         for (int i = 0; i < nt; ++i) {
