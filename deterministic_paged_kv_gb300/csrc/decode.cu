@@ -297,40 +297,46 @@ __global__ void __launch_bounds__(DEC_THREADS, 1)
         // MMAs, each waiting only for its own inputs, so the barrier checks of
         // one overlap the MMAs of the other.  tcgen05.commit covers the MMAs of
         // the committing thread, which is what each completion barrier tracks.
-        if (lane == 0) {
+        // Each issuer's whole warp runs its loop (converged, warp-uniform
+        // operands); elect.sync picks the lane that issues MMAs and commits.
+        {
             constexpr uint32_t TILE_DESC = DEC_TILE_BYTES >> 4;  // one 32 KiB tile in descriptor address units
             bool ok = true;
             if (warp == WARP_MMA) {
                 const uint32_t idS = idesc_f16_f32(DEC_BN, NH);
                 const uint32_t dK0 = desc_lo(s_base + OFF_K, 16), dQT = desc_lo(s_base + OFF_QT, 16);
-                ok = mbar_wait(smem_u32(&ctl->q_ready), 0, abort);
+                ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&ctl->q_ready), 0, abort));
                 for (int it = 0; it < n_loc && ok; ++it) {
                     const int k = it % DEC_KSTAGES, sb = it & 1;
-                    ok = mbar_wait(smem_u32(&ctl->k_ready[k]), (uint32_t)((it / DEC_KSTAGES) & 1), abort) &&
-                         (it < 2 || mbar_wait(smem_u32(&ctl->s_free[sb]), (uint32_t)(((it >> 1) - 1) & 1), abort));
+                    ok = __all_sync(0xffffffffu,
+                                    mbar_wait(smem_u32(&ctl->k_ready[k]), (uint32_t)((it / DEC_KSTAGES) & 1), abort) &&
+                                        (it < 2 || mbar_wait(smem_u32(&ctl->s_free[sb]),
+                                                             (uint32_t)(((it >> 1) - 1) & 1), abort)));
                     if (!ok) break;
                     tc_fence_after();
-                    mma_ss_steps<0, 8, K_MAJOR_128, K_MAJOR_16>(tmem + sb * NH, dK0 + (uint32_t)k * TILE_DESC, dQT,
+                    mma_ss_steps<0, 8, K_MAJOR_128, K_MAJOR_16, true>(tmem + sb * NH, dK0 + (uint32_t)k * TILE_DESC, dQT,
                                                                 idS, 0u);
-                    umma_commit(smem_u32(&ctl->s_full[sb]));
-                    umma_commit(smem_u32(&ctl->k_empty[k]));
+                    umma_commit_elect(smem_u32(&ctl->s_full[sb]));
+                    umma_commit_elect(smem_u32(&ctl->k_empty[k]));
                 }
             } else {
                 const uint32_t idO = idesc_bf16_f32(HEAD_DIM, NH, 1, 0);
                 const uint32_t dV0 = desc_lo(s_base + OFF_V, 2048), dPT = desc_lo(s_base + OFF_PT, 16);
                 for (int it = 0; it < n_loc && ok; ++it) {
-                    ok = mbar_wait(smem_u32(&ctl->p_ready[it & 1]), (uint32_t)((it >> 1) & 1), abort) &&
-                         mbar_wait(smem_u32(&ctl->v_full[it % DEC_VSTAGES]), (uint32_t)((it / DEC_VSTAGES) & 1), abort) &&
-                         (!(has_tail && it == n_loc - 1) || mbar_wait(smem_u32(&ctl->v_tail), 0, abort));
+                    ok = __all_sync(0xffffffffu,
+                                    mbar_wait(smem_u32(&ctl->p_ready[it & 1]), (uint32_t)((it >> 1) & 1), abort) &&
+                                        mbar_wait(smem_u32(&ctl->v_full[it % DEC_VSTAGES]),
+                                                  (uint32_t)((it / DEC_VSTAGES) & 1), abort) &&
+                                        (!(has_tail && it == n_loc - 1) || mbar_wait(smem_u32(&ctl->v_tail), 0, abort)));
                     if (!ok) break;
                     tc_fence_after();
-                    mma_ss_steps<0, 8, MN_MAJOR_PAGE, K_MAJOR_16>(tO, dV0 + (uint32_t)(it % DEC_VSTAGES) * TILE_DESC,
+                    mma_ss_steps<0, 8, MN_MAJOR_PAGE, K_MAJOR_16, true>(tO, dV0 + (uint32_t)(it % DEC_VSTAGES) * TILE_DESC,
                                                              dPT + (uint32_t)(it & 1) * (PT_BYTES >> 4), idO,
                                                              it > 0 ? 1u : 0u);
-                    umma_commit(smem_u32(&ctl->pv_done[it & 1]));
-                    umma_commit(smem_u32(&ctl->v_empty[it % DEC_VSTAGES]));
+                    umma_commit_elect(smem_u32(&ctl->pv_done[it & 1]));
+                    umma_commit_elect(smem_u32(&ctl->v_empty[it % DEC_VSTAGES]));
                 }
-                if (ok) umma_commit(smem_u32(&ctl->o_done));
+                if (ok) umma_commit_elect(smem_u32(&ctl->o_done));
             }
             if (!ok) {
                 const uint64_t t0 = global_timer_ns();  // let issued MMAs drain before TMEM is released

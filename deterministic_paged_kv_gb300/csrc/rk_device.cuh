@@ -233,35 +233,71 @@ __host__ __device__ constexpr uint32_t kstep_off(int layout, int ks) {
 }
 // D[tmem] (+)= A[smem] * B[smem], k-steps KS..END-1 of operands with the given
 // layouts; accumulates from k-step 1 on, and at k-step 0 iff acc0.
-template <int KS, int END, int LA, int LB>
+// ELECT = false: called by the single issuing thread.  ELECT = true: called by
+// a whole converged warp (operands stay warp-uniform) and the lane chosen by
+// elect.sync (the lowest active lane, the same every time) issues; that lane
+// must also issue the tcgen05.commit tracking the MMAs (umma_commit_elect).
+template <int KS, int END, int LA, int LB, bool ELECT = false>
 __device__ __forceinline__ void mma_ss_steps(uint32_t d, uint32_t a_lo, uint32_t b_lo, uint32_t idesc,
                                              uint32_t acc0) {
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t.reg .b32 al, bl;\n\t.reg .b64 da, db;\n\t"
-        "add.u32 al, %1, %5;\n\tadd.u32 bl, %2, %6;\n\t"
-        "mov.b64 da, {al, %4};\n\tmov.b64 db, {bl, %4};\n\t"
-        "setp.ne.b32 p, %7, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %3, p;\n\t}" ::"r"(d),
-        "r"(a_lo), "r"(b_lo), "r"(idesc), "r"(DESC_HI), "n"(kstep_off(LA, KS)), "n"(kstep_off(LB, KS)),
-        "r"(KS > 0 ? 1u : acc0)
-        : "memory");
-    if constexpr (KS + 1 < END) mma_ss_steps<KS + 1, END, LA, LB>(d, a_lo, b_lo, idesc, acc0);
+    if constexpr (ELECT) {
+        asm volatile(
+            "{\n\t.reg .pred p, e;\n\t.reg .b32 al, bl;\n\t.reg .b64 da, db;\n\t"
+            "add.u32 al, %1, %5;\n\tadd.u32 bl, %2, %6;\n\t"
+            "mov.b64 da, {al, %4};\n\tmov.b64 db, {bl, %4};\n\t"
+            "setp.ne.b32 p, %7, 0;\n\telect.sync _|e, 0xffffffff;\n\t"
+            "@e tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %3, p;\n\t}" ::"r"(d),
+            "r"(a_lo), "r"(b_lo), "r"(idesc), "r"(DESC_HI), "n"(kstep_off(LA, KS)), "n"(kstep_off(LB, KS)),
+            "r"(KS > 0 ? 1u : acc0)
+            : "memory");
+    } else {
+        asm volatile(
+            "{\n\t.reg .pred p;\n\t.reg .b32 al, bl;\n\t.reg .b64 da, db;\n\t"
+            "add.u32 al, %1, %5;\n\tadd.u32 bl, %2, %6;\n\t"
+            "mov.b64 da, {al, %4};\n\tmov.b64 db, {bl, %4};\n\t"
+            "setp.ne.b32 p, %7, 0;\n\t"
+            "tcgen05.mma.cta_group::1.kind::f16 [%0], da, db, %3, p;\n\t}" ::"r"(d),
+            "r"(a_lo), "r"(b_lo), "r"(idesc), "r"(DESC_HI), "n"(kstep_off(LA, KS)), "n"(kstep_off(LB, KS)),
+            "r"(KS > 0 ? 1u : acc0)
+            : "memory");
+    }
+    if constexpr (KS + 1 < END) mma_ss_steps<KS + 1, END, LA, LB, ELECT>(d, a_lo, b_lo, idesc, acc0);
 }
 // D[tmem] (+)= A[tmem] * B[smem], k-steps KS..END-1; A holds 8 columns of
-// packed 16-bit pairs per k-step.
-template <int KS, int END, int LB>
+// packed 16-bit pairs per k-step.  ELECT as above.
+template <int KS, int END, int LB, bool ELECT = false>
 __device__ __forceinline__ void mma_ts_steps(uint32_t d, uint32_t a_tmem, uint32_t b_lo, uint32_t idesc,
                                              uint32_t acc0) {
+    if constexpr (ELECT) {
+        asm volatile(
+            "{\n\t.reg .pred p, e;\n\t.reg .b32 at, bl;\n\t.reg .b64 db;\n\t"
+            "add.u32 at, %1, %5;\n\tadd.u32 bl, %2, %6;\n\t"
+            "mov.b64 db, {bl, %4};\n\t"
+            "setp.ne.b32 p, %7, 0;\n\telect.sync _|e, 0xffffffff;\n\t"
+            "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [at], db, %3, p;\n\t}" ::"r"(d),
+            "r"(a_tmem), "r"(b_lo), "r"(idesc), "r"(DESC_HI), "n"(KS * 8), "n"(kstep_off(LB, KS)),
+            "r"(KS > 0 ? 1u : acc0)
+            : "memory");
+    } else {
+        asm volatile(
+            "{\n\t.reg .pred p;\n\t.reg .b32 at, bl;\n\t.reg .b64 db;\n\t"
+            "add.u32 at, %1, %5;\n\tadd.u32 bl, %2, %6;\n\t"
+            "mov.b64 db, {bl, %4};\n\t"
+            "setp.ne.b32 p, %7, 0;\n\t"
+            "tcgen05.mma.cta_group::1.kind::f16 [%0], [at], db, %3, p;\n\t}" ::"r"(d),
+            "r"(a_tmem), "r"(b_lo), "r"(idesc), "r"(DESC_HI), "n"(KS * 8), "n"(kstep_off(LB, KS)),
+            "r"(KS > 0 ? 1u : acc0)
+            : "memory");
+    }
+    if constexpr (KS + 1 < END) mma_ts_steps<KS + 1, END, LB, ELECT>(d, a_tmem, b_lo, idesc, acc0);
+}
+// tcgen05.commit by the elected lane of a converged warp (the lane that
+// issued the MMAs it tracks with ELECT = true).
+__device__ __forceinline__ void umma_commit_elect(uint32_t bar) {
     asm volatile(
-        "{\n\t.reg .pred p;\n\t.reg .b32 at, bl;\n\t.reg .b64 db;\n\t"
-        "add.u32 at, %1, %5;\n\tadd.u32 bl, %2, %6;\n\t"
-        "mov.b64 db, {bl, %4};\n\t"
-        "setp.ne.b32 p, %7, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], [at], db, %3, p;\n\t}" ::"r"(d),
-        "r"(a_tmem), "r"(b_lo), "r"(idesc), "r"(DESC_HI), "n"(KS * 8), "n"(kstep_off(LB, KS)),
-        "r"(KS > 0 ? 1u : acc0)
+        "{\n\t.reg .pred e;\n\telect.sync _|e, 0xffffffff;\n\t"
+        "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}" ::"r"(bar)
         : "memory");
-    if constexpr (KS + 1 < END) mma_ts_steps<KS + 1, END, LB>(d, a_tmem, b_lo, idesc, acc0);
 }
 
 // Shared-memory matrix descriptor (tcgen05): start address, leading and
