@@ -375,11 +375,19 @@ def measure_ragged(args, dev, stream):
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
     t = time_launches(fn, 20, stream, flush=flush)
     ms = sum(t) / len(t)
+
+    def fn_dec():  # max_q_len 1: the decode launch alone (the chunk rows are left out)
+        binding.attn_ragged(p, 1, dind, dq, kc, vc, bt, kl, dpos, out, lse, stream=stream)
+
+    for _ in range(3):
+        fn_dec()
+    t = time_launches(fn_dec, 20, stream, flush=flush)
+    ms_dec = sum(t) / len(t)
     dec_bytes = 60 * 2048 * w.Hkv * w.D * 2 * 2
     pf_flops = 4.0 * w.D * w.Hq * 4 * sum(1536 + s + 1 for s in range(512))
     return {"workload": "ragged step: 60 decode rows (kv 2048) + 4 prefill chunks (512 at 1536..2047)",
             "l2": "flushed (256 MB write) between launches", "ms_per_launch": ms,
-            "decode_rows_kv_bytes": dec_bytes, "prefill_rows_flops": pf_flops,
+            "decode_launch_alone_ms": ms_dec, "decode_rows_kv_bytes": dec_bytes, "prefill_rows_flops": pf_flops,
             "note": "one call, two launches (decode rows, prefill rows)"}
 
 

@@ -108,6 +108,9 @@ __global__ void __launch_bounds__(DEC_THREADS, 1)
     decode_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
                   const __grid_constant__ DecodeArgs a) {
     extern __shared__ __align__(1024) uint8_t sm[];
+    // A launch that only reads what this grid reads (the prefill rows of a
+    // ragged batch) may fill the SMs this grid's last wave leaves idle.
+    griddep_launch_dependents();
     DecCtrl* ctl = reinterpret_cast<DecCtrl*>(sm + OFF_CTRL);
     const uint32_t s_base = smem_u32(sm);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -129,7 +132,10 @@ __global__ void __launch_bounds__(DEC_THREADS, 1)
             if (tid == 0 && a.status) atomicOr(a.status, RK_STATUS_POSITION);
             return;
         }
-        if (qe - qs != 1) return;  // no query, or a prefill row
+        if (qe - qs != 1) {  // no query, or a prefill row (flagged here when no prefill launch covers it)
+            if (qe - qs > a.max_q_len && tid == 0 && a.status) atomicOr(a.status, RK_STATUS_POSITION);
+            return;
+        }
         tq = qs;
     }
     const int kv_len = a.kv_lens[b];

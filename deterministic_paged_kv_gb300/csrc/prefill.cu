@@ -37,6 +37,7 @@
 // Nothing depends on B, W or the grid: tiles are fixed in logical positions
 // and tokens, and the reduction order within a row is fixed.
 #include <atomic>
+#include <cstring>
 
 #include "rk_device.cuh"
 
@@ -79,8 +80,11 @@ struct PfBars {
     float2 step16[ROPE_PAIRS];  // cos/sin of a 16-position turn per pair
     int pre_max[PF_THREADS / 32];    // per-warp largest query position (prologue)
     int pre_flags[PF_THREADS / 32];  // per-warp unsafe flags: 1 position, 2 page id
+    int sched[4 + PF_THREADS / 32];  // ragged schedule: level, rank, total units, row; per-warp counts
 };
 static_assert(sizeof(PfBars) <= PF_CTRL_BYTES, "prefill control block exceeds its reservation");
+static_assert((2 * PF_RAGGED_MAX_LEVELS + 1) * 4 <= KSTAGES * PF_TILE_BYTES,
+              "ragged schedule counters exceed the K stage buffers");
 static_assert(PF_SMEM_BYTES <= 232448, "prefill shared memory above the 227 KiB opt-in limit");
 
 __device__ __forceinline__ uint32_t sw_off(int row, int chunk) { return sw128_off(row, chunk); }
@@ -97,6 +101,118 @@ struct RowMap {
     }
 };
 
+// Ragged batch: the rows with two or more queries are cut into pairs of
+// q-tiles (2 rph queries; a row of q queries has np = ceil(q / (2 rph))
+// pairs), one work unit per pair and KV head.  Units are ordered by level d,
+// the pair counted back from the row's last (d = 0: every row's last pair,
+// which sees the most keys), then by row, so the heaviest units start first;
+// for rows of equal length this is the order of the padded grid.  Every CTA
+// derives its own unit w = blockIdx.x / Hkv from qo_indptr alone: a histogram
+// of np in shared memory, the level whose running count passes w, and the
+// rank of the row within that level.  Rows whose indptr entries are unsafe
+// or that hold more than max_q_len queries are left out; CTA 0 flags them
+// and a grid too small for the units (RK_STATUS_POSITION).  All threads call
+// this; it returns false when the CTA has no unit.
+struct RaggedUnit {
+    int b, pair, qs, qn;
+};
+
+__device__ __forceinline__ int ragged_pairs(const PrefillArgs& a, int r, int span, bool& unsafe) {
+    const int qs = __ldg(a.qo_indptr + r), qe = __ldg(a.qo_indptr + r + 1);
+    unsafe = !(qs >= 0 && qe >= qs && qe <= a.total_q && qe - qs <= a.max_q_len);
+    return (!unsafe && qe - qs >= 2) ? (qe - qs + span - 1) / span : 0;
+}
+
+__device__ bool ragged_unit(const PrefillArgs& a, PfBars* bars, int* hist, RaggedUnit& u) {
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int span = 2 * a.rows_per_head;
+    const int L = min((a.max_q_len + span - 1) / span, PF_RAGGED_MAX_LEVELS);
+    int* cnt = hist + L + 1;  // cnt[d]: rows with more than d pairs
+    const int w = (int)(blockIdx.x / a.Hkv);
+    for (int i = tid; i <= L; i += PF_THREADS) hist[i] = 0;
+    __syncthreads();
+    int unsafe_any = 0;
+    for (int r = tid; r < a.B; r += PF_THREADS) {
+        bool un;
+        const int np = ragged_pairs(a, r, span, un);
+        unsafe_any |= un ? 1 : 0;
+        if (np) atomicAdd(&hist[min(np, L)], 1);
+    }
+    unsafe_any = __syncthreads_or(unsafe_any);
+    if (warp == 0) {
+        // suffix sums of the histogram, top chunk of 32 levels first
+        int carry = 0;
+        for (int base = ((L - 1) >> 5) << 5; base >= 0; base -= 32) {
+            const int d = base + lane;
+            int v = d < L ? hist[d + 1] : 0;
+            for (int o = 1; o < 32; o <<= 1) {
+                const int t = __shfl_down_sync(0xffffffffu, v, o);
+                if (lane + o < 32) v += t;
+            }
+            v += carry;
+            if (d < L) cnt[d] = v;
+            carry = __shfl_sync(0xffffffffu, v, 0);
+        }
+        __syncwarp();
+        // the level whose inclusive running count first exceeds w
+        int run = 0, fd = -1, fk = 0;
+        for (int base = 0; base < L; base += 32) {
+            const int d = base + lane;
+            const int c = d < L ? cnt[d] : 0;
+            int v = c;
+            for (int o = 1; o < 32; o <<= 1) {
+                const int t = __shfl_up_sync(0xffffffffu, v, o);
+                if (lane >= o) v += t;
+            }
+            const unsigned hit = __ballot_sync(0xffffffffu, run + v > w);
+            if (fd < 0 && hit) {
+                const int f = __ffs(hit) - 1;
+                fd = base + f;
+                fk = w - (run + __shfl_sync(0xffffffffu, v - c, f));
+            }
+            run += __shfl_sync(0xffffffffu, v, 31);
+        }
+        if (lane == 0) {
+            bars->sched[0] = fd;
+            bars->sched[1] = fk;
+            bars->sched[2] = run;
+            bars->sched[3] = -1;
+        }
+    }
+    __syncthreads();
+    const int d = bars->sched[0], k = bars->sched[1], total = bars->sched[2];
+    if (blockIdx.x == 0 && tid == 0 && a.status && (unsafe_any || total > (int)(gridDim.x / a.Hkv)))
+        atomicOr(a.status, RK_STATUS_POSITION);
+    if (d < 0) return false;
+    // the unit's row: the k-th row, in index order, with more than d pairs
+    int offset = 0;
+    for (int r0 = 0; r0 < a.B; r0 += PF_THREADS) {
+        const int r = r0 + tid;
+        bool un;
+        const bool p = r < a.B && ragged_pairs(a, r, span, un) > d;
+        const unsigned bal = __ballot_sync(0xffffffffu, p);
+        if (lane == 0) bars->sched[4 + warp] = __popc(bal);
+        __syncthreads();
+        int pre = offset, tot = 0;
+        for (int w2 = 0; w2 < PF_THREADS / 32; ++w2) {
+            const int c = bars->sched[4 + w2];
+            pre += w2 < warp ? c : 0;
+            tot += c;
+        }
+        if (p && pre + __popc(bal & ((1u << lane) - 1u)) == k) bars->sched[3] = r;
+        offset += tot;
+        __syncthreads();
+        if (bars->sched[3] >= 0) break;
+    }
+    const int b = bars->sched[3];
+    if (b < 0) return false;  // the two passes read the same qo_indptr: not reached
+    u.b = b;
+    u.qs = __ldg(a.qo_indptr + b);
+    u.qn = __ldg(a.qo_indptr + b + 1) - u.qs;
+    u.pair = (u.qn + span - 1) / span - 1 - d;
+    return true;
+}
+
 __device__ __forceinline__ void write_rows(const PrefillArgs& a, const RowMap& rm, int kvh, int s0, float lse_val) {
     __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(a.out);
     const int rph = a.rows_per_head;
@@ -110,6 +226,14 @@ __device__ __forceinline__ void write_rows(const PrefillArgs& a, const RowMap& r
     }
 }
 
+// Launched after a ragged batch's decode launch with programmatic stream
+// serialization, this grid starts while that one drains (the two write
+// disjoint rows).  Its last CTA waits for that grid before it exits, so the
+// grid completes after it and work ordered after this grid sees both done.
+__device__ __forceinline__ void pdl_tail() {
+    if (blockIdx.x == gridDim.x - 1) griddep_wait();
+}
+
 __global__ void __launch_bounds__(PF_THREADS, 1)
     prefill_kernel(const __grid_constant__ CUtensorMap qmap, const __grid_constant__ CUtensorMap kmap,
                    const __grid_constant__ CUtensorMap vmap, const __grid_constant__ PrefillArgs a) {
@@ -119,31 +243,39 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
     const uint32_t s_base = smem_u32(sm);
     if (s_base & 1023u) {  // the swizzled operand layout needs a 1024-byte aligned base
         if (threadIdx.x == 0 && a.status) atomicOr(a.status, RK_STATUS_TIMEOUT);
+        pdl_tail();
         return;
     }
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, wg = warp >> 2;
 
     // ---- work unit: longest q-tile pairs first (later positions see more keys) ----
-    const int units = a.B * a.Hkv;
-    const int n_pairs = (a.n_qtiles + 1) / 2;
-    const int pair = n_pairs - 1 - (int)(blockIdx.x / units);
-    const int rem = (int)(blockIdx.x % units);
-    const int b = rem / a.Hkv, kvh = rem % a.Hkv;
     const int rph = a.rows_per_head;
-
-    // ---- row metadata (device copy) and memory-safety checks ----
-    RowMap rm{b, a.Sq, b * a.Sq, a.qo_indptr != nullptr};
-    if (rm.ragged) {
-        const int qs = a.qo_indptr[b], qe = a.qo_indptr[b + 1];
-        if (qs < 0 || qe < qs || qe > a.total_q || qe - qs > a.n_qtiles * rph) {
-            // unsafe, or more queries than the grid covers: nothing written
-            if (threadIdx.x == 0 && a.status) atomicOr(a.status, RK_STATUS_POSITION);
+    int b, kvh, pair;
+    RowMap rm{0, a.Sq, 0, a.qo_indptr != nullptr};
+    if (!rm.ragged) {
+        const int units = a.B * a.Hkv;
+        const int n_pairs = (a.n_qtiles + 1) / 2;
+        pair = n_pairs - 1 - (int)(blockIdx.x / units);
+        const int rem = (int)(blockIdx.x % units);
+        b = rem / a.Hkv;
+        kvh = rem % a.Hkv;
+        rm.b = b;
+        rm.qbase = b * a.Sq;
+    } else {
+        RaggedUnit u;
+        if (!ragged_unit(a, bars, reinterpret_cast<int*>(sm + OFF_K), u)) {
+            pdl_tail();
             return;
         }
-        if (qe - qs < 2) return;  // no query, or a single-query row (decode kernel)
-        rm.qn = qe - qs;
-        rm.qbase = qs;
+        b = u.b;
+        kvh = (int)(blockIdx.x % a.Hkv);
+        pair = u.pair;
+        rm.b = b;
+        rm.qn = u.qn;
+        rm.qbase = u.qs;
     }
+
+    // ---- row metadata (device copy) and memory-safety checks ----
     const int kv_len = a.kv_lens[b];
     const int32_t* pos_row = a.position_ids + rm.qbase;
     int bad = 0;
@@ -236,6 +368,7 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
         const float lv = bad ? __int_as_float(0x7fc00000) : -INFINITY;
         write_rows(a, rm, kvh, s00, lv);
         write_rows(a, rm, kvh, s00 + rph, lv);
+        pdl_tail();
         return;
     }
 
@@ -615,12 +748,13 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
         tc_fence_after();
         tmem_dealloc(tmem, TMEM_COLS);
     }
+    pdl_tail();
 }
 
 }  // namespace
 
 cudaError_t launch_prefill(const CUtensorMap& qm, const CUtensorMap& km, const CUtensorMap& vm,
-                           const PrefillArgs& a, cudaStream_t stream) {
+                           const PrefillArgs& a, cudaStream_t stream, bool overlap_previous) {
     static std::atomic<uint64_t> configured{0};
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
@@ -631,11 +765,27 @@ cudaError_t launch_prefill(const CUtensorMap& qm, const CUtensorMap& km, const C
         if (e != cudaSuccess) return e;
         configured.fetch_or(bit);
     }
-    const long long grid = (long long)a.B * a.Hkv * ((a.n_qtiles + 1) / 2);
+    const long long grid = a.qo_indptr ? (long long)a.ragged_units * a.Hkv
+                                       : (long long)a.B * a.Hkv * ((a.n_qtiles + 1) / 2);
     if (grid <= 0) return cudaSuccess;
     if (grid > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
-    prefill_kernel<<<(unsigned)grid, PF_THREADS, PF_SMEM_BYTES, stream>>>(qm, km, vm, a);
-    return cudaGetLastError();
+    if (!overlap_previous) {
+        prefill_kernel<<<(unsigned)grid, PF_THREADS, PF_SMEM_BYTES, stream>>>(qm, km, vm, a);
+        return cudaGetLastError();
+    }
+    cudaLaunchConfig_t cfg;
+    std::memset(&cfg, 0, sizeof cfg);
+    cfg.gridDim = dim3((unsigned)grid);
+    cfg.blockDim = dim3(PF_THREADS);
+    cfg.dynamicSmemBytes = PF_SMEM_BYTES;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr;
+    std::memset(&attr, 0, sizeof attr);
+    attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr.val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = &attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, prefill_kernel, qm, km, vm, a);
 }
 
 }  // namespace rk

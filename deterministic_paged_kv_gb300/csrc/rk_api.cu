@@ -4,6 +4,7 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <atomic>
 #include <climits>
 #include <cmath>
@@ -21,7 +22,7 @@ namespace rk {
 cudaError_t launch_decode(const CUtensorMap& km, const CUtensorMap& vm, const DecodeArgs& a,
                           cudaStream_t stream);
 cudaError_t launch_prefill(const CUtensorMap& qm, const CUtensorMap& km, const CUtensorMap& vm,
-                           const PrefillArgs& a, cudaStream_t stream);
+                           const PrefillArgs& a, cudaStream_t stream, bool overlap_previous = false);
 cudaError_t launch_kv_append(const AppendArgs& a, cudaStream_t stream);
 }  // namespace rk
 
@@ -277,6 +278,7 @@ int rk_paged_plan(rk_paged_plan_t* plan, int32_t B, int32_t Sq, int32_t Hq, int3
     plan->num_pages = num_pages;
     plan->causal = 1;
     plan->max_kv_len = max_kv;
+    plan->pf_units = -1;
     plan->sm_scale = (float)(1.0 / std::sqrt((double)D));
     plan->validated = check ? 1 : 0;
     plan->rope_theta = rope_theta;
@@ -329,6 +331,13 @@ int rk_paged_plan_ragged(rk_paged_plan_t* plan, int32_t B, int32_t total_q, int3
         plan->max_kv_len = max_kv;
         plan->validated = 1;
     }
+    const int32_t span = 2 * (rk::PF_BM / (Hq / Hkv));
+    int64_t units = 0;
+    for (int b = 0; b < B; ++b) {
+        const int32_t n = qo_indptr_h[b + 1] - qo_indptr_h[b];
+        if (n >= 2) units += (n + span - 1) / span;
+    }
+    plan->pf_units = (int32_t)units;  // at most total_q / 2
     *max_q_len = mq;
     return RK_OK;
 }
@@ -631,12 +640,29 @@ int rk_paged_attn_ragged(const rk_paged_plan_t* plan, int32_t max_q_len, const i
         a.qk_scale_log2 = qk;
         a.qo_indptr = qo_indptr_d;
         a.total_q = total_q;
+        a.max_q_len = max_q_len;
         std::memcpy(a.rope_turns, plan->rope_turns, sizeof a.rope_turns);
         cudaError_t e = rk::launch_decode(km, vm, a, st);
         if (e != cudaSuccess) return fail(RK_E_CUDA, "ragged decode launch: %s", cudaGetErrorString(e));
     }
     if (max_q_len < 2) return RK_OK;
-    // rows of two or more queries: the prefill kernel; packed q [total_q, Hq, D]
+    // rows of two or more queries: the prefill kernel, one CTA per work unit
+    // (pair of q-tiles) and KV head.  Without a count from the plan, bound the
+    // units over every batch of this shape: at most m = min(B, total_q / 2)
+    // rows hold two or more queries, each row at most levels pairs, and all
+    // of them together at most (total_q + (span - 1) m) / span.
+    const int64_t span = 2 * rph;
+    const int64_t levels = (max_q_len + span - 1) / span;
+    if (levels > rk::PF_RAGGED_MAX_LEVELS)
+        return fail(RK_E_UNSUPPORTED, "max_q_len %d needs %lld pairs of q-tiles per row (at most %d)", max_q_len,
+                    (long long)levels, rk::PF_RAGGED_MAX_LEVELS);
+    int64_t units = plan->pf_units;
+    if (units < 0) {
+        const int64_t m = std::min<int64_t>(plan->B, total_q / 2);
+        units = std::min<int64_t>(m * levels, ((int64_t)total_q + (span - 1) * m) / span);
+    }
+    units = std::max<int64_t>(units, 1);  // one CTA still checks the device indptr
+    // packed q [total_q, Hq, D]
     // seen as (d, token, head) so that a box (64, 128/G tokens, G heads) lands
     // head-major like the padded layout's q-tile
     CUtensorMap qm, km, vm;
@@ -671,8 +697,11 @@ int rk_paged_attn_ragged(const rk_paged_plan_t* plan, int32_t max_q_len, const i
     a.qk_scale_log2 = qk;
     a.qo_indptr = qo_indptr_d;
     a.total_q = total_q;
+    a.max_q_len = max_q_len;
+    a.ragged_units = (int32_t)units;
     std::memcpy(a.rope_turns, plan->rope_turns, sizeof a.rope_turns);
-    cudaError_t e = rk::launch_prefill(qm, km, vm, a, st);
+    // started while the decode launch drains: the two write disjoint rows
+    cudaError_t e = rk::launch_prefill(qm, km, vm, a, st, true);
     if (e != cudaSuccess) return fail(RK_E_CUDA, "ragged prefill launch: %s", cudaGetErrorString(e));
     return RK_OK;
 }

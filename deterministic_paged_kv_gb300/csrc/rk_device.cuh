@@ -164,6 +164,16 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
+// ------------------------------------------------- programmatic launch ----
+// A grid launched next on the stream with programmatic stream serialization
+// may start its CTAs once every CTA of this grid has executed this or exited.
+__device__ __forceinline__ void griddep_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+// Wait until the grids this one depends on programmatically have completed
+// and their writes are visible (at once for a launch without that dependency).
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 // ------------------------------------------------------------ tcgen05 ----
 
 // Allocate `ncols` TMEM columns (power of two >= 32); whole warp executes.

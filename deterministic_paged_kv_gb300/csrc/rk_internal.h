@@ -50,7 +50,7 @@ struct DecodeArgs {
     // with exactly one query.
     const int32_t* qo_indptr;
     int32_t total_q;
-    int32_t pad1;
+    int32_t max_q_len;            // rows with more queries are flagged (RK_STATUS_POSITION)
     uint64_t rope_turns[ROPE_PAIRS];
 };
 constexpr int DEC_SPLIT_GRAIN = 1024;  // split lengths are multiples of this many tokens (8 KV tiles)
@@ -79,9 +79,14 @@ struct PrefillArgs {
     // two or more queries (single-query rows go to the decode kernel).
     const int32_t* qo_indptr;
     int32_t total_q;
+    int32_t max_q_len;            // ragged: rows with more queries are not computed
+    int32_t ragged_units;         // ragged: work units of the grid (grid = ragged_units x Hkv)
     int32_t pad0;
     uint64_t rope_turns[ROPE_PAIRS];
 };
+// Ragged prefill schedule: the largest pair count of a row it handles (the
+// per-CTA scan keeps 2 x levels + 1 counters in a K stage buffer).
+constexpr int PF_RAGGED_MAX_LEVELS = 12000;
 
 // ------------------------------------------------------------ append ----
 // Write n_new tokens per row into the page cache (kv_lens after the append).

@@ -57,7 +57,7 @@
 extern "C" {
 #endif
 
-#define RK_PAGED_ABI_VERSION 1u
+#define RK_PAGED_ABI_VERSION 2u
 #define RK_PAGED_MAX_ROPE_PAIRS 64
 
 /* Status codes returned by the entry points. */
@@ -96,6 +96,11 @@ typedef struct rk_paged_plan {
     int32_t max_kv_len;   /* largest kv_len seen at plan time (0 for a shape-only plan) */
     float sm_scale;       /* 1 / sqrt(D) */
     int32_t validated;    /* 1 when metadata contents were checked, 0 for a shape-only plan */
+    /* Ragged batches: work units of the prefill grid (pairs of q-tiles of
+     * the rows with two or more queries), counted by rk_paged_plan_ragged
+     * from qo_indptr_h; -1 (rk_paged_plan, or set by the caller) sizes the
+     * grid for any contents with this total_q and max_q_len. */
+    int32_t pf_units;
     double rope_theta, rope_scale;
     /* Rotation rate of pair i in turns per position as a 0.64 fixed-point
      * fraction: round(2^64 * theta^(-2i/D) / (2 pi rope_scale)), i < D/2. */
@@ -278,7 +283,9 @@ int rk_paged_kv_append(const rk_paged_plan_t *plan, int32_t n_new, const void *k
  * then shapes and, when all three metadata arrays are given, the same list
  * as rk_paged_plan per row (rows with no query are skipped by the position
  * rules).  The plan holds Sq = total_q.  *max_q_len receives the largest
- * per-row query count (the prefill grid is sized by it).  Host only.
+ * per-row query count; plan->pf_units the number of prefill work units, a
+ * pair of q-tiles (2 x 128 / (Hq / Hkv) queries) of a row with two or more
+ * queries, which sizes the prefill grid exactly.  Host only.
  */
 int rk_paged_plan_ragged(rk_paged_plan_t *plan, int32_t B, int32_t total_q, int32_t Hq, int32_t Hkv,
                          int32_t D, int32_t page_size, int32_t num_pages, int32_t W,
@@ -295,11 +302,16 @@ int rk_paged_plan_ragged(rk_paged_plan_t *plan, int32_t B, int32_t total_q, int3
  *   qo_indptr_d   DEVICE int32 [B + 1].  Other buffers as above, DEVICE,
  *                 q / out / caches 16-byte aligned.
  * Two launches on `stream` (decode rows, then prefill rows), no allocation,
- * no host synchronisation: metadata is read on the device, so a captured
- * graph replays with new contents that respect max_q_len.  A row whose
- * qo_indptr entries are out of range or decreasing is not written and sets
- * RK_STATUS_POSITION.  Errors as rk_paged_attn_prefill, plus RK_E_ARG for
- * max_q_len or qo_indptr_d.
+ * no host synchronisation: metadata is read on the device, and each prefill
+ * CTA finds its work unit from qo_indptr_d (heaviest units first).  The
+ * prefill grid holds plan->pf_units units (for pf_units = -1: a bound that
+ * covers every batch of this total_q and max_q_len), so a captured graph
+ * replays with new contents that respect max_q_len and, unless pf_units is
+ * -1, need no more units than the plan counted.  A row whose qo_indptr
+ * entries are out of range or decreasing is not written and sets
+ * RK_STATUS_POSITION, as does work beyond the grid.  Errors as
+ * rk_paged_attn_prefill, plus RK_E_ARG for max_q_len or qo_indptr_d, and
+ * RK_E_UNSUPPORTED for more than 12000 pairs of q-tiles in one row.
  */
 int rk_paged_attn_ragged(const rk_paged_plan_t *plan, int32_t max_q_len, const int32_t *qo_indptr_d,
                          const void *q, const void *k_cache, const void *v_cache,

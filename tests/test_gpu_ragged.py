@@ -156,3 +156,68 @@ def test_ragged_status_on_unsafe_indptr_and_oversize_rows():
     assert int(st.item()) & binding.STATUS_POSITION
     s3, e3 = int(ind[3]), int(ind[4])
     assert bitwise_equal(out[s3:e3], good_out[s3:e3])
+    # max_q_len 1: only the decode launch runs; it flags the longer rows
+    st.zero_()
+    out.fill_(float("nan"))
+    binding.attn_ragged(p, 1, ind.cuda(), q.cuda(), d["k_cache"], d["v_cache"], d["block_table"], d["kv_lens"],
+                        pos.cuda(), out, lse, status=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) & binding.STATUS_POSITION
+    s2, e2 = int(ind[2]), int(ind[3])
+    assert bitwise_equal(out[s2:e2], good_out[s2:e2]) and bool(torch.isnan(out[s0:e0].float()).all())
+
+
+def _launch(w, p, max_q_len, ind=None, status=None):
+    q, ind0, pos = workloads.pack_ragged(w)
+    ind = ind0 if ind is None else ind
+    d = to_dev(w)
+    out = torch.full((q.shape[0], w.Hq, w.D), float("nan"), dtype=torch.bfloat16, device="cuda")
+    lse = torch.full((q.shape[0], w.Hq), float("nan"), dtype=torch.float32, device="cuda")
+    binding.attn_ragged(p, max_q_len, ind.cuda(), q.cuda(), d["k_cache"], d["v_cache"], d["block_table"],
+                        d["kv_lens"], pos.cuda(), out, lse, status=status)
+    torch.cuda.synchronize()
+    return out, lse
+
+
+@pytest.mark.parametrize("case", ["600_rows", "35_levels"])
+def test_ragged_many_rows_and_levels_match_oracle_and_the_bounded_grid(case):
+    """600 rows (more than the 512 threads that rank rows in one pass), or one
+    row of 35 pairs of q-tiles (more than the 32 levels one warp scans at a
+    time), G = 8 (32-query pairs): parity with the oracle, and the grid bounded
+    over every batch of this shape (pf_units = -1) gives the same bits as the
+    exact count."""
+    rng = np.random.default_rng(123)
+    if case == "600_rows":
+        q_lens = [int(x) for x in rng.choice([1, 1, 1, 2, 3, 17, 33, 64, 65], size=600)]
+    else:
+        q_lens = [1, 1100, 40, 2, 0, 1]
+    kv_lens = [int(n + rng.integers(0, 40)) for n in q_lens]
+    w = workloads.ragged_case(q_lens, kv_lens, seed=131, Hq=8, Hkv=1)
+    q, ind, pos = workloads.pack_ragged(w)
+    p, mq = binding.plan_ragged(w.B, q.shape[0], w.Hq, w.Hkv, w.D, 16, w.num_pages, w.W, ind, w.block_table,
+                                w.kv_lens, pos, w.rope_theta, w.rope_scale)
+    assert p.pf_units == sum(-(-n // 32) for n in q_lens if n >= 2)
+    out, lse = _launch(w, p, mq)
+    po, pl = padded_view(w, out, lse, ind)
+    m = row_mask(w)
+    ro, rl = oracle_ref(w, row_mask=m)
+    assert_parity(po, pl, ro, rl, mask=m)
+    p.pf_units = -1
+    out2, lse2 = _launch(w, p, mq)
+    assert bitwise_equal(out, out2) and bitwise_equal(lse, lse2)
+
+
+def test_ragged_grid_smaller_than_the_device_batch_is_flagged():
+    """A plan counted from another qo_indptr of the same total_q: the units
+    that fit are computed (bitwise as usual), the rest flag RK_STATUS_POSITION."""
+    w = workloads.ragged_case([2, 2, 1, 1], [100, 300, 50, 60], seed=137)
+    good_out, good_lse, ind = run_ragged(w)
+    T = int(ind[-1])
+    p_small, _ = binding.plan_ragged(w.B, T, w.Hq, w.Hkv, w.D, 16, w.num_pages, w.W, [0, 3, 4, 5, 6])
+    assert p_small.pf_units == 1
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    out, lse = _launch(w, p_small, 2, status=st)
+    assert int(st.item()) & binding.STATUS_POSITION
+    # unit 0 (level 0, first row) ran; decode rows ran in their own launch
+    assert bitwise_equal(out[0:2], good_out[0:2]) and bitwise_equal(lse[0:2], good_lse[0:2])
+    assert bitwise_equal(out[4:6], good_out[4:6]) and bitwise_equal(lse[4:6], good_lse[4:6])

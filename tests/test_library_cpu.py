@@ -76,7 +76,7 @@ def _plan(rk, B, Sq, Hq, Hkv, D, P, NP, W, bt, kv, pos, theta=1e6, scale=1.0):
 def test_plan_accepts_valid_decode_and_fills_fields(rk):
     bt, kv, pos = _ok_case()
     p = _plan(rk, 2, 1, 32, 8, 128, 16, 10, 4, bt, kv, pos)
-    assert p.abi == 1 and p.B == 2 and p.Sq == 1 and p.W == 4 and p.num_pages == 10
+    assert p.abi == rk.ABI_VERSION and p.B == 2 and p.Sq == 1 and p.W == 4 and p.num_pages == 10
     assert p.causal == 1 and p.max_kv_len == 40 and p.validated == 1
     assert p.sm_scale == pytest.approx(1 / math.sqrt(128))
     # also the kv_len-1 convention and a shape-only plan
@@ -209,6 +209,8 @@ def test_ragged_plan_validation_host_only(rk):
     T = q.shape[0]
     p, mq = rk.plan_ragged(w.B, T, 32, 8, 128, 16, w.num_pages, w.W, ind, w.block_table, w.kv_lens, pos)
     assert mq == 5 and p.Sq == T and p.validated == 1
+    assert p.pf_units == 2  # rows of 5 and 3 queries: one pair of 32-query q-tiles each
+    assert rk.plan(2, 1, 32, 8, 128, 16, 10, 4).pf_units == -1  # padded plan: no count
     for bad_ind in ([1, 1, 1, 6, 9], [0, 1, 0, 6, 9], [0, 1, 1, 6, 8]):
         with pytest.raises(rk.RkError) as e:
             rk.plan_ragged(w.B, T, 32, 8, 128, 16, w.num_pages, w.W, bad_ind, w.block_table, w.kv_lens, pos)
@@ -218,3 +220,20 @@ def test_ragged_plan_validation_host_only(rk):
     with pytest.raises(rk.RkError) as e:
         rk.plan_ragged(w.B, T, 32, 8, 128, 16, w.num_pages, w.W, ind, w.block_table, w.kv_lens, bad_pos)
     assert e.value.name == "RK_E_POSITION"
+
+
+@pytest.mark.parametrize("Hq,Hkv,expect", [(32, 8, 7), (32, 32, 4), (32, 4, 11)])
+def test_ragged_plan_counts_prefill_work_units(rk, Hq, Hkv, expect):
+    """pf_units = sum over rows of two or more queries of ceil(q / (2 x 128 / G)):
+    q-tiles hold 128 / G query positions and a work unit is a pair of them."""
+    from deterministic_paged_kv_gb300 import workloads
+    q_lens = [1, 130, 64, 65, 2, 0]
+    w = workloads.ragged_case(q_lens, [40, 200, 64, 100, 2, 7], seed=4, Hq=Hq, Hkv=Hkv)
+    q, ind, pos = workloads.pack_ragged(w)
+    p, mq = rk.plan_ragged(w.B, q.shape[0], Hq, Hkv, 128, 16, w.num_pages, w.W, ind, w.block_table,
+                           w.kv_lens, pos)
+    span = 2 * 128 // (Hq // Hkv)
+    assert mq == 130 and p.pf_units == expect == sum(-(-n // span) for n in q_lens if n >= 2)
+    # the count depends on qo_indptr alone: a shape-only ragged plan agrees
+    p2, _ = rk.plan_ragged(w.B, q.shape[0], Hq, Hkv, 128, 16, w.num_pages, w.W, ind)
+    assert p2.pf_units == expect and p2.validated == 0
