@@ -76,6 +76,13 @@ def _load():
             ctypes.c_void_p, ctypes.c_int, ctypes.c_int, ctypes.c_int,
             ctypes.c_int, ctypes.c_int, i32p, ctypes.c_int, i32p,
             ctypes.c_int, f64p]
+        lib.rk_oracle_attention_backward.restype = ctypes.c_int
+        lib.rk_oracle_attention_backward.argtypes = (
+            [ctypes.c_int] * 8
+            + [ctypes.c_void_p] * 3
+            + [ctypes.c_int, ctypes.c_void_p, ctypes.c_int, i32p, i32p, i32p,
+               ctypes.c_double, ctypes.c_double, ctypes.c_double]
+            + [ctypes.c_void_p] * 6 + [ctypes.c_int])
         lib.rk_oracle_max_threads.restype = ctypes.c_int
         lib.rk_oracle_max_threads.argtypes = []
         _lib = lib
@@ -196,3 +203,52 @@ def attention(q, k_cache, v_cache, block_table, kv_lens, position_ids,
     if rc != 0:
         raise ValueError("oracle attention failed with code %d" % rc)
     return out, lse
+
+
+def attention_backward(q, k_cache, v_cache, block_table, kv_lens, position_ids, dout,
+                       rope_theta: float = 1e6, rope_scale: float = 1.0,
+                       sm_scale: float | None = None, magnitudes: bool = False,
+                       threads: int | None = None):
+    """Float64 gradient of ``attention`` for L = sum(dout * out).
+
+    Returns ``(dq [B,Hq,Sq,D], dk, dv)`` with dk / dv in the cache layout
+    [num_pages, page_size, Hkv, D]: the pages a row references are written in
+    full (0 at slots past kv_len), every other entry is NaN.  With
+    ``magnitudes`` also returns ``(mag_dq, mag_dk, mag_dv)``: per element the
+    sum of the absolute values of its terms.  ``dout`` is [B, Hq, Sq, D],
+    float or bfloat16 bits; q / caches as in ``attention``.
+    """
+    lib = _load()
+    qa, qcode = _qkv(q)
+    ka, kcode = _qkv(k_cache)
+    va, vcode = _qkv(v_cache)
+    ga, gcode = _qkv(dout)
+    if not (qcode == kcode == vcode):
+        raise TypeError("q, k_cache and v_cache must share one element type")
+    B, Hq, Sq, D = qa.shape
+    NP, P, Hkv, D2 = ka.shape
+    if D2 != D or va.shape != ka.shape or ga.shape != qa.shape:
+        raise ValueError("shape mismatch")
+    bt = _i32(block_table)
+    kl = _i32(kv_lens)
+    pos = _i32(position_ids)
+    if bt.shape[0] != B or kl.shape != (B,) or pos.shape != (B, Sq):
+        raise ValueError("metadata shape mismatch")
+    if sm_scale is None:
+        sm_scale = 1.0 / np.sqrt(D)
+    dq = np.full((B, Hq, Sq, D), np.nan, dtype=np.float64)
+    dk = np.full((NP, P, Hkv, D), np.nan, dtype=np.float64)
+    dv = np.full((NP, P, Hkv, D), np.nan, dtype=np.float64)
+    mags = [np.full_like(dq, np.nan), np.full_like(dk, np.nan), np.full_like(dv, np.nan)] if magnitudes else None
+    mp = [m.ctypes.data for m in mags] if mags else [None, None, None]
+    rc = lib.rk_oracle_attention_backward(B, Sq, Hq, Hkv, D, P, NP, bt.shape[1],
+                                          qa.ctypes.data, ka.ctypes.data, va.ctypes.data, qcode,
+                                          ga.ctypes.data, gcode, _ptr_i32(bt), _ptr_i32(kl), _ptr_i32(pos),
+                                          float(rope_theta), float(rope_scale), float(sm_scale),
+                                          dq.ctypes.data, dk.ctypes.data, dv.ctypes.data,
+                                          mp[0], mp[1], mp[2], int(threads or 0))
+    if rc != 0:
+        raise ValueError("oracle attention_backward failed with code %d" % rc)
+    if magnitudes:
+        return dq, dk, dv, tuple(mags)
+    return dq, dk, dv

@@ -261,6 +261,205 @@ int rk_oracle_attention(int B, int Sq, int Hq, int Hkv, int D, int page_size,
     return err;
 }
 
+/*
+ * Gradient of the same attention, float64: "Add FlashInfer RoPE-fused paged
+ * attention scaffold", scope table, Backward row (dropout 0, deterministic
+ * backward).  For the scalar L = sum over (b, h, s, d) of dout * out, with
+ * out as computed by rk_oracle_attention, it returns dL/dq, dL/dk_cache and
+ * dL/dv_cache.  Per query (rotated q' at position p, visible keys t < nv,
+ * rotated keys k'_t):
+ *
+ *   s_t   = sm_scale * (q' . k'_t),   P_t = exp(s_t - lse),   out = sum_t P_t v_t
+ *   Dq    = dout . out
+ *   dP_t  = dout . v_t,               dS_t = P_t (dP_t - Dq)
+ *   dv_t += P_t dout                  dk'_t += sm_scale dS_t q'
+ *   dq'   = sm_scale sum_t dS_t k'_t
+ *
+ * and the rotation is undone with its transpose (rotation by the negative
+ * angle): dq = R(p)^T dq', dk_t = R(t)^T dk'_t.  The derivation is the chain
+ * rule through the softmax (d softmax_t / d s_u = P_t (delta_tu - P_u)).
+ *
+ * Outputs: dq [B, Hq, Sq, D]; dk, dv in the cache layout [num_pages,
+ * page_size, Hkv, D].  For every row the pages of its first ceil(kv_len / P)
+ * table entries are written in full (slots at or past kv_len get 0); other
+ * pages are left untouched.  mag_dq / mag_dk / mag_dv (optional, same
+ * layouts) receive the sums of the absolute values of the terms of each
+ * output element (after the rotation: |R^T x|_i <= |x_i| + |x_(i +- D/2)|),
+ * from which rounding-error bounds of other implementations are derived.
+ * Work is split over (b, KV head): each unit owns its keys' dk / dv.
+ */
+int rk_oracle_attention_backward(int B, int Sq, int Hq, int Hkv, int D, int page_size,
+                                 int num_pages, int W, const void *q, const void *k_cache,
+                                 const void *v_cache, int qkv_dtype, const void *dout,
+                                 int dout_dtype, const int32_t *block_table,
+                                 const int32_t *kv_lens, const int32_t *position_ids,
+                                 double rope_theta, double rope_scale, double sm_scale,
+                                 double *dq, double *dk, double *dv, double *mag_dq,
+                                 double *mag_dk, double *mag_dv, int nthreads) {
+    if (B < 0 || Sq < 0 || Hq <= 0 || Hkv <= 0 || D <= 0 || (D % 2) ||
+        page_size <= 0 || W < 0 || Hq % Hkv)
+        return ORACLE_E_ARG;
+    const int G = Hq / Hkv, half = D / 2;
+    const int64_t units = (int64_t)B * Hkv;
+    int err = ORACLE_OK;
+#ifdef _OPENMP
+    if (nthreads > 0) omp_set_num_threads(nthreads);
+#pragma omp parallel for schedule(dynamic, 1)
+#endif
+    for (int64_t u = 0; u < units; ++u) {
+        const int b = (int)(u / Hkv), kh = (int)(u % Hkv);
+        const int n = kv_lens[b];
+        if (n < 0 || n > W * page_size) {
+#ifdef _OPENMP
+#pragma omp atomic write
+#endif
+            err = ORACLE_E_ARG;
+            continue;
+        }
+        const size_t nd = (size_t)n * D + 1;
+        double *kr = (double *)malloc(sizeof(double) * nd);   /* rotated keys */
+        double *vr = (double *)malloc(sizeof(double) * nd);
+        double *gk = (double *)calloc(nd, sizeof(double));    /* dk' (rotated domain) */
+        double *gv = (double *)calloc(nd, sizeof(double));
+        double *mk = (double *)calloc(nd, sizeof(double));    /* magnitudes of dk' terms */
+        double *mv = (double *)calloc(nd, sizeof(double));
+        double *pr = (double *)malloc(sizeof(double) * ((size_t)n + 1));
+        double *ds = (double *)malloc(sizeof(double) * ((size_t)n + 1));
+        double *tmp = (double *)malloc(sizeof(double) * (size_t)D);
+        double *qr = (double *)malloc(sizeof(double) * (size_t)D);
+        double *go = (double *)malloc(sizeof(double) * (size_t)D);
+        double *ov = (double *)malloc(sizeof(double) * (size_t)D);
+        double *gq = (double *)malloc(sizeof(double) * (size_t)D);
+        double *mq = (double *)malloc(sizeof(double) * (size_t)D);
+        if (!kr || !vr || !gk || !gv || !mk || !mv || !pr || !ds || !tmp || !qr || !go || !ov || !gq || !mq) {
+            free(kr); free(vr); free(gk); free(gv); free(mk); free(mv); free(pr); free(ds);
+            free(tmp); free(qr); free(go); free(ov); free(gq); free(mq);
+#ifdef _OPENMP
+#pragma omp atomic write
+#endif
+            err = ORACLE_E_NOMEM;
+            continue;
+        }
+        int bad = 0;
+        for (int t = 0; t < n && !bad; ++t) {
+            int page = block_table[(int64_t)b * W + t / page_size];
+            if (page < 0 || page >= num_pages) { bad = 1; break; }
+            int64_t src = (((int64_t)page * page_size + t % page_size) * Hkv + kh) * D;
+            for (int d = 0; d < D; ++d) {
+                tmp[d] = to_f64(k_cache, src + d, qkv_dtype);
+                vr[(int64_t)t * D + d] = to_f64(v_cache, src + d, qkv_dtype);
+            }
+            rk_oracle_rope(tmp, D, (double)t, rope_theta, rope_scale, kr + (int64_t)t * D);
+        }
+        for (int g = 0; g < G && !bad; ++g) {
+            const int h = kh * G + g;
+            for (int s = 0; s < Sq; ++s) {
+                const int p = position_ids[(int64_t)b * Sq + s];
+                const int nv = p < 0 ? 0 : (p + 1 < n ? p + 1 : n);
+                const int64_t qoff = (((int64_t)b * Hq + h) * Sq + s) * D;
+                if (nv == 0) {  /* out = 0 does not depend on anything */
+                    for (int d = 0; d < D; ++d) {
+                        dq[qoff + d] = 0.0;
+                        if (mag_dq) mag_dq[qoff + d] = 0.0;
+                    }
+                    continue;
+                }
+                for (int d = 0; d < D; ++d) tmp[d] = to_f64(q, qoff + d, qkv_dtype);
+                rk_oracle_rope(tmp, D, (double)p, rope_theta, rope_scale, qr);
+                for (int d = 0; d < D; ++d) go[d] = to_f64(dout, qoff + d, dout_dtype);
+                /* forward again: probabilities and the output */
+                double m = -INFINITY;
+                for (int t = 0; t < nv; ++t) {
+                    double acc = 0.0;
+                    const double *kt = kr + (int64_t)t * D;
+                    for (int d = 0; d < D; ++d) acc += qr[d] * kt[d];
+                    pr[t] = acc * sm_scale;
+                    if (pr[t] > m) m = pr[t];
+                }
+                double sum = 0.0;
+                for (int t = 0; t < nv; ++t) {
+                    pr[t] = exp(pr[t] - m);
+                    sum += pr[t];
+                }
+                for (int d = 0; d < D; ++d) ov[d] = 0.0;
+                for (int t = 0; t < nv; ++t) {
+                    pr[t] /= sum;
+                    const double *vt = vr + (int64_t)t * D;
+                    for (int d = 0; d < D; ++d) ov[d] += pr[t] * vt[d];
+                }
+                double Dq = 0.0;
+                for (int d = 0; d < D; ++d) Dq += go[d] * ov[d];
+                /* softmax gradient */
+                for (int t = 0; t < nv; ++t) {
+                    double dp = 0.0;
+                    const double *vt = vr + (int64_t)t * D;
+                    for (int d = 0; d < D; ++d) dp += go[d] * vt[d];
+                    ds[t] = pr[t] * (dp - Dq);
+                }
+                /* dq' and its magnitudes; dk', dv accumulate over queries */
+                for (int d = 0; d < D; ++d) { gq[d] = 0.0; mq[d] = 0.0; }
+                for (int t = 0; t < nv; ++t) {
+                    const double *kt = kr + (int64_t)t * D;
+                    double *gkt = gk + (int64_t)t * D, *gvt = gv + (int64_t)t * D;
+                    double *mkt = mk + (int64_t)t * D, *mvt = mv + (int64_t)t * D;
+                    const double w = sm_scale * ds[t], aw = fabs(w);
+                    for (int d = 0; d < D; ++d) {
+                        gq[d] += w * kt[d];
+                        mq[d] += aw * fabs(kt[d]);
+                        gkt[d] += w * qr[d];
+                        mkt[d] += aw * fabs(qr[d]);
+                        gvt[d] += pr[t] * go[d];
+                        mvt[d] += pr[t] * fabs(go[d]);
+                    }
+                }
+                /* back to the pre-rotation domain: dq = R(p)^T dq' */
+                for (int d = 0; d < D; ++d) tmp[d] = gq[d];
+                rk_oracle_rope(tmp, D, -(double)p, rope_theta, rope_scale, dq + qoff);
+                if (mag_dq)
+                    for (int i = 0; i < half; ++i) {
+                        const double a = mq[i] + mq[i + half];
+                        mag_dq[qoff + i] = a;
+                        mag_dq[qoff + i + half] = a;
+                    }
+            }
+        }
+        if (!bad) {
+            /* write the row's pages: dk_t = R(t)^T dk'_t, dv_t; 0 past kv_len */
+            const int npages = (n + page_size - 1) / page_size;
+            for (int t = 0; t < npages * page_size; ++t) {
+                int page = block_table[(int64_t)b * W + t / page_size];
+                int64_t dst = (((int64_t)page * page_size + t % page_size) * Hkv + kh) * D;
+                if (t < n) {
+                    rk_oracle_rope(gk + (int64_t)t * D, D, -(double)t, rope_theta, rope_scale, dk + dst);
+                    for (int d = 0; d < D; ++d) dv[dst + d] = gv[(int64_t)t * D + d];
+                    for (int i = 0; i < half; ++i) {
+                        const double a = mk[(int64_t)t * D + i] + mk[(int64_t)t * D + i + half];
+                        if (mag_dk) { mag_dk[dst + i] = a; mag_dk[dst + i + half] = a; }
+                    }
+                    if (mag_dv)
+                        for (int d = 0; d < D; ++d) mag_dv[dst + d] = mv[(int64_t)t * D + d];
+                } else {
+                    for (int d = 0; d < D; ++d) {
+                        dk[dst + d] = 0.0;
+                        dv[dst + d] = 0.0;
+                        if (mag_dk) mag_dk[dst + d] = 0.0;
+                        if (mag_dv) mag_dv[dst + d] = 0.0;
+                    }
+                }
+            }
+        }
+        free(kr); free(vr); free(gk); free(gv); free(mk); free(mv); free(pr); free(ds);
+        free(tmp); free(qr); free(go); free(ov); free(gq); free(mq);
+        if (bad) {
+#ifdef _OPENMP
+#pragma omp atomic write
+#endif
+            err = ORACLE_E_PAGE;
+        }
+    }
+    return err;
+}
+
 /* Threads OpenMP will use for a parallel region (1 without OpenMP). */
 int rk_oracle_max_threads(void) {
 #ifdef _OPENMP

@@ -1,0 +1,197 @@
+"""Pins for the oracle's attention gradient (``oracle.attention_backward``),
+independent of its code.
+
+The gradient of L = sum(dout * out) is checked against central finite
+differences of the (separately pinned) float64 forward, against reverse-mode
+autodiff of a dense attention written here in torch, and against closed forms
+that hold for the exact gradient: the keys' dv sum to the queries' dout, the
+rotated-domain dk sums to zero, a single visible key passes dout straight to
+dv and nothing to q or k, and a zero dout gives zero gradients.  A slip in the
+softmax derivative (a missing Dq = dout . out term, a wrong sign), in the
+scale, in the inverse rotation, in the GQA accumulation or in the page
+scatter fails at least one of them.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+
+THETA = 1e6
+
+
+def _case(seed, D=16, Hq=4, Hkv=2, kv=(37, 20), Sq=3, NP=6, conv=(0, 1)):
+    """Two rows on shuffled pages; row b's queries at the trailing positions
+    (conv 0: last position kv_len - 1, conv 1: kv_len)."""
+    rng = np.random.default_rng(seed)
+    B = len(kv)
+    kc = rng.standard_normal((NP, 16, Hkv, D))
+    vc = rng.standard_normal((NP, 16, Hkv, D))
+    perm = rng.permutation(NP)
+    W = max((n + 15) // 16 for n in kv)
+    bt = np.full((B, W), -1, dtype=np.int32)
+    k = 0
+    for b, n in enumerate(kv):
+        for j in range((n + 15) // 16):
+            bt[b, j] = perm[k]
+            k += 1
+    q = rng.standard_normal((B, Hq, Sq, D))
+    pos = np.array([[n - Sq + s + conv[b] for s in range(Sq)] for b, n in enumerate(kv)], dtype=np.int32)
+    dout = rng.standard_normal((B, Hq, Sq, D))
+    return q, kc, vc, bt, np.array(kv, dtype=np.int32), pos, dout
+
+
+def _loss(q, kc, vc, bt, kv, pos, dout):
+    out, _ = oracle.attention(q, kc, vc, bt, kv, pos)
+    return float(np.sum(out * dout))
+
+
+def _referenced(bt, kv, NP):
+    """Mask [NP] of pages some row references."""
+    m = np.zeros(NP, bool)
+    for b, n in enumerate(kv):
+        for j in range((int(n) + 15) // 16):
+            m[bt[b, j]] = True
+    return m
+
+
+def test_backward_matches_central_differences():
+    q, kc, vc, bt, kv, pos, dout = _case(1)
+    dq, dk, dv = oracle.attention_backward(q, kc, vc, bt, kv, pos, dout)
+    h = 1e-5
+    rng = np.random.default_rng(2)
+    ref = _referenced(bt, kv, kc.shape[0])
+    # every element of dq; a random sample of the referenced cache entries
+    for idx in np.ndindex(q.shape):
+        e = np.zeros_like(q)
+        e[idx] = h
+        fd = (_loss(q + e, kc, vc, bt, kv, pos, dout) - _loss(q - e, kc, vc, bt, kv, pos, dout)) / (2 * h)
+        assert abs(fd - dq[idx]) <= 1e-6 * (1 + abs(fd)), idx
+    pages = np.nonzero(ref)[0]
+    for _ in range(120):
+        pg = int(rng.choice(pages))
+        idx = (pg, int(rng.integers(16)), int(rng.integers(kc.shape[2])), int(rng.integers(kc.shape[3])))
+        for cache, grad, name in ((kc, dk, "k"), (vc, dv, "v")):
+            e = np.zeros_like(cache)
+            e[idx] = h
+            args_p = (q, cache + e, vc, bt, kv, pos, dout) if name == "k" else (q, kc, cache + e, bt, kv, pos, dout)
+            args_m = (q, cache - e, vc, bt, kv, pos, dout) if name == "k" else (q, kc, cache - e, bt, kv, pos, dout)
+            fd = (_loss(*args_p) - _loss(*args_m)) / (2 * h)
+            assert abs(fd - grad[idx]) <= 1e-6 * (1 + abs(fd)), (name, idx)
+    # pages no row references are left untouched (NaN)
+    assert np.isnan(dk[~ref]).all() and np.isnan(dv[~ref]).all()
+    assert np.isfinite(dk[ref]).all() and np.isfinite(dv[ref]).all()
+
+
+def _torch_dense(q, K, V, kv, pos, Hkv, theta=THETA):
+    """Dense causal attention with rotate-half RoPE written with torch ops
+    (cos / sin tables, contiguous K/V [B, Hkv, T, D]); autodiff target."""
+    B, Hq, Sq, D = q.shape
+    G = Hq // Hkv
+    half = D // 2
+    inv = theta ** (-2.0 * torch.arange(half, dtype=torch.float64) / D)
+
+    def rot(x, p):  # x [..., D], p broadcastable positions
+        a = p[..., None] * inv
+        c, s = torch.cos(a), torch.sin(a)
+        lo, hi = x[..., :half], x[..., half:]
+        return torch.cat([lo * c - hi * s, hi * c + lo * s], dim=-1)
+
+    outs = []
+    for b in range(B):
+        n = int(kv[b])
+        t = torch.arange(n, dtype=torch.float64)
+        Kr = rot(K[b, :, :n], t)  # [Hkv, n, D]
+        qp = torch.as_tensor(pos[b], dtype=torch.float64)
+        Qr = rot(q[b], qp[None, :])  # [Hq, Sq, D]
+        sc = torch.einsum("hsd,htd->hst", Qr, Kr.repeat_interleave(G, dim=0)) / math.sqrt(D)
+        vis = torch.arange(n)[None, :] <= torch.as_tensor(pos[b])[:, None]
+        sc = sc.masked_fill(~vis[None], float("-inf"))
+        outs.append(torch.softmax(sc, dim=-1) @ V[b, :, :n].repeat_interleave(G, dim=0))
+    return torch.stack(outs)
+
+
+def test_backward_matches_dense_autodiff_with_gqa():
+    q, kc, vc, bt, kv, pos, dout = _case(3, D=16, Hq=8, Hkv=2, kv=(50, 33), Sq=5, NP=8)
+    dq, dk, dv = oracle.attention_backward(q, kc, vc, bt, kv, pos, dout)
+    B, Hq, Sq, D = q.shape
+    Hkv, T = kc.shape[2], max(kv)
+    # contiguous K / V gathered through the table, with their page slots
+    K = np.zeros((B, Hkv, T, D))
+    V = np.zeros((B, Hkv, T, D))
+    for b in range(B):
+        for t in range(kv[b]):
+            K[b, :, t] = kc[bt[b, t // 16], t % 16]
+            V[b, :, t] = vc[bt[b, t // 16], t % 16]
+    qt = torch.tensor(q, requires_grad=True)
+    Kt = torch.tensor(K, requires_grad=True)
+    Vt = torch.tensor(V, requires_grad=True)
+    out = _torch_dense(qt, Kt, Vt, kv, pos, Hkv)
+    (out * torch.tensor(dout)).sum().backward()
+    np.testing.assert_allclose(dq, qt.grad.numpy(), atol=1e-11)
+    for b in range(B):
+        for t in range(kv[b]):
+            np.testing.assert_allclose(dk[bt[b, t // 16], t % 16], Kt.grad[b, :, t].numpy(), atol=1e-11)
+            np.testing.assert_allclose(dv[bt[b, t // 16], t % 16], Vt.grad[b, :, t].numpy(), atol=1e-11)
+        last = bt[b, (kv[b] - 1) // 16]
+        assert (dk[last, (kv[b] - 1) % 16 + 1:] == 0).all()  # slots past kv_len
+
+
+def test_dv_sums_to_dout_and_rotated_dk_sums_to_zero():
+    """sum_t P_t = 1 gives sum over keys of dv = sum over the group's queries
+    of dout; sum_t dS_t = 0 gives sum over keys of R(t) dk_t = 0."""
+    q, kc, vc, bt, kv, pos, dout = _case(5, D=128, Hq=4, Hkv=2, kv=(45, 30), Sq=4, NP=6)
+    dq, dk, dv = oracle.attention_backward(q, kc, vc, bt, kv, pos, dout)
+    Hkv, G = kc.shape[2], q.shape[1] // kc.shape[2]
+    for b, n in enumerate(kv):
+        for kh in range(Hkv):
+            sv = sum(dv[bt[b, t // 16], t % 16, kh] for t in range(n))
+            sd = dout[b, kh * G:(kh + 1) * G].sum(axis=(0, 1))
+            np.testing.assert_allclose(sv, sd, atol=1e-11)
+            sk = sum(oracle.rope(dk[bt[b, t // 16], t % 16, kh], float(t)) for t in range(n))
+            np.testing.assert_allclose(sk, 0.0, atol=1e-10)
+
+
+def test_single_key_and_zero_dout():
+    rng = np.random.default_rng(7)
+    D, Hq, Hkv = 128, 2, 1
+    kc = rng.standard_normal((2, 16, Hkv, D))
+    vc = rng.standard_normal((2, 16, Hkv, D))
+    bt = np.array([[1]], dtype=np.int32)
+    kv = np.array([1], dtype=np.int32)
+    q = rng.standard_normal((1, Hq, 1, D))
+    pos = np.array([[0]], dtype=np.int32)
+    dout = rng.standard_normal((1, Hq, 1, D))
+    dq, dk, dv = oracle.attention_backward(q, kc, vc, bt, kv, pos, dout)
+    # out = v_0 whatever q and k are: dv_0 = sum of the heads' dout, no q / k gradient
+    np.testing.assert_allclose(dv[1, 0, 0], dout[0, :, 0].sum(axis=0), atol=1e-14)
+    assert np.abs(dq).max() == 0.0 and np.abs(dk[1]).max() == 0.0
+    assert (dv[1, 1:] == 0).all()
+    z = oracle.attention_backward(q, kc, vc, bt, kv, pos, np.zeros_like(dout))
+    assert all(np.nan_to_num(g).max() == 0.0 and np.nan_to_num(g).min() == 0.0 for g in z)
+
+
+def test_magnitudes_bound_the_values():
+    q, kc, vc, bt, kv, pos, dout = _case(9, D=128)
+    dq, dk, dv, (mq, mk, mv) = oracle.attention_backward(q, kc, vc, bt, kv, pos, dout, magnitudes=True)
+    ref = _referenced(bt, kv, kc.shape[0])
+    assert (np.abs(dq) <= mq + 1e-12).all()
+    assert (np.abs(dk[ref]) <= mk[ref] + 1e-12).all() and (np.abs(dv[ref]) <= mv[ref] + 1e-12).all()
+    assert mq.max() > 0 and mk[ref].max() > 0 and mv[ref].max() > 0
+
+
+def test_backward_page_permutation_moves_gradients_with_pages():
+    q, kc, vc, bt, kv, pos, dout = _case(11, D=32)
+    dq, dk, dv = oracle.attention_backward(q, kc, vc, bt, kv, pos, dout)
+    NP = kc.shape[0]
+    perm = np.random.default_rng(12).permutation(NP)  # new page id of old page i
+    kc2 = np.empty_like(kc)
+    vc2 = np.empty_like(vc)
+    kc2[perm] = kc
+    vc2[perm] = vc
+    bt2 = np.where(bt >= 0, perm[np.maximum(bt, 0)], -1).astype(np.int32)
+    dq2, dk2, dv2 = oracle.attention_backward(q, kc2, vc2, bt2, kv, pos, dout)
+    assert np.array_equal(dq, dq2)
+    assert np.array_equal(dk2[perm], dk, equal_nan=True) and np.array_equal(dv2[perm], dv, equal_nan=True)
