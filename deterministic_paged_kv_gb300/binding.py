@@ -95,6 +95,8 @@ def load(path: str | None = None):
             [i32p, i32p, i32p, i32p, ctypes.c_double, ctypes.c_double, ctypes.POINTER(ctypes.c_int32)]
         lib.rk_paged_attn_ragged.restype = ctypes.c_int
         lib.rk_paged_attn_ragged.argtypes = [ctypes.POINTER(Plan), ctypes.c_int32] + [vp] * 11
+        lib.rk_paged_attn_prefill_backward.restype = ctypes.c_int
+        lib.rk_paged_attn_prefill_backward.argtypes = [ctypes.POINTER(Plan)] + [vp] * 15
         lib.rk_last_error.restype = ctypes.c_char_p
         lib.rk_last_error.argtypes = []
         lib.rk_paged_policy.restype = ctypes.c_char_p
@@ -201,6 +203,30 @@ def attn_prefill(p: Plan, q, k_cache, v_cache, block_table, kv_lens, position_id
     """rk_paged_attn_prefill on device tensors; asynchronous on ``stream``."""
     _launch(load().rk_paged_attn_prefill, p, q, k_cache, v_cache, block_table, kv_lens,
             position_ids, out, lse, status, stream)
+
+
+def attn_prefill_backward(p: Plan, q, k_cache, v_cache, block_table, kv_lens, position_ids, out, lse, dout,
+                          dq, dk_cache, dv_cache, delta, status=None, stream=None):
+    """rk_paged_attn_prefill_backward on device tensors: dq [B, Hq, Sq, D],
+    dk_cache / dv_cache [num_pages, 16, Hkv, D] and delta [B, Hq, Sq], all
+    float32; asynchronous on ``stream``."""
+    import torch
+    for t, dt, name in ((q, torch.bfloat16, "q"), (k_cache, torch.bfloat16, "k_cache"),
+                        (v_cache, torch.bfloat16, "v_cache"), (out, torch.bfloat16, "out"),
+                        (lse, torch.float32, "lse"), (dout, torch.bfloat16, "dout"),
+                        (dq, torch.float32, "dq"), (dk_cache, torch.float32, "dk_cache"),
+                        (dv_cache, torch.float32, "dv_cache"), (delta, torch.float32, "delta"),
+                        (block_table, torch.int32, "block_table"), (kv_lens, torch.int32, "kv_lens"),
+                        (position_ids, torch.int32, "position_ids")):
+        if t.dtype != dt:
+            raise TypeError("%s must be %s (got %s)" % (name, dt, t.dtype))
+    if status is not None and status.dtype != torch.int32:
+        raise TypeError("status must be int32")
+    rc = load().rk_paged_attn_prefill_backward(
+        ctypes.byref(p), _dptr(q), _dptr(k_cache), _dptr(v_cache), _dptr(block_table), _dptr(kv_lens),
+        _dptr(position_ids), _dptr(out), _dptr(lse), _dptr(dout), _dptr(dq), _dptr(dk_cache), _dptr(dv_cache),
+        _dptr(delta), _dptr(status), _stream(stream))
+    _check(rc)
 
 
 def decode_split_scratch_bytes(p: Plan, split_tokens: int) -> int:

@@ -24,6 +24,7 @@ cudaError_t launch_decode(const CUtensorMap& km, const CUtensorMap& vm, const De
 cudaError_t launch_prefill(const CUtensorMap& qm, const CUtensorMap& km, const CUtensorMap& vm,
                            const PrefillArgs& a, cudaStream_t stream, bool overlap_previous = false);
 cudaError_t launch_kv_append(const AppendArgs& a, cudaStream_t stream);
+cudaError_t launch_backward(const BackwardArgs& a, cudaStream_t stream);
 }  // namespace rk
 
 namespace {
@@ -593,6 +594,53 @@ int rk_paged_attn_prefill(const rk_paged_plan_t* plan, const void* q, const void
     std::memcpy(a.rope_turns, plan->rope_turns, sizeof a.rope_turns);
     cudaError_t e = rk::launch_prefill(qm, km, vm, a, reinterpret_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return fail(RK_E_CUDA, "prefill launch: %s", cudaGetErrorString(e));
+    return RK_OK;
+}
+
+int rk_paged_attn_prefill_backward(const rk_paged_plan_t* plan, const void* q, const void* k_cache,
+                                   const void* v_cache, const int32_t* block_table_d, const int32_t* kv_lens_d,
+                                   const int32_t* position_ids_d, const void* out, const float* lse,
+                                   const void* dout, float* dq, float* dk_cache, float* dv_cache, float* delta,
+                                   int32_t* status_d, rk_stream_t stream) {
+    g_err.clear();
+    int rc = check_launch_common(plan, q, k_cache, v_cache, block_table_d, kv_lens_d, position_ids_d, out, lse);
+    if (rc) return rc;
+    if (plan->B == 0) return RK_OK;
+    if (!dout || !dq || !delta) return fail(RK_E_ARG, "dout, dq and delta must be non-null device pointers");
+    if (plan->num_pages > 0 && (!dk_cache || !dv_cache)) return fail(RK_E_ARG, "dk_cache / dv_cache is NULL");
+    if (!aligned(dout, 16) || !aligned(dq, 16) || (dk_cache && !aligned(dk_cache, 16)) ||
+        (dv_cache && !aligned(dv_cache, 16)) || !aligned(delta, 4))
+        return fail(RK_E_ARG, "dout, dq, dk_cache and dv_cache must be 16-byte aligned, delta 4-byte aligned");
+    rk::BackwardArgs a;
+    std::memset(&a, 0, sizeof a);
+    a.q = q;
+    a.k_cache = k_cache;
+    a.v_cache = v_cache;
+    a.block_table = block_table_d;
+    a.kv_lens = kv_lens_d;
+    a.position_ids = position_ids_d;
+    a.out = out;
+    a.lse = lse;
+    a.dout = dout;
+    a.dq = dq;
+    a.dk = dk_cache;
+    a.dv = dv_cache;
+    a.delta = delta;
+    a.status = status_d;
+    a.B = plan->B;
+    a.Sq = plan->Sq;
+    a.Hq = plan->Hq;
+    a.Hkv = plan->Hkv;
+    a.G = plan->Hq / plan->Hkv;
+    a.W = plan->W;
+    a.num_pages = plan->num_pages;
+    // key tiles of the widest row the table allows (tiles past a row's pages exit at once)
+    a.n_key_tiles = (int32_t)(((int64_t)plan->W * rk::PAGE + rk::BW_KT - 1) / rk::BW_KT);
+    a.sm_scale = (float)(1.0 / std::sqrt((double)plan->D));
+    a.qk_scale_log2 = (float)((1.0 / std::sqrt((double)plan->D)) * 1.4426950408889634074);
+    std::memcpy(a.rope_turns, plan->rope_turns, sizeof a.rope_turns);
+    cudaError_t e = rk::launch_backward(a, reinterpret_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return fail(RK_E_CUDA, "backward launch: %s", cudaGetErrorString(e));
     return RK_OK;
 }
 

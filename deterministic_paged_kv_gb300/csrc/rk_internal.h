@@ -88,6 +88,37 @@ struct PrefillArgs {
 // per-CTA scan keeps 2 x levels + 1 counters in a K stage buffer).
 constexpr int PF_RAGGED_MAX_LEVELS = 12000;
 
+// ---------------------------------------------------------- backward ----
+// Gradient of causal paged prefill (padded layout, q / out / dout
+// [B, Hq, Sq, D] bf16, lse [B, Hq, Sq] fp32): dq [B, Hq, Sq, D] fp32, dk / dv
+// in the cache layout [num_pages, 16, Hkv, D] fp32, delta [B, Hq, Sq] fp32
+// (rowsum(dout * out); written by the dq launch, read by the dk/dv launch).
+struct BackwardArgs {
+    const void* q;
+    const void* k_cache;
+    const void* v_cache;
+    const int32_t* block_table;   // [B, W]
+    const int32_t* kv_lens;       // [B]
+    const int32_t* position_ids;  // [B, Sq]
+    const void* out;
+    const float* lse;
+    const void* dout;
+    float* dq;
+    float* dk;
+    float* dv;
+    float* delta;
+    int32_t* status;
+    int32_t B, Sq, Hq, Hkv, G, W, num_pages;
+    int32_t n_key_tiles;          // key tiles of BW_KT tokens covering the longest row (dk/dv grid)
+    float sm_scale;
+    float qk_scale_log2;          // sm_scale * log2(e)
+    uint64_t rope_turns[ROPE_PAIRS];
+};
+constexpr int BW_THREADS = 128;  // 4 warps, 16 accumulator rows each
+constexpr int BW_KT = 64;        // keys per dk/dv CTA and per key tile of the dq kernel
+constexpr int BW_QB = 64;        // query rows (position x head) per dq CTA
+constexpr int BW_QB_KV = 32;     // query rows per step of the dk/dv kernel
+
 // ------------------------------------------------------------ append ----
 // Write n_new tokens per row into the page cache (kv_lens after the append).
 struct AppendArgs {

@@ -319,6 +319,44 @@ int rk_paged_attn_ragged(const rk_paged_plan_t *plan, int32_t max_q_len, const i
                          const int32_t *position_ids_d, void *out, float *lse, int32_t *status_d,
                          rk_stream_t stream);
 
+/*
+ * rk_paged_attn_prefill_backward -- deterministic gradient of
+ * rk_paged_attn_prefill ("Add FlashInfer RoPE-fused paged attention
+ * scaffold", scope table, Backward row: dropout 0, deterministic backward
+ * required).  For L = sum(dout * out) it writes dL/dq and dL/d(k_cache),
+ * dL/d(v_cache) (gradients of the pre-RoPE inputs; RoPE is applied to q and
+ * K on the fly and undone by its transpose on dq and dk).
+ *   plan, q, k_cache, v_cache, block_table_d, kv_lens_d, position_ids_d:
+ *                 as for rk_paged_attn_prefill (same validation).
+ *   out, lse      DEVICE bf16 [B, Hq, Sq, D] / fp32 [B, Hq, Sq]: that call's
+ *                 results (P = exp(score - lse) is recomputed from them).
+ *   dout          DEVICE bf16 [B, Hq, Sq, D], 16-byte aligned.
+ *   dq            DEVICE fp32 [B, Hq, Sq, D], 16-byte aligned (written).
+ *   dk_cache, dv_cache
+ *                 DEVICE fp32 [num_pages, 16, Hkv, D], 16-byte aligned: for
+ *                 every row the pages of its first ceil(kv_len / 16) table
+ *                 entries are written in full (0 at slots past kv_len); no
+ *                 other entry is touched.  Rows sharing a page (rejected by
+ *                 rk_paged_plan) give unspecified values on it.
+ *   delta         DEVICE fp32 [B, Hq, Sq], 4-byte aligned: caller-owned
+ *                 workspace, left holding rowsum(dout * out).
+ * Deterministic and batch-invariant: every output element is accumulated by
+ * one CTA in a fixed order (dq over key tiles ascending, dk / dv over query
+ * blocks ascending), no atomics.  Arithmetic: FP32 accumulation on the
+ * tensor cores; rotated q / k and dS rounded to FP16, P to BF16 for the dV
+ * product.  Two launches on `stream` (dq with delta, then dk / dv), no
+ * allocation, no host synchronisation.  Device status bits as the forward;
+ * rows whose rotated operands or dS leave the FP16 range get NaN gradients
+ * and RK_STATUS_RANGE.  Errors: as rk_paged_attn_prefill, plus RK_E_ARG for
+ * a null or misaligned dout / dq / dk_cache / dv_cache / delta.
+ */
+int rk_paged_attn_prefill_backward(const rk_paged_plan_t *plan, const void *q, const void *k_cache,
+                                   const void *v_cache, const int32_t *block_table_d,
+                                   const int32_t *kv_lens_d, const int32_t *position_ids_d,
+                                   const void *out, const float *lse, const void *dout, float *dq,
+                                   float *dk_cache, float *dv_cache, float *delta, int32_t *status_d,
+                                   rk_stream_t stream);
+
 /* Message of the last failing call on this thread ("" if none).  The
  * pointer stays valid until the next library call on the same thread. */
 const char *rk_last_error(void);

@@ -82,7 +82,7 @@ def _load():
             + [ctypes.c_void_p] * 3
             + [ctypes.c_int, ctypes.c_void_p, ctypes.c_int, i32p, i32p, i32p,
                ctypes.c_double, ctypes.c_double, ctypes.c_double]
-            + [ctypes.c_void_p] * 6 + [ctypes.c_int])
+            + [ctypes.c_void_p] * 8 + [ctypes.c_int])
         lib.rk_oracle_max_threads.restype = ctypes.c_int
         lib.rk_oracle_max_threads.argtypes = []
         _lib = lib
@@ -214,9 +214,11 @@ def attention_backward(q, k_cache, v_cache, block_table, kv_lens, position_ids, 
     Returns ``(dq [B,Hq,Sq,D], dk, dv)`` with dk / dv in the cache layout
     [num_pages, page_size, Hkv, D]: the pages a row references are written in
     full (0 at slots past kv_len), every other entry is NaN.  With
-    ``magnitudes`` also returns ``(mag_dq, mag_dk, mag_dv)``: per element the
-    sum of the absolute values of its terms.  ``dout`` is [B, Hq, Sq, D],
-    float or bfloat16 bits; q / caches as in ``attention``.
+    ``magnitudes`` also returns ``(mag_dq, mag_dk, mag_dv, sens_dq, sens_dk)``:
+    per element the sum of the absolute values of its terms, and of its terms'
+    dependence on Dq = dout . out scaled by sum_d |dout_d out_d| (how far a
+    relative change of out moves it).  ``dout`` is [B, Hq, Sq, D], float or
+    bfloat16 bits; q / caches as in ``attention``.
     """
     lib = _load()
     qa, qcode = _qkv(q)
@@ -239,14 +241,15 @@ def attention_backward(q, k_cache, v_cache, block_table, kv_lens, position_ids, 
     dq = np.full((B, Hq, Sq, D), np.nan, dtype=np.float64)
     dk = np.full((NP, P, Hkv, D), np.nan, dtype=np.float64)
     dv = np.full((NP, P, Hkv, D), np.nan, dtype=np.float64)
-    mags = [np.full_like(dq, np.nan), np.full_like(dk, np.nan), np.full_like(dv, np.nan)] if magnitudes else None
-    mp = [m.ctypes.data for m in mags] if mags else [None, None, None]
+    mags = ([np.full_like(dq, np.nan), np.full_like(dk, np.nan), np.full_like(dv, np.nan),
+             np.full_like(dq, np.nan), np.full_like(dk, np.nan)] if magnitudes else None)
+    mp = [m.ctypes.data for m in mags] if mags else [None] * 5
     rc = lib.rk_oracle_attention_backward(B, Sq, Hq, Hkv, D, P, NP, bt.shape[1],
                                           qa.ctypes.data, ka.ctypes.data, va.ctypes.data, qcode,
                                           ga.ctypes.data, gcode, _ptr_i32(bt), _ptr_i32(kl), _ptr_i32(pos),
                                           float(rope_theta), float(rope_scale), float(sm_scale),
                                           dq.ctypes.data, dk.ctypes.data, dv.ctypes.data,
-                                          mp[0], mp[1], mp[2], int(threads or 0))
+                                          mp[0], mp[1], mp[2], mp[3], mp[4], int(threads or 0))
     if rc != 0:
         raise ValueError("oracle attention_backward failed with code %d" % rc)
     if magnitudes:

@@ -286,6 +286,10 @@ int rk_oracle_attention(int B, int Sq, int Hq, int Hkv, int D, int page_size,
  * layouts) receive the sums of the absolute values of the terms of each
  * output element (after the rotation: |R^T x|_i <= |x_i| + |x_(i +- D/2)|),
  * from which rounding-error bounds of other implementations are derived.
+ * sens_dq / sens_dk (optional) receive, per element, the sum of the absolute
+ * values of its terms' dependence on Dq scaled by A = sum_d |dout_d out_d|
+ * (the bound on a relative change of every out element entering Dq):
+ * sum_t sm_scale P_t |k'_t| A for dq', sum_q sm_scale P_t |q'| A for dk'.
  * Work is split over (b, KV head): each unit owns its keys' dk / dv.
  */
 int rk_oracle_attention_backward(int B, int Sq, int Hq, int Hkv, int D, int page_size,
@@ -295,7 +299,8 @@ int rk_oracle_attention_backward(int B, int Sq, int Hq, int Hkv, int D, int page
                                  const int32_t *kv_lens, const int32_t *position_ids,
                                  double rope_theta, double rope_scale, double sm_scale,
                                  double *dq, double *dk, double *dv, double *mag_dq,
-                                 double *mag_dk, double *mag_dv, int nthreads) {
+                                 double *mag_dk, double *mag_dv, double *sens_dq,
+                                 double *sens_dk, int nthreads) {
     if (B < 0 || Sq < 0 || Hq <= 0 || Hkv <= 0 || D <= 0 || (D % 2) ||
         page_size <= 0 || W < 0 || Hq % Hkv)
         return ORACLE_E_ARG;
@@ -323,6 +328,7 @@ int rk_oracle_attention_backward(int B, int Sq, int Hq, int Hkv, int D, int page
         double *gv = (double *)calloc(nd, sizeof(double));
         double *mk = (double *)calloc(nd, sizeof(double));    /* magnitudes of dk' terms */
         double *mv = (double *)calloc(nd, sizeof(double));
+        double *sk = (double *)calloc(nd, sizeof(double));    /* Dq sensitivity of dk' */
         double *pr = (double *)malloc(sizeof(double) * ((size_t)n + 1));
         double *ds = (double *)malloc(sizeof(double) * ((size_t)n + 1));
         double *tmp = (double *)malloc(sizeof(double) * (size_t)D);
@@ -331,9 +337,11 @@ int rk_oracle_attention_backward(int B, int Sq, int Hq, int Hkv, int D, int page
         double *ov = (double *)malloc(sizeof(double) * (size_t)D);
         double *gq = (double *)malloc(sizeof(double) * (size_t)D);
         double *mq = (double *)malloc(sizeof(double) * (size_t)D);
-        if (!kr || !vr || !gk || !gv || !mk || !mv || !pr || !ds || !tmp || !qr || !go || !ov || !gq || !mq) {
-            free(kr); free(vr); free(gk); free(gv); free(mk); free(mv); free(pr); free(ds);
-            free(tmp); free(qr); free(go); free(ov); free(gq); free(mq);
+        double *sq = (double *)malloc(sizeof(double) * (size_t)D);
+        if (!kr || !vr || !gk || !gv || !mk || !mv || !sk || !pr || !ds || !tmp || !qr || !go || !ov || !gq ||
+            !mq || !sq) {
+            free(kr); free(vr); free(gk); free(gv); free(mk); free(mv); free(sk); free(pr); free(ds);
+            free(tmp); free(qr); free(go); free(ov); free(gq); free(mq); free(sq);
 #ifdef _OPENMP
 #pragma omp atomic write
 #endif
@@ -361,6 +369,7 @@ int rk_oracle_attention_backward(int B, int Sq, int Hq, int Hkv, int D, int page
                     for (int d = 0; d < D; ++d) {
                         dq[qoff + d] = 0.0;
                         if (mag_dq) mag_dq[qoff + d] = 0.0;
+                        if (sens_dq) sens_dq[qoff + d] = 0.0;
                     }
                     continue;
                 }
@@ -387,8 +396,11 @@ int rk_oracle_attention_backward(int B, int Sq, int Hq, int Hkv, int D, int page
                     const double *vt = vr + (int64_t)t * D;
                     for (int d = 0; d < D; ++d) ov[d] += pr[t] * vt[d];
                 }
-                double Dq = 0.0;
-                for (int d = 0; d < D; ++d) Dq += go[d] * ov[d];
+                double Dq = 0.0, A = 0.0;
+                for (int d = 0; d < D; ++d) {
+                    Dq += go[d] * ov[d];
+                    A += fabs(go[d] * ov[d]);
+                }
                 /* softmax gradient */
                 for (int t = 0; t < nv; ++t) {
                     double dp = 0.0;
@@ -397,17 +409,20 @@ int rk_oracle_attention_backward(int B, int Sq, int Hq, int Hkv, int D, int page
                     ds[t] = pr[t] * (dp - Dq);
                 }
                 /* dq' and its magnitudes; dk', dv accumulate over queries */
-                for (int d = 0; d < D; ++d) { gq[d] = 0.0; mq[d] = 0.0; }
+                for (int d = 0; d < D; ++d) { gq[d] = 0.0; mq[d] = 0.0; sq[d] = 0.0; }
                 for (int t = 0; t < nv; ++t) {
                     const double *kt = kr + (int64_t)t * D;
                     double *gkt = gk + (int64_t)t * D, *gvt = gv + (int64_t)t * D;
                     double *mkt = mk + (int64_t)t * D, *mvt = mv + (int64_t)t * D;
-                    const double w = sm_scale * ds[t], aw = fabs(w);
+                    double *skt = sk + (int64_t)t * D;
+                    const double w = sm_scale * ds[t], aw = fabs(w), ws = sm_scale * pr[t] * A;
                     for (int d = 0; d < D; ++d) {
                         gq[d] += w * kt[d];
                         mq[d] += aw * fabs(kt[d]);
+                        sq[d] += ws * fabs(kt[d]);
                         gkt[d] += w * qr[d];
                         mkt[d] += aw * fabs(qr[d]);
+                        skt[d] += ws * fabs(qr[d]);
                         gvt[d] += pr[t] * go[d];
                         mvt[d] += pr[t] * fabs(go[d]);
                     }
@@ -415,12 +430,11 @@ int rk_oracle_attention_backward(int B, int Sq, int Hq, int Hkv, int D, int page
                 /* back to the pre-rotation domain: dq = R(p)^T dq' */
                 for (int d = 0; d < D; ++d) tmp[d] = gq[d];
                 rk_oracle_rope(tmp, D, -(double)p, rope_theta, rope_scale, dq + qoff);
-                if (mag_dq)
-                    for (int i = 0; i < half; ++i) {
-                        const double a = mq[i] + mq[i + half];
-                        mag_dq[qoff + i] = a;
-                        mag_dq[qoff + i + half] = a;
-                    }
+                for (int i = 0; i < half; ++i) {
+                    const double a = mq[i] + mq[i + half], c = sq[i] + sq[i + half];
+                    if (mag_dq) { mag_dq[qoff + i] = a; mag_dq[qoff + i + half] = a; }
+                    if (sens_dq) { sens_dq[qoff + i] = c; sens_dq[qoff + i + half] = c; }
+                }
             }
         }
         if (!bad) {
@@ -434,7 +448,9 @@ int rk_oracle_attention_backward(int B, int Sq, int Hq, int Hkv, int D, int page
                     for (int d = 0; d < D; ++d) dv[dst + d] = gv[(int64_t)t * D + d];
                     for (int i = 0; i < half; ++i) {
                         const double a = mk[(int64_t)t * D + i] + mk[(int64_t)t * D + i + half];
+                        const double c = sk[(int64_t)t * D + i] + sk[(int64_t)t * D + i + half];
                         if (mag_dk) { mag_dk[dst + i] = a; mag_dk[dst + i + half] = a; }
+                        if (sens_dk) { sens_dk[dst + i] = c; sens_dk[dst + i + half] = c; }
                     }
                     if (mag_dv)
                         for (int d = 0; d < D; ++d) mag_dv[dst + d] = mv[(int64_t)t * D + d];
@@ -444,12 +460,13 @@ int rk_oracle_attention_backward(int B, int Sq, int Hq, int Hkv, int D, int page
                         dv[dst + d] = 0.0;
                         if (mag_dk) mag_dk[dst + d] = 0.0;
                         if (mag_dv) mag_dv[dst + d] = 0.0;
+                        if (sens_dk) sens_dk[dst + d] = 0.0;
                     }
                 }
             }
         }
-        free(kr); free(vr); free(gk); free(gv); free(mk); free(mv); free(pr); free(ds);
-        free(tmp); free(qr); free(go); free(ov); free(gq); free(mq);
+        free(kr); free(vr); free(gk); free(gv); free(mk); free(mv); free(sk); free(pr); free(ds);
+        free(tmp); free(qr); free(go); free(ov); free(gq); free(mq); free(sq);
         if (bad) {
 #ifdef _OPENMP
 #pragma omp atomic write

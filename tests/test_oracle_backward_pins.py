@@ -175,11 +175,29 @@ def test_single_key_and_zero_dout():
 
 def test_magnitudes_bound_the_values():
     q, kc, vc, bt, kv, pos, dout = _case(9, D=128)
-    dq, dk, dv, (mq, mk, mv) = oracle.attention_backward(q, kc, vc, bt, kv, pos, dout, magnitudes=True)
+    dq, dk, dv, (mq, mk, mv, sq, sk) = oracle.attention_backward(q, kc, vc, bt, kv, pos, dout, magnitudes=True)
     ref = _referenced(bt, kv, kc.shape[0])
     assert (np.abs(dq) <= mq + 1e-12).all()
     assert (np.abs(dk[ref]) <= mk[ref] + 1e-12).all() and (np.abs(dv[ref]) <= mv[ref] + 1e-12).all()
     assert mq.max() > 0 and mk[ref].max() > 0 and mv[ref].max() > 0
+    # Dq sensitivity of dq, restated for one query from its definition with numpy:
+    # sum over visible keys of sm_scale * P_t * |k'_t| * sum_d |dout_d out_d|, rotation-combined
+    b, h, s_ = 1, 3, 2
+    G = q.shape[1] // kc.shape[2]
+    p = int(pos[b, s_])
+    n = min(p + 1, int(kv[b]))
+    kr = np.array([oracle.rope(kc[bt[b, t // 16], t % 16, h // G], float(t)) for t in range(n)])
+    qr = oracle.rope(q[b, h, s_], float(p))
+    sc = kr @ qr / math.sqrt(q.shape[3])
+    P = np.exp(sc - sc.max())
+    P /= P.sum()
+    out = P @ np.array([vc[bt[b, t // 16], t % 16, h // G] for t in range(n)])
+    A = np.sum(np.abs(dout[b, h, s_] * out))
+    raw = (P[:, None] * np.abs(kr)).sum(axis=0) * A / math.sqrt(q.shape[3])
+    half = q.shape[3] // 2
+    want = np.concatenate([raw[:half] + raw[half:], raw[:half] + raw[half:]])
+    np.testing.assert_allclose(sq[b, h, s_], want, rtol=1e-12)
+    assert (sq >= 0).all() and (sk[ref] >= 0).all() and sq.max() > 0
 
 
 def test_backward_page_permutation_moves_gradients_with_pages():
