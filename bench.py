@@ -276,6 +276,55 @@ def measure_prefill(args, dev, stream, world, tf_burst, peak_kind):
     return prefill
 
 
+def measure_backward(args, dev, stream, tf_burst, peak_kind):
+    """Time rk_paged_attn_prefill_backward on the long full-causal prefill
+    (B=1, S=8192; forward run once before timing for out / lse; L2 flushed
+    between launches).  Algorithmic FLOPs: the five products of the attention
+    gradient (scores, dP, dV, dK, dQ) over the causal-visible pairs,
+    10 * D * pairs * Hq = 2.5 x the forward's."""
+    import torch
+
+    from deterministic_paged_kv_gb300 import binding, workloads
+    names = ("q", "k_cache", "v_cache", "block_table", "kv_lens", "position_ids")
+    w = workloads.prefill_long()
+    d = {k: getattr(w, k).to(dev) for k in names}
+    p = binding.plan(w.B, w.Sq, w.Hq, w.Hkv, w.D, 16, w.num_pages, w.W, w.block_table, w.kv_lens,
+                     w.position_ids, w.rope_theta, w.rope_scale)
+    out = torch.empty_like(d["q"])
+    lse = torch.empty((w.B, w.Hq, w.Sq), dtype=torch.float32, device=dev)
+    binding.attn_prefill(p, d["q"], d["k_cache"], d["v_cache"], d["block_table"], d["kv_lens"],
+                         d["position_ids"], out, lse, stream=stream)
+    g = torch.Generator().manual_seed(1099)
+    dout = torch.randn(w.q.shape, generator=g).to(torch.bfloat16).to(dev)
+    dq = torch.empty(w.q.shape, dtype=torch.float32, device=dev)
+    dk = torch.empty(w.k_cache.shape, dtype=torch.float32, device=dev)
+    dv = torch.empty(w.v_cache.shape, dtype=torch.float32, device=dev)
+    delta = torch.empty((w.B, w.Hq, w.Sq), dtype=torch.float32, device=dev)
+
+    def step():
+        binding.attn_prefill_backward(p, d["q"], d["k_cache"], d["v_cache"], d["block_table"], d["kv_lens"],
+                                      d["position_ids"], out, lse, dout, dq, dk, dv, delta, stream=stream)
+
+    for _ in range(3):
+        step()
+    torch.cuda.synchronize()
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    t = time_launches(step, max(5, min(args.steps, 10)), stream, flush=flush)
+    ms = sum(t) / len(t)
+    flops = 2.5 * prefill_alg_flops(w)
+    achieved = flops / (ms * 1e-3) / 1e12
+    return {"metric": "paged prefill backward TFLOP/s", "value": achieved, "unit": "TFLOP/s",
+            "ms_per_launch": ms, "launches": len(t),
+            "config": {"workload": w.name + " page=16, backward (dq, dk, dv)",
+                       "l2": "flushed (256 MB write) between launches",
+                       "flops": "10*D*visible_pairs*Hq = %.4g" % flops},
+            "roofline": {"bound": "tensor", "achieved": achieved, "peak": tf_burst, "unit": "TFLOP/s",
+                         "frac": achieved / tf_burst, "traffic": None,
+                         "kernel": "attn_bwd_dq_kernel + attn_bwd_dkdv_kernel (mma.sync)",
+                         "peak_kind": peak_kind + " (bf16 dense, burst)"},
+            "note": "two launches per call (dq with delta, then dk/dv); deterministic, no atomics"}
+
+
 def measure_decode_long(args, dev, stream, hbm, peak_kind, split_tokens=2048):
     """Time decode_long (B=1, kv 32768: 8 CTAs without splitting) through the
     split-free entry point and the fixed-split entry point; L2 flushed between
@@ -413,6 +462,11 @@ def run_ours(args):
 
     hbm, tf_burst, tf_sust, peak_kind = peaks()
     names = ("q", "k_cache", "v_cache", "block_table", "kv_lens", "position_ids")
+    if args.backward_only:
+        bw = measure_backward(args, dev, stream, tf_burst, peak_kind)
+        if rank == 0:
+            print(json.dumps(bw))
+        return 0
     if args.prefill_only:
         pf = measure_prefill(args, dev, stream, world, tf_burst, peak_kind)
         if rank == 0:
@@ -495,6 +549,7 @@ def run_ours(args):
     dlong = None if args.no_long else measure_decode_long(args, dev, stream, hbm, peak_kind)
     append = None if args.no_long else measure_append(args, dev, stream, hbm, peak_kind)
     ragged = None if args.no_long else measure_ragged(args, dev, stream)
+    backward = None if args.no_long else measure_backward(args, dev, stream, tf_burst, peak_kind)
 
     clk.__exit__(None, None, None)
     cpu = None
@@ -526,6 +581,7 @@ def run_ours(args):
             "decode_long": dlong,
             "kv_append": append,
             "ragged_step": ragged,
+            "prefill_backward": backward,
         }
         if args.no_e2e:
             line["e2e"] = line["e2e_resident_cache"] = None
@@ -548,6 +604,8 @@ def main():
                     help="skip the decode_long (split-free vs fixed-split decode), kv_append and ragged_step objects")
     ap.add_argument("--no-prefill", action="store_true",
                     help="skip the prefill object (profiling runs of the decode kernel)")
+    ap.add_argument("--backward-only", action="store_true",
+                    help="time only the prefill backward on the long full-causal workload")
     ap.add_argument("--prefill-only", action="store_true",
                     help="time only the prefill workload and print its object (profiling runs)")
     args = ap.parse_args()

@@ -83,6 +83,7 @@ def referenced_pages(w):
 
 CASES = {
     "full_prefill_200": dict(B=1, Sq=200, kv=[200], Hq=32, Hkv=8),
+    "full_prefill_1000": dict(B=1, Sq=1000, kv=[1000], Hq=32, Hkv=8),
     "chunks_300_170": dict(B=2, Sq=70, kv=[300, 170], Hq=32, Hkv=8),
     "mha_G1": dict(B=2, Sq=40, kv=[150, 77], Hq=8, Hkv=8),
     "gqa_G8": dict(B=2, Sq=40, kv=[150, 77], Hq=64, Hkv=8),
