@@ -119,6 +119,83 @@ __device__ __forceinline__ void load_plain(uint8_t* dst, int rows, Src src) {
     }
 }
 
+// Asynchronous 16-byte global -> shared copy (zero fill when !valid: nothing is read).
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, bool valid) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(valid ? 16 : 0)
+                 : "memory");
+}
+__device__ __forceinline__ void cp_async4(uint32_t dst, const void* src, bool valid) {
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(dst), "l"(src), "r"(valid ? 4 : 0) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_group 0;" ::: "memory"); }
+
+// Start copying rows of 128 bf16 into swizzled rows: row r from src(r)
+// (nullptr: zeros).  Completion: cp_async_wait_all by the issuing threads,
+// then a barrier.
+template <class Src>
+__device__ __forceinline__ void copy_rows_async(uint32_t dst, int rows, Src src, const void* any_valid) {
+    for (int it = threadIdx.x; it < rows * 16; it += BW_THREADS) {
+        const int r = it >> 4, c = it & 15;
+        const uint4* p = src(r);
+        cp_async16(dst + swz(r, c), p ? static_cast<const void*>(p + c) : any_valid, p != nullptr);
+    }
+}
+
+// Rotate in place 64 swizzled bf16 rows at positions t0 + r into FP16: thread
+// handles chunk pair c = tid & 7 of rows r0 + 16 m (r0 = tid >> 3), with exact
+// angles at r0 and 16-position angle-addition steps (step16) after it.
+static_assert(BW_THREADS == 128 && BW_KT == 64, "rotate_tile_inplace: 16 row groups of 8 chunk pairs, 4 rows each");
+__device__ __forceinline__ uint32_t rotate_tile_inplace(uint8_t* buf, int t0, const uint64_t* turns,
+                                                        const float2* step16, uint32_t range) {
+    const int c = threadIdx.x & 7, r0 = threadIdx.x >> 3;
+    float2 cs[4], sn[4], dcs[4], dsn[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+        rope_cos_sin((uint32_t)(t0 + r0), turns[8 * c + 2 * e], cs[e].x, sn[e].x);
+        rope_cos_sin((uint32_t)(t0 + r0), turns[8 * c + 2 * e + 1], cs[e].y, sn[e].y);
+        const float2 a = step16[8 * c + 2 * e], b = step16[8 * c + 2 * e + 1];
+        dcs[e] = make_float2(a.x, b.x);
+        dsn[e] = make_float2(a.y, b.y);
+    }
+#pragma unroll
+    for (int m = 0; m < BW_KT / 16; ++m) {
+        const int r = r0 + 16 * m;
+        uint4* lo = reinterpret_cast<uint4*>(buf + swz(r, c));
+        uint4* hi = reinterpret_cast<uint4*>(buf + swz(r, c + 8));
+        uint4 x = *lo, y = *hi;
+        range = rotate_regs_f16(x, y, cs, sn, range);
+        *lo = x;
+        *hi = y;
+        rope_step(cs, sn, dcs, dsn);
+    }
+    return range;
+}
+
+// Rotate in place `rows` swizzled bf16 rows into FP16, row r at position pos(r)
+// (exact angles per row).
+template <class Pos>
+__device__ __forceinline__ uint32_t rotate_rows_inplace(uint8_t* buf, int rows, Pos pos, const uint64_t* turns,
+                                                        uint32_t range) {
+    for (int it = threadIdx.x; it < rows * 8; it += BW_THREADS) {
+        const int r = it >> 3, c = it & 7;
+        const int ps = pos(r);
+        float2 cs[4], sn[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            rope_cos_sin((uint32_t)ps, turns[8 * c + 2 * e], cs[e].x, sn[e].x);
+            rope_cos_sin((uint32_t)ps, turns[8 * c + 2 * e + 1], cs[e].y, sn[e].y);
+        }
+        uint4* lo = reinterpret_cast<uint4*>(buf + swz(r, c));
+        uint4* hi = reinterpret_cast<uint4*>(buf + swz(r, c + 8));
+        uint4 x = *lo, y = *hi;
+        range = rotate_regs_f16(x, y, cs, sn, range);
+        *lo = x;
+        *hi = y;
+    }
+    return range;
+}
+
 // dS -> FP16 pair; flags a value outside the FP16 range.
 __device__ __forceinline__ uint32_t pack_ds(float a, float b, bool& over) {
     over |= !(fabsf(a) < F16_MAX) || !(fabsf(b) < F16_MAX);
@@ -149,9 +226,10 @@ __device__ __forceinline__ void unrotate_row(float (&acc)[16][4], int half_sel, 
 // of one key tile, per-row lse (log2 domain), delta and position, RoPE rates.
 constexpr int DQ_OFF_Q = 0;
 constexpr int DQ_OFF_DO = DQ_OFF_Q + BW_QB * 256;
-constexpr int DQ_OFF_K = DQ_OFF_DO + BW_QB * 256;
-constexpr int DQ_OFF_V = DQ_OFF_K + BW_KT * 256;
-constexpr int DQ_OFF_L = DQ_OFF_V + BW_KT * 256;
+constexpr int DQ_OFF_K = DQ_OFF_DO + BW_QB * 256;  // two K stages (copied raw, rotated in place)
+constexpr int DQ_OFF_V = DQ_OFF_K + 2 * BW_KT * 256;  // two V stages
+constexpr int DQ_OFF_S = DQ_OFF_V + 2 * BW_KT * 256;  // cos / sin of a 16-position step per pair
+constexpr int DQ_OFF_L = DQ_OFF_S + ROPE_PAIRS * 8;
 constexpr int DQ_OFF_D = DQ_OFF_L + BW_QB * 4;
 constexpr int DQ_OFF_P = DQ_OFF_D + BW_QB * 4;
 constexpr int DQ_OFF_T = DQ_OFF_P + BW_QB * 4;
@@ -168,6 +246,7 @@ __global__ void __launch_bounds__(BW_THREADS) attn_bwd_dq_kernel(const __grid_co
     int* sP = reinterpret_cast<int*>(sm + DQ_OFF_P);
     uint64_t* sT = reinterpret_cast<uint64_t*>(sm + DQ_OFF_T);
     int* sF = reinterpret_cast<int*>(sm + DQ_OFF_F);  // [0] status bits, [1] largest visible key count
+    float2* sS = reinterpret_cast<float2*>(sm + DQ_OFF_S);
     const uint32_t base = smem_u32(sm);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int G = a.G, nrows = a.Sq * G;
@@ -187,7 +266,12 @@ __global__ void __launch_bounds__(BW_THREADS) attn_bwd_dq_kernel(const __grid_co
         sF[0] = (kv_len < 0 || kv_len > a.W * PAGE) ? RK_STATUS_KVLEN : 0;
         sF[1] = 0;
     }
-    if (tid < ROPE_PAIRS) sT[tid] = a.rope_turns[tid];
+    if (tid < ROPE_PAIRS) {
+        sT[tid] = a.rope_turns[tid];
+        float c, sn;
+        rope_cos_sin(16u, a.rope_turns[tid], c, sn);  // the row step of rotate_tile_inplace
+        sS[tid] = make_float2(c, sn);
+    }
     __syncthreads();
     if (tid < BW_QB) {
         int p = -1;
@@ -258,26 +342,31 @@ __global__ void __launch_bounds__(BW_THREADS) attn_bwd_dq_kernel(const __grid_co
     const int n_tiles = bad ? 0 : (n_keys + BW_KT - 1) / BW_KT;
     bool over = false;
     const size_t kstride = (size_t)a.Hkv * HEAD_DIM;
+    // K / V tiles of 64 keys, double-buffered: tile kt + 1 is copied (cp.async)
+    // while tile kt is rotated and used; keys no row of the block sees are
+    // zero-filled (their pages were not checked).
+    auto key_ptr = [&](const void* cache, int t) -> const uint4* {
+        if (t >= n_keys) return nullptr;
+        const int pg = __ldg(bt + t / PAGE);
+        return reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(cache) +
+                                              ((size_t)pg * PAGE + t % PAGE) * kstride + (size_t)kvh * HEAD_DIM);
+    };
+    auto issue_tile = [&](int kt) {
+        const int t0 = kt * BW_KT, st = kt & 1;
+        copy_rows_async(base + DQ_OFF_K + st * BW_KT * 256, BW_KT, [&](int r) { return key_ptr(a.k_cache, t0 + r); },
+                        a.k_cache);
+        copy_rows_async(base + DQ_OFF_V + st * BW_KT * 256, BW_KT, [&](int r) { return key_ptr(a.v_cache, t0 + r); },
+                        a.v_cache);
+        cp_async_commit();
+    };
+    if (n_tiles > 0) issue_tile(0);
     for (int kt = 0; kt < n_tiles; ++kt) {
-        __syncthreads();  // the previous tile's operands are no longer read
-        const int t0 = kt * BW_KT;
-        range = load_rotated(
-            sm + DQ_OFF_K, BW_KT,
-            [&](int r) -> const uint4* {
-                const int t = t0 + r;
-                if (t >= n_keys) return nullptr;  // no row of the block sees it (and its page was not checked)
-                const int pg = __ldg(bt + t / PAGE);
-                return reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(a.k_cache) +
-                                                      ((size_t)pg * PAGE + t % PAGE) * kstride + (size_t)kvh * HEAD_DIM);
-            },
-            [&](int r) { return t0 + r; }, sT, range);
-        load_plain(sm + DQ_OFF_V, BW_KT, [&](int r) -> const uint4* {
-            const int t = t0 + r;
-            if (t >= n_keys) return nullptr;
-            const int pg = __ldg(bt + t / PAGE);
-            return reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(a.v_cache) +
-                                                  ((size_t)pg * PAGE + t % PAGE) * kstride + (size_t)kvh * HEAD_DIM);
-        });
+        const int t0 = kt * BW_KT, st = kt & 1;
+        const uint32_t offK = DQ_OFF_K + st * BW_KT * 256, offV = DQ_OFF_V + st * BW_KT * 256;
+        cp_async_wait_all();
+        __syncthreads();  // tile kt landed everywhere; tile kt - 1 is no longer read
+        if (kt + 1 < n_tiles) issue_tile(kt + 1);
+        range = rotate_tile_inplace(sm + offK, t0, sT, sS, range);
         __syncthreads();
         // S = Q' K'^T and dP = dout V^T for this warp's 16 rows x 64 keys
         float s[8][4], dp[8][4];
@@ -291,8 +380,8 @@ __global__ void __launch_bounds__(BW_THREADS) attn_bwd_dq_kernel(const __grid_co
 #pragma unroll
             for (int np = 0; np < 4; ++np) {
                 uint32_t bk[4], bv[4];
-                ldsm_x4(bk, b_addr(base + DQ_OFF_K, 16 * np, 2 * kk, lane));
-                ldsm_x4(bv, b_addr(base + DQ_OFF_V, 16 * np, 2 * kk, lane));
+                ldsm_x4(bk, b_addr(base + offK, 16 * np, 2 * kk, lane));
+                ldsm_x4(bv, b_addr(base + offV, 16 * np, 2 * kk, lane));
                 mma_f16(s[2 * np], aq, bk[0], bk[1]);
                 mma_f16(s[2 * np + 1], aq, bk[2], bk[3]);
                 mma_bf16(dp[2 * np], ao, bv[0], bv[1]);
@@ -325,7 +414,7 @@ __global__ void __launch_bounds__(BW_THREADS) attn_bwd_dq_kernel(const __grid_co
 #pragma unroll
             for (int nd = 0; nd < 8; ++nd) {
                 uint32_t bk[4];
-                ldsm_x4_t(bk, bt_addr(base + DQ_OFF_K, 16 * ks, 2 * nd, lane));
+                ldsm_x4_t(bk, bt_addr(base + offK, 16 * ks, 2 * nd, lane));
                 mma_f16(acc[2 * nd], sa, bk[0], bk[1]);
                 mma_f16(acc[2 * nd + 1], sa, bk[2], bk[3]);
             }
@@ -359,22 +448,22 @@ __global__ void __launch_bounds__(BW_THREADS) attn_bwd_dq_kernel(const __grid_co
 }
 
 // Shared memory of the dk/dv kernel: K' / V of the CTA's 64 keys, Q' / dout of
-// one block of 32 query rows, per-row lse (log2 domain), delta, position.
+// one block of 64 query rows, per-row lse (natural log), delta, position.
 constexpr int KV_OFF_K = 0;
 constexpr int KV_OFF_V = KV_OFF_K + BW_KT * 256;
-constexpr int KV_OFF_Q = KV_OFF_V + BW_KT * 256;
-constexpr int KV_OFF_DO = KV_OFF_Q + BW_QB_KV * 256;
-constexpr int KV_OFF_L = KV_OFF_DO + BW_QB_KV * 256;
-constexpr int KV_OFF_D = KV_OFF_L + BW_QB_KV * 4;
-constexpr int KV_OFF_P = KV_OFF_D + BW_QB_KV * 4;
-constexpr int KV_OFF_T = KV_OFF_P + BW_QB_KV * 4;
+constexpr int KV_OFF_Q = KV_OFF_V + BW_KT * 256;          // two query blocks (copied raw, rotated in place)
+constexpr int KV_OFF_DO = KV_OFF_Q + 2 * BW_QB_KV * 256;   // two dout blocks
+constexpr int KV_OFF_L = KV_OFF_DO + 2 * BW_QB_KV * 256;   // [2][64] lse (natural log)
+constexpr int KV_OFF_D = KV_OFF_L + 2 * BW_QB_KV * 4;      // [2][64] delta
+constexpr int KV_OFF_P = KV_OFF_D + 2 * BW_QB_KV * 4;      // [2][64] positions
+constexpr int KV_OFF_T = KV_OFF_P + 2 * BW_QB_KV * 4;
 constexpr int KV_OFF_F = KV_OFF_T + ROPE_PAIRS * 8;
 constexpr int KV_SMEM = KV_OFF_F + 16;
 
 // One CTA per (row b, KV head, tile of 64 keys), first tiles first (they are
 // seen by the most queries).  Walks the query rows that can see the tile (the
 // first position >= the tile's first key, found by bisection of the ascending
-// positions) in blocks of 32, ascending, and writes the tile's pages of dk / dv
+// positions) in blocks of 64, ascending, and writes the tile's pages of dk / dv
 // (slots past kv_len get 0).  Reads delta from the dq launch.
 __global__ void __launch_bounds__(BW_THREADS) attn_bwd_dkdv_kernel(const __grid_constant__ BackwardArgs a) {
     extern __shared__ __align__(128) uint8_t sm[];
@@ -441,92 +530,100 @@ __global__ void __launch_bounds__(BW_THREADS) attn_bwd_dkdv_kernel(const __grid_
     const int ka = t0 + 16 * warp + (lane >> 2), kb = ka + 8;  // this lane's two key rows
     bool over = false;
     const int qb0 = sF[1] * G / BW_QB_KV, nqb = (nrows + BW_QB_KV - 1) / BW_QB_KV;
-    for (int qb = qb0; qb < nqb; ++qb) {
-        __syncthreads();  // the previous block's operands are no longer read
-        auto q_off = [&](int r) -> size_t {
-            const int qr = qb * BW_QB_KV + r;
-            return (((size_t)b * a.Hq + kvh * G + qr % G) * a.Sq + qr / G);
-        };
+    // Query blocks of 64 rows, double-buffered: block qb + 1 (q, dout, lse,
+    // delta, positions) is copied (cp.async) while block qb is rotated and used.
+    auto q_off = [&](int qr) -> size_t {  // element offset / HEAD_DIM of query row qr in [B, Hq, Sq]
+        return (((size_t)b * a.Hq + kvh * G + qr % G) * a.Sq + qr / G);
+    };
+    auto issue_block = [&](int qb) {
+        const int sb = qb & 1, r0 = qb * BW_QB_KV;
+        copy_rows_async(base + KV_OFF_Q + sb * BW_QB_KV * 256, BW_QB_KV, [&](int r) -> const uint4* {
+            return r0 + r < nrows ? reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(a.q) +
+                                                                   q_off(r0 + r) * HEAD_DIM)
+                                  : nullptr;
+        }, a.q);
+        copy_rows_async(base + KV_OFF_DO + sb * BW_QB_KV * 256, BW_QB_KV, [&](int r) -> const uint4* {
+            return r0 + r < nrows ? reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(a.dout) +
+                                                                   q_off(r0 + r) * HEAD_DIM)
+                                  : nullptr;
+        }, a.dout);
         if (tid < BW_QB_KV) {
-            const bool ok = qb * BW_QB_KV + tid < nrows;
-            const int qr = qb * BW_QB_KV + tid;
-            sP[tid] = ok ? a.position_ids[(size_t)b * a.Sq + qr / G] : -1;
-            sL[tid] = ok ? a.lse[q_off(tid)] * LOG2E : 0.0f;
-            sD[tid] = ok ? a.delta[q_off(tid)] : 0.0f;
+            const bool ok = r0 + tid < nrows;
+            const size_t o = ok ? q_off(r0 + tid) : 0;
+            cp_async4(base + KV_OFF_P + (sb * BW_QB_KV + tid) * 4,
+                      a.position_ids + (size_t)b * a.Sq + (ok ? (r0 + tid) / G : 0), ok);
+            cp_async4(base + KV_OFF_L + (sb * BW_QB_KV + tid) * 4, a.lse + o, ok);
+            cp_async4(base + KV_OFF_D + (sb * BW_QB_KV + tid) * 4, a.delta + o, ok);
         }
+        cp_async_commit();
+    };
+    if (qb0 < nqb) issue_block(qb0);
+    for (int qb = qb0; qb < nqb; ++qb) {
+        const int sb = qb & 1;
+        const int nvalid = nrows - qb * BW_QB_KV;  // rows of this block that exist
+        const uint32_t offQ = KV_OFF_Q + sb * BW_QB_KV * 256, offO = KV_OFF_DO + sb * BW_QB_KV * 256;
+        const int* bP = sP + sb * BW_QB_KV;
+        const float* bL = sL + sb * BW_QB_KV;
+        const float* bD = sD + sb * BW_QB_KV;
+        cp_async_wait_all();
+        __syncthreads();  // block qb landed everywhere; block qb - 1 is no longer read
+        if (qb + 1 < nqb) issue_block(qb + 1);
+        range = rotate_rows_inplace(sm + offQ, BW_QB_KV, [&](int r) { return max(bP[r], 0); }, sT, range);
         __syncthreads();
-        range = load_rotated(
-            sm + KV_OFF_Q, BW_QB_KV,
-            [&](int r) -> const uint4* {
-                return qb * BW_QB_KV + r < nrows
-                           ? reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(a.q) + q_off(r) * HEAD_DIM)
-                           : nullptr;
-            },
-            [&](int r) { return max(sP[r], 0); }, sT, range);
-        load_plain(sm + KV_OFF_DO, BW_QB_KV, [&](int r) -> const uint4* {
-            return qb * BW_QB_KV + r < nrows
-                       ? reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(a.dout) + q_off(r) * HEAD_DIM)
-                       : nullptr;
-        });
-        __syncthreads();
-        // S^T = K' Q'^T and dP^T = V dout^T: this warp's 16 keys x 32 query rows
-        float st[4][4], dpt[4][4];
+        // S^T = K' Q'^T and dP^T = V dout^T: this warp's 16 keys x 64 query rows
+        float st[8][4], dpt[8][4];
 #pragma unroll
-        for (int j = 0; j < 4; ++j) st[j][0] = st[j][1] = st[j][2] = st[j][3] = dpt[j][0] = dpt[j][1] = dpt[j][2] = dpt[j][3] = 0.0f;
+        for (int j = 0; j < 8; ++j) st[j][0] = st[j][1] = st[j][2] = st[j][3] = dpt[j][0] = dpt[j][1] = dpt[j][2] = dpt[j][3] = 0.0f;
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk) {
             uint32_t ak[4], av[4];
             ldsm_x4(ak, a_addr(base + KV_OFF_K, 16 * warp, 2 * kk, lane));
             ldsm_x4(av, a_addr(base + KV_OFF_V, 16 * warp, 2 * kk, lane));
 #pragma unroll
-            for (int np = 0; np < 2; ++np) {
+            for (int np = 0; np < 4; ++np) {
                 uint32_t bq[4], bo[4];
-                ldsm_x4(bq, b_addr(base + KV_OFF_Q, 16 * np, 2 * kk, lane));
-                ldsm_x4(bo, b_addr(base + KV_OFF_DO, 16 * np, 2 * kk, lane));
+                ldsm_x4(bq, b_addr(base + offQ, 16 * np, 2 * kk, lane));
+                ldsm_x4(bo, b_addr(base + offO, 16 * np, 2 * kk, lane));
                 mma_f16(st[2 * np], ak, bq[0], bq[1]);
                 mma_f16(st[2 * np + 1], ak, bq[2], bq[3]);
                 mma_bf16(dpt[2 * np], av, bo[0], bo[1]);
                 mma_bf16(dpt[2 * np + 1], av, bo[2], bo[3]);
             }
         }
-        // P^T (kept for dV) and dS^T (into st)
-        float pt[4][4];
+        // P^T (BF16, for dV) and dS^T (FP16, for dK') packed straight into the A
+        // fragments of the k = query-row steps: score tile j is half j & 1 of step j >> 1
+        uint32_t pa[4][4], sa[4][4];
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
+        for (int j = 0; j < 8; ++j) {
+            float pv[4], dv4[4];
 #pragma unroll
             for (int e = 0; e < 2; ++e) {
                 const int qc = 8 * j + 2 * (lane & 3) + e;
-                const int p = sP[qc];
-                const float l2 = sL[qc], dl = sD[qc];
-                const float p0 = (ka <= p && ka < kv_len) ? ex2(st[j][e] * a.qk_scale_log2 - l2) : 0.0f;
-                const float p1 = (kb <= p && kb < kv_len) ? ex2(st[j][2 + e] * a.qk_scale_log2 - l2) : 0.0f;
-                pt[j][e] = p0;
-                pt[j][2 + e] = p1;
-                st[j][e] = p0 * (dpt[j][e] - dl);
-                st[j][2 + e] = p1 * (dpt[j][2 + e] - dl);
+                const int p = qc < nvalid ? bP[qc] : -1;
+                const float l2 = bL[qc] * LOG2E, dl = bD[qc];
+                pv[e] = (ka <= p && ka < kv_len) ? ex2(st[j][e] * a.qk_scale_log2 - l2) : 0.0f;
+                pv[2 + e] = (kb <= p && kb < kv_len) ? ex2(st[j][2 + e] * a.qk_scale_log2 - l2) : 0.0f;
+                dv4[e] = pv[e] * (dpt[j][e] - dl);
+                dv4[2 + e] = pv[2 + e] * (dpt[j][2 + e] - dl);
             }
+            const int ks = j >> 1, h = j & 1;
+            pa[ks][2 * h] = pack_bf16x2(pv[0], pv[1]);
+            pa[ks][2 * h + 1] = pack_bf16x2(pv[2], pv[3]);
+            sa[ks][2 * h] = pack_ds(dv4[0], dv4[1], over);
+            sa[ks][2 * h + 1] = pack_ds(dv4[2], dv4[3], over);
         }
-        // dV += P^T dout and dK' += dS^T Q' (k = query rows, 2 steps of 16)
+        // dV += P^T dout and dK' += dS^T Q' (k = query rows, 4 steps of 16)
 #pragma unroll
-        for (int ks = 0; ks < 2; ++ks) {
-            uint32_t pa[4], sa[4];
-            pa[0] = pack_bf16x2(pt[2 * ks][0], pt[2 * ks][1]);
-            pa[1] = pack_bf16x2(pt[2 * ks][2], pt[2 * ks][3]);
-            pa[2] = pack_bf16x2(pt[2 * ks + 1][0], pt[2 * ks + 1][1]);
-            pa[3] = pack_bf16x2(pt[2 * ks + 1][2], pt[2 * ks + 1][3]);
-            sa[0] = pack_ds(st[2 * ks][0], st[2 * ks][1], over);
-            sa[1] = pack_ds(st[2 * ks][2], st[2 * ks][3], over);
-            sa[2] = pack_ds(st[2 * ks + 1][0], st[2 * ks + 1][1], over);
-            sa[3] = pack_ds(st[2 * ks + 1][2], st[2 * ks + 1][3], over);
+        for (int ks = 0; ks < 4; ++ks) {
 #pragma unroll
             for (int nd = 0; nd < 8; ++nd) {
                 uint32_t bo[4], bq[4];
-                ldsm_x4_t(bo, bt_addr(base + KV_OFF_DO, 16 * ks, 2 * nd, lane));
-                ldsm_x4_t(bq, bt_addr(base + KV_OFF_Q, 16 * ks, 2 * nd, lane));
-                mma_bf16(dv[2 * nd], pa, bo[0], bo[1]);
-                mma_bf16(dv[2 * nd + 1], pa, bo[2], bo[3]);
-                mma_f16(dk[2 * nd], sa, bq[0], bq[1]);
-                mma_f16(dk[2 * nd + 1], sa, bq[2], bq[3]);
+                ldsm_x4_t(bo, bt_addr(base + offO, 16 * ks, 2 * nd, lane));
+                ldsm_x4_t(bq, bt_addr(base + offQ, 16 * ks, 2 * nd, lane));
+                mma_bf16(dv[2 * nd], pa[ks], bo[0], bo[1]);
+                mma_bf16(dv[2 * nd + 1], pa[ks], bo[2], bo[3]);
+                mma_f16(dk[2 * nd], sa[ks], bq[0], bq[1]);
+                mma_f16(dk[2 * nd + 1], sa[ks], bq[2], bq[3]);
             }
         }
     }

@@ -117,7 +117,7 @@ struct BackwardArgs {
 constexpr int BW_THREADS = 128;  // 4 warps, 16 accumulator rows each
 constexpr int BW_KT = 64;        // keys per dk/dv CTA and per key tile of the dq kernel
 constexpr int BW_QB = 64;        // query rows (position x head) per dq CTA
-constexpr int BW_QB_KV = 32;     // query rows per step of the dk/dv kernel
+constexpr int BW_QB_KV = 64;     // query rows per step of the dk/dv kernel
 
 // ------------------------------------------------------------ append ----
 // Write n_new tokens per row into the page cache (kv_lens after the append).
