@@ -320,7 +320,7 @@ def measure_backward(args, dev, stream, tf_burst, peak_kind):
                        "flops": "10*D*visible_pairs*Hq = %.4g" % flops},
             "roofline": {"bound": "tensor", "achieved": achieved, "peak": tf_burst, "unit": "TFLOP/s",
                          "frac": achieved / tf_burst, "traffic": None,
-                         "kernel": "attn_bwd_dq_kernel + attn_bwd_dkdv_kernel (mma.sync)",
+                         "kernel": "attn_bwd_dq_tc_kernel + attn_bwd_dkdv_tc_kernel (tcgen05)",
                          "peak_kind": peak_kind + " (bf16 dense, burst)"},
             "note": "two launches per call (dq with delta, then dk/dv); deterministic, no atomics"}
 

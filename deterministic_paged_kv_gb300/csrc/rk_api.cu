@@ -24,7 +24,10 @@ cudaError_t launch_decode(const CUtensorMap& km, const CUtensorMap& vm, const De
 cudaError_t launch_prefill(const CUtensorMap& qm, const CUtensorMap& km, const CUtensorMap& vm,
                            const PrefillArgs& a, cudaStream_t stream, bool overlap_previous = false);
 cudaError_t launch_kv_append(const AppendArgs& a, cudaStream_t stream);
-cudaError_t launch_backward(const BackwardArgs& a, cudaStream_t stream);
+cudaError_t launch_backward_dkdv_tc(const CUtensorMap& qm, const CUtensorMap& om, const CUtensorMap& km,
+                                    const CUtensorMap& vm, const BackwardArgs& a, cudaStream_t stream);
+cudaError_t launch_backward_dq_tc(const CUtensorMap& qm, const CUtensorMap& om, const CUtensorMap& km,
+                                  const CUtensorMap& vm, const BackwardArgs& a, cudaStream_t stream);
 }  // namespace rk
 
 namespace {
@@ -634,12 +637,33 @@ int rk_paged_attn_prefill_backward(const rk_paged_plan_t* plan, const void* q, c
     a.G = plan->Hq / plan->Hkv;
     a.W = plan->W;
     a.num_pages = plan->num_pages;
-    // key tiles of the widest row the table allows (tiles past a row's pages exit at once)
-    a.n_key_tiles = (int32_t)(((int64_t)plan->W * rk::PAGE + rk::BW_KT - 1) / rk::BW_KT);
     a.sm_scale = (float)(1.0 / std::sqrt((double)plan->D));
     a.qk_scale_log2 = (float)((1.0 / std::sqrt((double)plan->D)) * 1.4426950408889634074);
     std::memcpy(a.rope_turns, plan->rope_turns, sizeof a.rope_turns);
-    cudaError_t e = rk::launch_backward(a, reinterpret_cast<cudaStream_t>(stream));
+    // tensor maps of the dk / dv kernel: q and dout [B, Hq, Sq, D] as 4-D (d, position, head, row) with
+    // a box of one 64-column half of a query block (64, 128/G positions, G heads, 1 row); both caches
+    // in 16-token x 64-dim page boxes (the K-major tile layout of both A operands)
+    CUtensorMap qm, om, km, vm;
+    {
+        const int G = plan->Hq / plan->Hkv;
+        const cuuint64_t dims[4] = {(cuuint64_t)rk::HEAD_DIM, (cuuint64_t)plan->Sq, (cuuint64_t)plan->Hq,
+                                    (cuuint64_t)plan->B};
+        const cuuint64_t strides[3] = {(cuuint64_t)rk::HEAD_DIM * 2, (cuuint64_t)plan->Sq * rk::HEAD_DIM * 2,
+                                       (cuuint64_t)plan->Hq * plan->Sq * rk::HEAD_DIM * 2};
+        const cuuint32_t box[4] = {64, (cuuint32_t)(rk::PF_BM / G), (cuuint32_t)G, 1};
+        if ((rc = make_map(&qm, q, 4, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B, "q"))) return rc;
+        if ((rc = make_map(&om, dout, 4, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B, "dout"))) return rc;
+    }
+    const bool have = plan->num_pages > 0;
+    if ((rc = make_cache_map(&km, have ? k_cache : q, have ? plan->num_pages : 1, have ? plan->Hkv : 1, 64,
+                             CU_TENSOR_MAP_SWIZZLE_128B, "k_cache")))
+        return rc;
+    if ((rc = make_cache_map(&vm, have ? v_cache : q, have ? plan->num_pages : 1, have ? plan->Hkv : 1, 64,
+                             CU_TENSOR_MAP_SWIZZLE_128B, "v_cache")))
+        return rc;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    cudaError_t e = rk::launch_backward_dq_tc(qm, om, km, vm, a, st);  // dq and delta
+    if (e == cudaSuccess) e = rk::launch_backward_dkdv_tc(qm, om, km, vm, a, st);
     if (e != cudaSuccess) return fail(RK_E_CUDA, "backward launch: %s", cudaGetErrorString(e));
     return RK_OK;
 }

@@ -109,15 +109,10 @@ struct BackwardArgs {
     float* delta;
     int32_t* status;
     int32_t B, Sq, Hq, Hkv, G, W, num_pages;
-    int32_t n_key_tiles;          // key tiles of BW_KT tokens covering the longest row (dk/dv grid)
     float sm_scale;
     float qk_scale_log2;          // sm_scale * log2(e)
     uint64_t rope_turns[ROPE_PAIRS];
 };
-constexpr int BW_THREADS = 128;  // 4 warps, 16 accumulator rows each
-constexpr int BW_KT = 64;        // keys per dk/dv CTA and per key tile of the dq kernel
-constexpr int BW_QB = 64;        // query rows (position x head) per dq CTA
-constexpr int BW_QB_KV = 64;     // query rows per step of the dk/dv kernel
 
 // ------------------------------------------------------------ append ----
 // Write n_new tokens per row into the page cache (kv_lens after the append).

@@ -343,9 +343,9 @@ int rk_paged_attn_ragged(const rk_paged_plan_t *plan, int32_t max_q_len, const i
  * Deterministic and batch-invariant: every output element is accumulated by
  * one CTA in a fixed order (dq over key tiles ascending, dk / dv over query
  * blocks ascending), no atomics.  Arithmetic: FP32 accumulation on the
- * tensor cores; rotated q / k and dS rounded to FP16, P to BF16 for the dV
- * product.  Two launches on `stream` (dq with delta, then dk / dv), no
- * allocation, no host synchronisation.  Device status bits as the forward;
+ * tcgen05 tensor cores (accumulators in TMEM); rotated q / k and dS rounded
+ * to FP16, P to BF16 for the dV product.  Two launches on `stream` (dq with
+ * delta, then dk / dv), no allocation, no host synchronisation.  Device status bits as the forward;
  * rows whose rotated operands or dS leave the FP16 range get NaN gradients
  * and RK_STATUS_RANGE.  Errors: as rk_paged_attn_prefill, plus RK_E_ARG for
  * a null or misaligned dout / dq / dk_cache / dv_cache / delta.
