@@ -56,7 +56,7 @@ constexpr int BT_OFF_V = BT_OFF_K + BT_TILE;
 constexpr int BT_OFF_Q = BT_OFF_V + BT_TILE;      // two stages
 constexpr int BT_OFF_DO = BT_OFF_Q + 2 * BT_TILE;  // two stages
 constexpr int BT_OFF_LD = BT_OFF_DO + 2 * BT_TILE; // two stages of [lse2 | delta | position] x 128
-constexpr int BT_LD_BYTES = 3 * BT_QB * 4;
+constexpr int BT_LD_BYTES = 3 * BT_QB * 4 + 16;  // + the smallest position of each 32-column quarter
 constexpr int BT_OFF_BAR = BT_OFF_LD + 2 * BT_LD_BYTES;
 constexpr int BT_CTRL_BYTES = 2048;
 constexpr int BT_SMEM = BT_OFF_BAR + BT_CTRL_BYTES;
@@ -304,7 +304,10 @@ __global__ void __launch_bounds__(BT_THREADS, 1)
                 float* ld = reinterpret_cast<float*>(sm + BT_OFF_LD + st * BT_LD_BYTES);
                 ld[tid] = valid ? a.lse[o] * 1.4426950408889634074f : 0.0f;
                 ld[BT_QB + tid] = valid ? a.delta[o] : 0.0f;
-                reinterpret_cast<int*>(ld)[2 * BT_QB + tid] = valid ? a.position_ids[(size_t)b * a.Sq + s] : -1;
+                const int pq = valid ? a.position_ids[(size_t)b * a.Sq + s] : -1;
+                reinterpret_cast<int*>(ld)[2 * BT_QB + tid] = pq;
+                const int pmin = __reduce_min_sync(0xffffffffu, pq);  // warp w holds columns 32 w .. 32 w + 31
+                if (lane == 0) reinterpret_cast<int*>(ld)[3 * BT_QB + warp] = pmin;
             }
             // query rows g * rph + sl share position s0 + sl: exact angles per distinct position
             uint8_t* qt = sm + BT_OFF_Q + st * BT_TILE;
@@ -358,25 +361,46 @@ __global__ void __launch_bounds__(BT_THREADS, 1)
                 tmem_ld32(tmem + lane_addr + cb, xs);
                 tmem_ld32(tmem + lane_addr + 128 + cb, xd);
                 tmem_ld_wait();
+                // every column (valid, position >= this key) sees every key row of the warp: no masks
+                if (__all_sync(0xffffffffu, key_ok && t <= lp[BT_QB + (cb >> 5)])) {
+                    const float2 sc2 = make_float2(scl, scl);
 #pragma unroll
-                for (int c = 0; c < 32; c += 4) {
-                    const float4 l4 = *reinterpret_cast<const float4*>(ld + cb + c);
-                    const float4 d4 = *reinterpret_cast<const float4*>(ld + BT_QB + cb + c);
-                    const int4 p4 = *reinterpret_cast<const int4*>(lp + cb + c);
-                    const float lv[4] = {l4.x, l4.y, l4.z, l4.w}, dv[4] = {d4.x, d4.y, d4.z, d4.w};
-                    const int pv[4] = {p4.x, p4.y, p4.z, p4.w};
-                    float pp[4], ds[4];
+                    for (int c = 0; c < 32; c += 4) {
+                        const float4 l4 = *reinterpret_cast<const float4*>(ld + cb + c);
+                        const float4 d4 = *reinterpret_cast<const float4*>(ld + BT_QB + cb + c);
 #pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const bool vis = key_ok && t <= pv[e];
-                        pp[e] = vis ? ex2(__uint_as_float(xs[c + e]) * scl - lv[e]) : 0.0f;
-                        ds[e] = vis ? pp[e] * (__uint_as_float(xd[c + e]) - dv[e]) : 0.0f;
-                        over |= !(fabsf(ds[e]) < 65504.0f);
+                        for (int e = 0; e < 4; e += 2) {
+                            const float2 nl = e ? make_float2(-l4.z, -l4.w) : make_float2(-l4.x, -l4.y);
+                            const float2 nd = e ? make_float2(-d4.z, -d4.w) : make_float2(-d4.x, -d4.y);
+                            const float2 t2 =
+                                ffma2(make_float2(__uint_as_float(xs[c + e]), __uint_as_float(xs[c + e + 1])), sc2, nl);
+                            const float2 pp = make_float2(ex2(t2.x), ex2(t2.y));
+                            const float2 ds = fmul2(
+                                pp, fadd2(make_float2(__uint_as_float(xd[c + e]), __uint_as_float(xd[c + e + 1])), nd));
+                            xs[(c + e) >> 1] = pack_bf16x2(pp.x, pp.y);
+                            xd[(c + e) >> 1] = pack_f16x2(ds.x, ds.y);
+                        }
                     }
-                    xs[c >> 1] = pack_bf16x2(pp[0], pp[1]);
-                    xs[(c >> 1) + 1] = pack_bf16x2(pp[2], pp[3]);
-                    xd[c >> 1] = pack_f16x2(ds[0], ds[1]);
-                    xd[(c >> 1) + 1] = pack_f16x2(ds[2], ds[3]);
+                } else {
+#pragma unroll
+                    for (int c = 0; c < 32; c += 4) {
+                        const float4 l4 = *reinterpret_cast<const float4*>(ld + cb + c);
+                        const float4 d4 = *reinterpret_cast<const float4*>(ld + BT_QB + cb + c);
+                        const int4 p4 = *reinterpret_cast<const int4*>(lp + cb + c);
+                        const float lv[4] = {l4.x, l4.y, l4.z, l4.w}, dv[4] = {d4.x, d4.y, d4.z, d4.w};
+                        const int pv[4] = {p4.x, p4.y, p4.z, p4.w};
+                        float pp[4], ds[4];
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            const bool vis = key_ok && t <= pv[e];
+                            pp[e] = vis ? ex2(__uint_as_float(xs[c + e]) * scl - lv[e]) : 0.0f;
+                            ds[e] = vis ? pp[e] * (__uint_as_float(xd[c + e]) - dv[e]) : 0.0f;
+                        }
+                        xs[c >> 1] = pack_bf16x2(pp[0], pp[1]);
+                        xs[(c >> 1) + 1] = pack_bf16x2(pp[2], pp[3]);
+                        xd[c >> 1] = pack_f16x2(ds[0], ds[1]);
+                        xd[(c >> 1) + 1] = pack_f16x2(ds[2], ds[3]);
+                    }
                 }
                 tmem_st16(tmem + lane_addr + c0 + 16 * h, *reinterpret_cast<uint32_t(*)[16]>(&xs[0]));
                 tmem_st16(tmem + lane_addr + 128 + c0 + 16 * h, *reinterpret_cast<uint32_t(*)[16]>(&xd[0]));
@@ -385,9 +409,19 @@ __global__ void __launch_bounds__(BT_THREADS, 1)
             tc_fence_before();
             mbar_arrive(smem_u32(&bars->p_ready));
         }
-        if (over) bars->range_bad = 1;
         if (ok) ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&bars->done), 0, abort));
         tc_fence_after();
+        if (ok && hsel == 0) {  // a dS beyond the FP16 range (rounded to infinity) leaves dK' non-finite
+#pragma unroll 1
+            for (int c4 = 0; c4 < 4; ++c4) {
+                uint32_t v[32];
+                tmem_ld32(tmem + lane_addr + 384 + 32 * c4, v);
+                tmem_ld_wait();
+#pragma unroll
+                for (int k = 0; k < 32; ++k) over |= !isfinite(__uint_as_float(v[k]));
+            }
+        }
+        if (over) bars->range_bad = 1;
         named_bar_sync(1, 384);  // every range flag is set
         const bool bad_out = bars->range_bad != 0 || !ok;
         if (tid == 128 && bad_out && a.status) atomicOr(a.status, ok ? RK_STATUS_RANGE : RK_STATUS_TIMEOUT);
@@ -737,18 +771,29 @@ __global__ void __launch_bounds__(BT_THREADS, 1)
                 tmem_ld32(tmem + lane_addr + cb, xs);
                 tmem_ld32(tmem + lane_addr + 128 + cb, xd);
                 tmem_ld_wait();
+                // every key of these 32 columns visible to every row of the warp: no masks
+                if (__all_sync(0xffffffffu, tb + cb + 31 <= p && tb + cb + 31 < kv_len)) {
+                    const float2 sc2 = make_float2(scl, scl), nl2 = make_float2(-l2, -l2), nd2 = make_float2(-delta, -delta);
 #pragma unroll
-                for (int c = 0; c < 32; c += 2) {
-                    float ds[2];
-#pragma unroll
-                    for (int e = 0; e < 2; ++e) {
-                        const int t = tb + cb + c + e;
-                        const bool vis = t <= p && t < kv_len;
-                        const float pp = vis ? ex2(__uint_as_float(xs[c + e]) * scl - l2) : 0.0f;
-                        ds[e] = vis ? pp * (__uint_as_float(xd[c + e]) - delta) : 0.0f;
-                        over |= !(fabsf(ds[e]) < 65504.0f);
+                    for (int c = 0; c < 32; c += 2) {
+                        const float2 t2 = ffma2(make_float2(__uint_as_float(xs[c]), __uint_as_float(xs[c + 1])), sc2, nl2);
+                        const float2 pp = make_float2(ex2(t2.x), ex2(t2.y));
+                        const float2 ds = fmul2(pp, fadd2(make_float2(__uint_as_float(xd[c]), __uint_as_float(xd[c + 1])), nd2));
+                        xs[c >> 1] = pack_f16x2(ds.x, ds.y);
                     }
-                    xs[c >> 1] = pack_f16x2(ds[0], ds[1]);
+                } else {
+#pragma unroll
+                    for (int c = 0; c < 32; c += 2) {
+                        float ds[2];
+#pragma unroll
+                        for (int e = 0; e < 2; ++e) {
+                            const int t = tb + cb + c + e;
+                            const bool vis = t <= p && t < kv_len;
+                            const float pp = vis ? ex2(__uint_as_float(xs[c + e]) * scl - l2) : 0.0f;
+                            ds[e] = vis ? pp * (__uint_as_float(xd[c + e]) - delta) : 0.0f;
+                        }
+                        xs[c >> 1] = pack_f16x2(ds[0], ds[1]);
+                    }
                 }
                 tmem_st16(tmem + lane_addr + c0 + 16 * h, *reinterpret_cast<uint32_t(*)[16]>(&xs[0]));
             }
@@ -756,20 +801,23 @@ __global__ void __launch_bounds__(BT_THREADS, 1)
             tc_fence_before();
             mbar_arrive(smem_u32(&bars->p_ready));
         }
-        if (over) bars->range_bad = 1;
         if (ok) ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&bars->done), 0, abort));
         tc_fence_after();
-        named_bar_sync(1, 384);
-        const bool bad_out = bars->range_bad != 0 || !ok;
-        if (tid == 128 && bad_out && a.status) atomicOr(a.status, ok ? RK_STATUS_RANGE : RK_STATUS_TIMEOUT);
         // epilogue: dq = R(p)^T (scale dQ'); warpgroup 1 takes rotation pairs 0..31
-        // (dims 0..31 and 64..95), warpgroup 2 pairs 32..63 (dims 32..63 and 96..127)
+        // (dims 0..31 and 64..95), warpgroup 2 pairs 32..63 (dims 32..63 and 96..127).
+        // A dS beyond the FP16 range (rounded to infinity) leaves dQ' non-finite.
         uint32_t lo[32], hi[32];
         if (ok) {  // warp-uniform; every lane loads
             tmem_ld32(tmem + lane_addr + 256 + 32 * hsel, lo);
             tmem_ld32(tmem + lane_addr + 256 + 64 + 32 * hsel, hi);
             tmem_ld_wait();
+#pragma unroll
+            for (int k = 0; k < 32; ++k) over |= !isfinite(__uint_as_float(lo[k])) || !isfinite(__uint_as_float(hi[k]));
         }
+        if (over && valid) bars->range_bad = 1;
+        named_bar_sync(1, 384);
+        const bool bad_out = bars->range_bad != 0 || !ok;
+        if (tid == 128 && bad_out && a.status) atomicOr(a.status, ok ? RK_STATUS_RANGE : RK_STATUS_TIMEOUT);
         if (valid) {
             float* dst = a.dq + o * HEAD_DIM;
 #pragma unroll
