@@ -299,11 +299,11 @@ def measure_backward(args, dev, stream, tf_burst, peak_kind):
     dq = torch.empty(w.q.shape, dtype=torch.float32, device=dev)
     dk = torch.empty(w.k_cache.shape, dtype=torch.float32, device=dev)
     dv = torch.empty(w.v_cache.shape, dtype=torch.float32, device=dev)
-    delta = torch.empty((w.B, w.Hq, w.Sq), dtype=torch.float32, device=dev)
+    ws = torch.empty(binding.prefill_backward_workspace_bytes(p), dtype=torch.uint8, device=dev)
 
     def step():
         binding.attn_prefill_backward(p, d["q"], d["k_cache"], d["v_cache"], d["block_table"], d["kv_lens"],
-                                      d["position_ids"], out, lse, dout, dq, dk, dv, delta, stream=stream)
+                                      d["position_ids"], out, lse, dout, dq, dk, dv, ws, stream=stream)
 
     for _ in range(3):
         step()
@@ -322,7 +322,7 @@ def measure_backward(args, dev, stream, tf_burst, peak_kind):
                          "frac": achieved / tf_burst, "traffic": None,
                          "kernel": "attn_bwd_dq_tc_kernel + attn_bwd_dkdv_tc_kernel (tcgen05)",
                          "peak_kind": peak_kind + " (bf16 dense, burst)"},
-            "note": "two launches per call (dq with delta, then dk/dv); deterministic, no atomics"}
+            "note": "four launches per call (rotation of q and K into the workspace, dq with delta, dk/dv); deterministic, no atomics"}
 
 
 def measure_decode_long(args, dev, stream, hbm, peak_kind, split_tokens=2048):

@@ -96,7 +96,10 @@ def load(path: str | None = None):
         lib.rk_paged_attn_ragged.restype = ctypes.c_int
         lib.rk_paged_attn_ragged.argtypes = [ctypes.POINTER(Plan), ctypes.c_int32] + [vp] * 11
         lib.rk_paged_attn_prefill_backward.restype = ctypes.c_int
-        lib.rk_paged_attn_prefill_backward.argtypes = [ctypes.POINTER(Plan)] + [vp] * 15
+        lib.rk_paged_attn_prefill_backward.argtypes = [ctypes.POINTER(Plan)] + [vp] * 13 + \
+            [ctypes.c_uint64, vp, vp]
+        lib.rk_paged_prefill_backward_workspace_bytes.restype = ctypes.c_int
+        lib.rk_paged_prefill_backward_workspace_bytes.argtypes = [ctypes.POINTER(Plan), ctypes.POINTER(ctypes.c_uint64)]
         lib.rk_last_error.restype = ctypes.c_char_p
         lib.rk_last_error.argtypes = []
         lib.rk_paged_policy.restype = ctypes.c_char_p
@@ -205,27 +208,36 @@ def attn_prefill(p: Plan, q, k_cache, v_cache, block_table, kv_lens, position_id
             position_ids, out, lse, status, stream)
 
 
+def prefill_backward_workspace_bytes(p: Plan) -> int:
+    """rk_paged_prefill_backward_workspace_bytes: device workspace bytes of the backward."""
+    n = ctypes.c_uint64(0)
+    _check(load().rk_paged_prefill_backward_workspace_bytes(ctypes.byref(p), ctypes.byref(n)))
+    return int(n.value)
+
+
 def attn_prefill_backward(p: Plan, q, k_cache, v_cache, block_table, kv_lens, position_ids, out, lse, dout,
-                          dq, dk_cache, dv_cache, delta, status=None, stream=None):
-    """rk_paged_attn_prefill_backward on device tensors: dq [B, Hq, Sq, D],
-    dk_cache / dv_cache [num_pages, 16, Hkv, D] and delta [B, Hq, Sq], all
-    float32; asynchronous on ``stream``."""
+                          dq, dk_cache, dv_cache, workspace, status=None, stream=None):
+    """rk_paged_attn_prefill_backward on device tensors: dq [B, Hq, Sq, D] and
+    dk_cache / dv_cache [num_pages, 16, Hkv, D] float32; ``workspace`` a CUDA
+    tensor of at least ``prefill_backward_workspace_bytes`` bytes (any dtype,
+    256-byte aligned); asynchronous on ``stream``."""
     import torch
     for t, dt, name in ((q, torch.bfloat16, "q"), (k_cache, torch.bfloat16, "k_cache"),
                         (v_cache, torch.bfloat16, "v_cache"), (out, torch.bfloat16, "out"),
                         (lse, torch.float32, "lse"), (dout, torch.bfloat16, "dout"),
                         (dq, torch.float32, "dq"), (dk_cache, torch.float32, "dk_cache"),
-                        (dv_cache, torch.float32, "dv_cache"), (delta, torch.float32, "delta"),
+                        (dv_cache, torch.float32, "dv_cache"),
                         (block_table, torch.int32, "block_table"), (kv_lens, torch.int32, "kv_lens"),
                         (position_ids, torch.int32, "position_ids")):
         if t.dtype != dt:
             raise TypeError("%s must be %s (got %s)" % (name, dt, t.dtype))
     if status is not None and status.dtype != torch.int32:
         raise TypeError("status must be int32")
+    nbytes = workspace.numel() * workspace.element_size()
     rc = load().rk_paged_attn_prefill_backward(
         ctypes.byref(p), _dptr(q), _dptr(k_cache), _dptr(v_cache), _dptr(block_table), _dptr(kv_lens),
         _dptr(position_ids), _dptr(out), _dptr(lse), _dptr(dout), _dptr(dq), _dptr(dk_cache), _dptr(dv_cache),
-        _dptr(delta), _dptr(status), _stream(stream))
+        _dptr(workspace), nbytes, _dptr(status), _stream(stream))
     _check(rc)
 
 

@@ -27,6 +27,7 @@
 //                 dk, warpgroup 2 dv;
 //   warp 12       TMA producer (the key and value tiles once, query / dout
 //                 blocks double-buffered); warp 13 MMA issuer.
+#include <algorithm>
 #include <atomic>
 #include <cstring>
 
@@ -63,7 +64,7 @@ constexpr int BT_SMEM = BT_OFF_BAR + BT_CTRL_BYTES;
 static_assert(BT_SMEM <= 232448, "shared memory above the 227 KiB opt-in limit");
 
 struct BtBars {
-    uint64_t k_full, k_ready, v_full;
+    uint64_t k_full, v_full;
     uint64_t q_full[2], q_ready[2], q_empty[2];
     uint64_t s_full, p_ready, done;
     uint32_t tmem_base;
@@ -92,6 +93,70 @@ __device__ __forceinline__ void mma_ts_split(uint32_t d, uint32_t a_tmem, uint32
         "n"(kstep_off(LB, KS)), "r"(KS > 0 ? 1u : acc0)
         : "memory");
     if constexpr (KS + 1 < 8) mma_ts_split<KS + 1, LB>(d, a_tmem, b_lo, idesc, acc0);
+}
+
+
+// ---------------------------------------------------------- rotation ----
+// The backward reads every query block once per key tile and every key tile
+// once per query tile, so RoPE is applied once per call instead: q and the
+// pages of each row's keys are rotated (FP32 math, exact angles from the
+// fixed-point rates) and stored as FP16 in the caller's workspace.  A
+// pre-RoPE element with |x| >= 2^15 (whose rotation may leave the FP16 range)
+// is stored as infinity: the gradients it enters come out non-finite and are
+// reported as RK_STATUS_RANGE by the kernels below.
+__device__ __forceinline__ void rotate_store(const uint4* src, uint4* dst, int c, int pos, const uint64_t* turns) {
+    uint4 lo = __ldg(src + c), hi = __ldg(src + c + 8);
+    const uint32_t lw[4] = {lo.x, lo.y, lo.z, lo.w}, hw[4] = {hi.x, hi.y, hi.z, hi.w};
+    uint32_t big = 0;
+#pragma unroll
+    for (int k = 0; k < 4; ++k) big |= (uint32_t)range_exceeded(__vmaxu2(lw[k] & 0x7fff7fffu, hw[k] & 0x7fff7fffu));
+    float2 cs[4], sn[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+        rope_cos_sin((uint32_t)pos, turns[8 * c + 2 * e], cs[e].x, sn[e].x);
+        rope_cos_sin((uint32_t)pos, turns[8 * c + 2 * e + 1], cs[e].y, sn[e].y);
+    }
+    rotate_regs_f16(lo, hi, cs, sn, 0u);
+    if (big) lo = hi = make_uint4(0x7c007c00u, 0x7c007c00u, 0x7c007c00u, 0x7c007c00u);
+    dst[c] = lo;
+    dst[c + 8] = hi;
+}
+
+// one thread per (query row, chunk pair): q_rot[b, h, s] = R(position) q[b, h, s]
+__global__ void __launch_bounds__(256) rotate_q_kernel(const __grid_constant__ BackwardArgs a) {
+    const long long n = (long long)a.B * a.Hq * a.Sq * 8;
+    for (long long it = (long long)blockIdx.x * blockDim.x + threadIdx.x; it < n; it += (long long)gridDim.x * blockDim.x) {
+        const long long row = it >> 3;  // (b * Hq + h) * Sq + s
+        const int c = (int)(it & 7), s = (int)(row % a.Sq), b = (int)(row / ((long long)a.Hq * a.Sq));
+        const int p = a.position_ids[(size_t)b * a.Sq + s];
+        rotate_store(reinterpret_cast<const uint4*>(a.q) + row * 16, reinterpret_cast<uint4*>(a.q_rot) + row * 16, c,
+                     max(p, 0), a.rope_turns);
+    }
+}
+
+// one thread per (row, table entry, slot, KV head, chunk pair) of the keys a row
+// holds: k_rot[page, slot, kvh] = R(t) k_cache[page, slot, kvh], t = 16 entry + slot
+// (0 past kv_len); unsafe lengths or page ids are skipped (the kernels report them)
+__global__ void __launch_bounds__(256) rotate_k_kernel(const __grid_constant__ BackwardArgs a) {
+    const long long per_row = (long long)a.W * PAGE * a.Hkv * 8;
+    const long long n = (long long)a.B * per_row;
+    for (long long it = (long long)blockIdx.x * blockDim.x + threadIdx.x; it < n; it += (long long)gridDim.x * blockDim.x) {
+        const int b = (int)(it / per_row);
+        const long long rem = it % per_row;
+        const int c = (int)(rem & 7), kvh = (int)((rem >> 3) % a.Hkv), t = (int)((rem >> 3) / a.Hkv);
+        const int kv_len = a.kv_lens[b];
+        if (kv_len < 0 || kv_len > a.W * PAGE || t >= (kv_len + PAGE - 1) / PAGE * PAGE) continue;
+        const int pg = __ldg(a.block_table + (size_t)b * a.W + t / PAGE);
+        if (pg < 0 || pg >= a.num_pages) continue;
+        const size_t e = ((size_t)pg * PAGE + t % PAGE) * a.Hkv + kvh;  // 256-byte row index
+        uint4* dst = reinterpret_cast<uint4*>(a.k_rot) + e * 16;
+        if (t < kv_len) {
+            rotate_store(reinterpret_cast<const uint4*>(a.k_cache) + e * 16, dst, c, t, a.rope_turns);
+        } else {
+            dst[c] = make_uint4(0, 0, 0, 0);
+            dst[c + 8] = make_uint4(0, 0, 0, 0);
+        }
+    }
 }
 
 // Write rows [0, n_rows) of a key tile's dk and dv as zeros (no query sees it).
@@ -136,7 +201,6 @@ __global__ void __launch_bounds__(BT_THREADS, 1)
         bars->abort = 0;
         bars->range_bad = 0;
         mbar_init(smem_u32(&bars->k_full), 1);
-        mbar_init(smem_u32(&bars->k_ready), 128);
         mbar_init(smem_u32(&bars->v_full), 1);
         for (int j = 0; j < 2; ++j) {
             mbar_init(smem_u32(&bars->q_full[j]), 1);
@@ -240,7 +304,7 @@ __global__ void __launch_bounds__(BT_THREADS, 1)
             const uint32_t idK = (1u << 4) | (1u << 16) | ((uint32_t)(HEAD_DIM >> 3) << 17) |
                                  ((uint32_t)(BT_KEYS >> 4) << 24);
             const uint32_t dK = desc_lo(s_base + BT_OFF_K, 16), dV = desc_lo(s_base + BT_OFF_V, 16);
-            bool ok = mbar_wait(smem_u32(&bars->k_ready), 0, abort) && mbar_wait(smem_u32(&bars->v_full), 0, abort);
+            bool ok = mbar_wait(smem_u32(&bars->k_full), 0, abort) && mbar_wait(smem_u32(&bars->v_full), 0, abort);
             for (int jj = 0; jj < nblk && ok; ++jj) {
                 const int st = jj & 1;
                 if (!(ok = mbar_wait(smem_u32(&bars->q_ready[st]), (uint32_t)((jj >> 1) & 1), abort))) break;
@@ -267,32 +331,10 @@ __global__ void __launch_bounds__(BT_THREADS, 1)
         named_bar_sync(2, BT_THREADS);
     } else if (wg == 0) {
         asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(BT_REG_XFORM));
-        // ================================================== transform WG ====
-        uint32_t range = 0;
-        const int u = tid & 7, r0 = tid >> 3;  // pair-chunk u of rows r0 + 16 m
-        bool ok = mbar_wait(smem_u32(&bars->k_full), 0, abort);
-        if (ok) {
-            // keys at positions t0 + r: exact angles at r0, 16-position steps after it
-            uint8_t* kt_s = sm + BT_OFF_K;
-            float2 c[4], sn[4], dcs[4], dsn[4];
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                rope_cos_sin((uint32_t)(t0 + r0), bars->turns[8 * u + 2 * e], c[e].x, sn[e].x);
-                rope_cos_sin((uint32_t)(t0 + r0), bars->turns[8 * u + 2 * e + 1], c[e].y, sn[e].y);
-                const float2 s0v = bars->step16[8 * u + 2 * e], s1v = bars->step16[8 * u + 2 * e + 1];
-                dcs[e] = make_float2(s0v.x, s1v.x);
-                dsn[e] = make_float2(s0v.y, s1v.y);
-            }
-#pragma unroll 2
-            for (int m = 0; m < 8; ++m) {
-                const int r = r0 + 16 * m;
-                const uint32_t off = sw128_off(r, u);
-                if (t0 + r < kv_len) range = rotate_chunk_f16(kt_s + off, kt_s + 16384 + off, c, sn, range);
-                rope_step(c, sn, dcs, dsn);
-            }
-            fence_proxy_async_smem();
-            mbar_arrive(smem_u32(&bars->k_ready));
-        }
+        // ================================================= staging WG ====
+        // q and K arrive rotated (FP16, workspace); this warpgroup stages each
+        // block's lse (log2 domain), delta and positions for the gradient warps
+        bool ok = true;
         for (int jj = 0; jj < nblk && ok; ++jj) {
             const int st = jj & 1;
             if (!(ok = mbar_wait(smem_u32(&bars->q_full[st]), (uint32_t)((jj >> 1) & 1), abort))) break;
@@ -309,28 +351,10 @@ __global__ void __launch_bounds__(BT_THREADS, 1)
                 const int pmin = __reduce_min_sync(0xffffffffu, pq);  // warp w holds columns 32 w .. 32 w + 31
                 if (lane == 0) reinterpret_cast<int*>(ld)[3 * BT_QB + warp] = pmin;
             }
-            // query rows g * rph + sl share position s0 + sl: exact angles per distinct position
-            uint8_t* qt = sm + BT_OFF_Q + st * BT_TILE;
-            for (int k = 0; k * 16 < rph; ++k) {
-                const int sl = r0 + 16 * k, s = s0 + sl;
-                const int p = s < a.Sq ? a.position_ids[(size_t)b * a.Sq + s] : 0;
-                float2 c[4], sn[4];
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    rope_cos_sin((uint32_t)p, bars->turns[8 * u + 2 * e], c[e].x, sn[e].x);
-                    rope_cos_sin((uint32_t)p, bars->turns[8 * u + 2 * e + 1], c[e].y, sn[e].y);
-                }
-                for (int g = 0; g < G; ++g) {
-                    const uint32_t off = sw128_off(g * rph + sl, u);
-                    const uint32_t nr = rotate_chunk_f16(qt + off, qt + 16384 + off, c, sn, range);
-                    if (s < a.Sq) range = nr;
-                }
-            }
-            fence_proxy_async_smem();
             mbar_arrive(smem_u32(&bars->q_ready[st]));
         }
-        if (range_exceeded(range)) bars->range_bad = 1;
-        named_bar_sync(1, 384);  // transform done: the range flag is final for the epilogue
+        named_bar_sync(1, 384);
+
         named_bar_sync(2, BT_THREADS);
     } else {
         asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(BT_REG_GRAD));
@@ -411,11 +435,11 @@ __global__ void __launch_bounds__(BT_THREADS, 1)
         }
         if (ok) ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&bars->done), 0, abort));
         tc_fence_after();
-        if (ok && hsel == 0) {  // a dS beyond the FP16 range (rounded to infinity) leaves dK' non-finite
+        if (ok) {  // an operand or dS beyond the FP16 range (infinity) leaves dK' / dV non-finite
 #pragma unroll 1
             for (int c4 = 0; c4 < 4; ++c4) {
                 uint32_t v[32];
-                tmem_ld32(tmem + lane_addr + 384 + 32 * c4, v);
+                tmem_ld32(tmem + lane_addr + (hsel ? 256 : 384) + 32 * c4, v);
                 tmem_ld_wait();
 #pragma unroll
                 for (int k = 0; k < 32; ++k) over |= !isfinite(__uint_as_float(v[k]));
@@ -484,18 +508,22 @@ __global__ void __launch_bounds__(BT_THREADS, 1)
 //   dQ' += dS K'   (dS written back over S as the A operand, K' read MN-major),
 // and at the end dq = R(p)^T (scale dQ').  delta = rowsum(dout * out) of the
 // tile's rows is formed first (from the staged dout tile and out) and written
-// for the dk / dv kernel.  TMEM: S [0,128), dP [128,256), dQ' [256,384).
+// for the dk / dv kernel.  TMEM: S0 [0,128), S1 [128,256), dP [256,384),
+// dQ' [384,512): S(i + 1) goes into the other S buffer while the gradient of
+// tile i runs, so the tensor pipe does not wait for it.  Three K stages (K(i)
+// is read by S(i) and dQ'(i), K(i + 1) by S(i + 1) meanwhile), two V stages.
+constexpr int DT_KST = 3, DT_VST = 2;
 constexpr int DT_OFF_Q = 0;
 constexpr int DT_OFF_DO = DT_OFF_Q + BT_TILE;
-constexpr int DT_OFF_K = DT_OFF_DO + BT_TILE;      // two stages
-constexpr int DT_OFF_V = DT_OFF_K + 2 * BT_TILE;   // two stages
-constexpr int DT_OFF_BAR = DT_OFF_V + 2 * BT_TILE;
+constexpr int DT_OFF_K = DT_OFF_DO + BT_TILE;
+constexpr int DT_OFF_V = DT_OFF_K + DT_KST * BT_TILE;
+constexpr int DT_OFF_BAR = DT_OFF_V + DT_VST * BT_TILE;
 constexpr int DT_SMEM = DT_OFF_BAR + BT_CTRL_BYTES;
 static_assert(DT_SMEM <= 232448, "shared memory above the 227 KiB opt-in limit");
 
 struct DqBars {
-    uint64_t q_full, q_ready;
-    uint64_t k_full[2], k_ready[2], v_full[2], kv_empty[2];
+    uint64_t q_full;
+    uint64_t k_full[DT_KST], k_empty[DT_KST], v_full[DT_VST], v_empty[DT_VST];
     uint64_t s_full, p_ready, done;
     uint32_t tmem_base;
     int abort;
@@ -533,12 +561,13 @@ __global__ void __launch_bounds__(BT_THREADS, 1)
         bars->abort = 0;
         bars->range_bad = 0;
         mbar_init(smem_u32(&bars->q_full), 1);
-        mbar_init(smem_u32(&bars->q_ready), 128);
-        for (int j = 0; j < 2; ++j) {
+        for (int j = 0; j < DT_KST; ++j) {
             mbar_init(smem_u32(&bars->k_full[j]), 1);
-            mbar_init(smem_u32(&bars->k_ready[j]), 128);
+            mbar_init(smem_u32(&bars->k_empty[j]), 1);
+        }
+        for (int j = 0; j < DT_VST; ++j) {
             mbar_init(smem_u32(&bars->v_full[j]), 1);
-            mbar_init(smem_u32(&bars->kv_empty[j]), 1);
+            mbar_init(smem_u32(&bars->v_empty[j]), 1);
         }
         mbar_init(smem_u32(&bars->s_full), 1);
         mbar_init(smem_u32(&bars->p_ready), 256);
@@ -611,13 +640,14 @@ __global__ void __launch_bounds__(BT_THREADS, 1)
             tma_load_4d(s_base + DT_OFF_DO + 16384, &omap, qb, 64, s0, kvh * G, b);
             int issued = 0;
             for (int i = 0; i < n_tiles; ++i) {
-                const int st = i & 1;
-                if (!mbar_wait(smem_u32(&bars->kv_empty[0]) + 8 * st, ((((uint32_t)i >> 1) & 1u) ^ 1u), abort)) break;
+                const int ks = i % DT_KST, vs = i % DT_VST;
+                if (!mbar_wait(smem_u32(&bars->k_empty[ks]), (((uint32_t)(i / DT_KST)) & 1u) ^ 1u, abort)) break;
+                if (!mbar_wait(smem_u32(&bars->v_empty[vs]), (((uint32_t)(i / DT_VST)) & 1u) ^ 1u, abort)) break;
                 const int np = min(BT_KEYS / PAGE, (n_keys + PAGE - 1) / PAGE - i * (BT_KEYS / PAGE));
-                const uint32_t kb = smem_u32(&bars->k_full[0]) + 8 * st, vb = smem_u32(&bars->v_full[0]) + 8 * st;
+                const uint32_t kb = smem_u32(&bars->k_full[ks]), vb = smem_u32(&bars->v_full[vs]);
                 mbar_arrive_expect_tx(kb, (uint32_t)np * 2 * 2048);
                 mbar_arrive_expect_tx(vb, (uint32_t)np * 2 * 2048);
-                const uint32_t kt = s_base + DT_OFF_K + st * BT_TILE, vt = s_base + DT_OFF_V + st * BT_TILE;
+                const uint32_t kt = s_base + DT_OFF_K + ks * BT_TILE, vt = s_base + DT_OFF_V + vs * BT_TILE;
                 for (int p = 0; p < np; ++p) {
                     const int pg = __ldg(bt + i * (BT_KEYS / PAGE) + p);
                     tma_load_3d(kt + p * 2048, &kmap, kb, 0, kvh, pg * PAGE);
@@ -629,10 +659,10 @@ __global__ void __launch_bounds__(BT_THREADS, 1)
             }
             if (*abort) {
                 mbar_wait_drain(qb, 0);
-                for (int i = max(0, issued - 2); i < issued; ++i) {
-                    mbar_wait_drain(smem_u32(&bars->k_full[i & 1]), (uint32_t)((i >> 1) & 1));
-                    mbar_wait_drain(smem_u32(&bars->v_full[i & 1]), (uint32_t)((i >> 1) & 1));
-                }
+                for (int i = max(0, issued - DT_KST); i < issued; ++i)
+                    mbar_wait_drain(smem_u32(&bars->k_full[i % DT_KST]), (uint32_t)((i / DT_KST) & 1));
+                for (int i = max(0, issued - DT_VST); i < issued; ++i)
+                    mbar_wait_drain(smem_u32(&bars->v_full[i % DT_VST]), (uint32_t)((i / DT_VST) & 1));
             }
         } else if (warp == WARP_MMA && lane == 0) {
             // ================================================= MMA issuer ====
@@ -641,21 +671,32 @@ __global__ void __launch_bounds__(BT_THREADS, 1)
             const uint32_t idQ = (1u << 4) | (1u << 16) | ((uint32_t)(HEAD_DIM >> 3) << 17) |
                                  ((uint32_t)(BT_QB >> 4) << 24);
             const uint32_t dQa = desc_lo(s_base + DT_OFF_Q, 16), dOa = desc_lo(s_base + DT_OFF_DO, 16);
-            bool ok = mbar_wait(smem_u32(&bars->q_ready), 0, abort);
-            for (int i = 0; i < n_tiles && ok; ++i) {
-                const int st = i & 1;
-                const uint32_t par = (uint32_t)((i >> 1) & 1);
-                if (!(ok = mbar_wait(smem_u32(&bars->k_ready[st]), par, abort))) break;
-                if (!(ok = mbar_wait(smem_u32(&bars->v_full[st]), par, abort))) break;
+            // pipe order: S(0), dP(0), S(1), dQ'(0), dP(1), S(2), dQ'(1), ...
+            bool ok = mbar_wait(smem_u32(&bars->q_full), 0, abort) && mbar_wait(smem_u32(&bars->k_full[0]), 0, abort);
+            if (ok) {
                 tc_fence_after();
-                const uint32_t kt = s_base + DT_OFF_K + st * BT_TILE, vt = s_base + DT_OFF_V + st * BT_TILE;
-                mma_ss_steps<0, 8, K_MAJOR_128, K_MAJOR_128>(tmem, dQa, desc_lo(kt, 16), idS, 0u);
-                mma_ss_steps<0, 8, K_MAJOR_128, K_MAJOR_128>(tmem + 128, dOa, desc_lo(vt, 16), idP, 0u);
-                umma_commit(smem_u32(&bars->s_full));
+                mma_ss_steps<0, 8, K_MAJOR_128, K_MAJOR_128>(tmem, dQa, desc_lo(s_base + DT_OFF_K, 16), idS, 0u);
+            }
+            for (int i = 0; i < n_tiles && ok; ++i) {
+                const int ks = i % DT_KST, vs = i % DT_VST;
+                if (!(ok = mbar_wait(smem_u32(&bars->v_full[vs]), (uint32_t)((i / DT_VST) & 1), abort))) break;
+                tc_fence_after();
+                mma_ss_steps<0, 8, K_MAJOR_128, K_MAJOR_128>(tmem + 256, dOa, desc_lo(s_base + DT_OFF_V + vs * BT_TILE, 16),
+                                                             idP, 0u);
+                umma_commit(smem_u32(&bars->s_full));        // S(i) and dP(i)
+                umma_commit(smem_u32(&bars->v_empty[vs]));   // V(i) read
+                if (i + 1 < n_tiles) {  // S(i + 1) into the other S buffer while the gradient of tile i runs
+                    const int k1 = (i + 1) % DT_KST;
+                    if (!(ok = mbar_wait(smem_u32(&bars->k_full[k1]), (uint32_t)(((i + 1) / DT_KST) & 1), abort))) break;
+                    tc_fence_after();
+                    mma_ss_steps<0, 8, K_MAJOR_128, K_MAJOR_128>(tmem + 128 * ((i + 1) & 1), dQa,
+                                                                 desc_lo(s_base + DT_OFF_K + k1 * BT_TILE, 16), idS, 0u);
+                }
                 if (!(ok = mbar_wait(smem_u32(&bars->p_ready), (uint32_t)(i & 1), abort))) break;
                 tc_fence_after();
-                mma_ts_split<0, MN_MAJOR>(tmem + 256, tmem, desc_lo(kt, 16384), idQ, i > 0 ? 1u : 0u);
-                umma_commit(smem_u32(&bars->kv_empty[st]));  // K'(i) and V(i) read
+                mma_ts_split<0, MN_MAJOR>(tmem + 384, tmem + 128 * (i & 1),
+                                          desc_lo(s_base + DT_OFF_K + ks * BT_TILE, 16384), idQ, i > 0 ? 1u : 0u);
+                umma_commit(smem_u32(&bars->k_empty[ks]));  // K'(i) read by S(i) and dQ'(i)
             }
             if (ok) {
                 umma_commit(smem_u32(&bars->done));
@@ -669,56 +710,7 @@ __global__ void __launch_bounds__(BT_THREADS, 1)
         named_bar_sync(2, BT_THREADS);
     } else if (wg == 0) {
         asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(BT_REG_XFORM));
-        // ================================================== transform WG ====
-        uint32_t range = 0;
-        const int u = tid & 7, r0 = tid >> 3;
-        bool ok = mbar_wait(smem_u32(&bars->q_full), 0, abort);
-        if (ok) {  // query rows g * rph + sl at position s0 + sl: exact angles per distinct position
-            uint8_t* qs = sm + DT_OFF_Q;
-            for (int k = 0; k * 16 < rph; ++k) {
-                const int sl = r0 + 16 * k, s = s0 + sl;
-                const int p = s < a.Sq ? pos_row[s] : 0;
-                float2 c[4], sn[4];
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    rope_cos_sin((uint32_t)p, bars->turns[8 * u + 2 * e], c[e].x, sn[e].x);
-                    rope_cos_sin((uint32_t)p, bars->turns[8 * u + 2 * e + 1], c[e].y, sn[e].y);
-                }
-                for (int g = 0; g < G; ++g) {
-                    const uint32_t off = sw128_off(g * rph + sl, u);
-                    const uint32_t nr = rotate_chunk_f16(qs + off, qs + 16384 + off, c, sn, range);
-                    if (s < a.Sq) range = nr;
-                }
-            }
-            fence_proxy_async_smem();
-            mbar_arrive(smem_u32(&bars->q_ready));
-        }
-        // key tiles: positions t0 + r, exact angles at r0 and 16-position steps
-        for (int i = 0; i < n_tiles && ok; ++i) {
-            const int st = i & 1;
-            if (!(ok = mbar_wait(smem_u32(&bars->k_full[st]), (uint32_t)((i >> 1) & 1), abort))) break;
-            uint8_t* kt_s = sm + DT_OFF_K + st * BT_TILE;
-            const int t0 = i * BT_KEYS;
-            float2 c[4], sn[4], dcs[4], dsn[4];
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                rope_cos_sin((uint32_t)(t0 + r0), bars->turns[8 * u + 2 * e], c[e].x, sn[e].x);
-                rope_cos_sin((uint32_t)(t0 + r0), bars->turns[8 * u + 2 * e + 1], c[e].y, sn[e].y);
-                const float2 s0v = bars->step16[8 * u + 2 * e], s1v = bars->step16[8 * u + 2 * e + 1];
-                dcs[e] = make_float2(s0v.x, s1v.x);
-                dsn[e] = make_float2(s0v.y, s1v.y);
-            }
-#pragma unroll 2
-            for (int m = 0; m < 8; ++m) {
-                const int r = r0 + 16 * m;
-                const uint32_t off = sw128_off(r, u);
-                if (t0 + r < n_keys) range = rotate_chunk_f16(kt_s + off, kt_s + 16384 + off, c, sn, range);
-                rope_step(c, sn, dcs, dsn);
-            }
-            fence_proxy_async_smem();
-            mbar_arrive(smem_u32(&bars->k_ready[st]));
-        }
-        if (range_exceeded(range)) bars->range_bad = 1;
+        // q and K arrive rotated (FP16, workspace): this warpgroup has no work
         named_bar_sync(1, 384);
         named_bar_sync(2, BT_THREADS);
     } else {
@@ -764,12 +756,13 @@ __global__ void __launch_bounds__(BT_THREADS, 1)
             if (!(ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&bars->s_full), (uint32_t)(i & 1), abort)))) break;
             tc_fence_after();
             const int tb = i * BT_KEYS;
+            const uint32_t sbuf = 128u * (uint32_t)(i & 1);  // this tile's S buffer
 #pragma unroll 1
             for (int h = 0; h < 2; ++h) {
                 const int cb = c0 + 32 * h;
                 uint32_t xs[32], xd[32];
-                tmem_ld32(tmem + lane_addr + cb, xs);
-                tmem_ld32(tmem + lane_addr + 128 + cb, xd);
+                tmem_ld32(tmem + lane_addr + sbuf + cb, xs);
+                tmem_ld32(tmem + lane_addr + 256 + cb, xd);
                 tmem_ld_wait();
                 // every key of these 32 columns visible to every row of the warp: no masks
                 if (__all_sync(0xffffffffu, tb + cb + 31 <= p && tb + cb + 31 < kv_len)) {
@@ -795,7 +788,7 @@ __global__ void __launch_bounds__(BT_THREADS, 1)
                         xs[c >> 1] = pack_f16x2(ds[0], ds[1]);
                     }
                 }
-                tmem_st16(tmem + lane_addr + c0 + 16 * h, *reinterpret_cast<uint32_t(*)[16]>(&xs[0]));
+                tmem_st16(tmem + lane_addr + sbuf + c0 + 16 * h, *reinterpret_cast<uint32_t(*)[16]>(&xs[0]));
             }
             tmem_st_wait();
             tc_fence_before();
@@ -808,8 +801,8 @@ __global__ void __launch_bounds__(BT_THREADS, 1)
         // A dS beyond the FP16 range (rounded to infinity) leaves dQ' non-finite.
         uint32_t lo[32], hi[32];
         if (ok) {  // warp-uniform; every lane loads
-            tmem_ld32(tmem + lane_addr + 256 + 32 * hsel, lo);
-            tmem_ld32(tmem + lane_addr + 256 + 64 + 32 * hsel, hi);
+            tmem_ld32(tmem + lane_addr + 384 + 32 * hsel, lo);
+            tmem_ld32(tmem + lane_addr + 384 + 64 + 32 * hsel, hi);
             tmem_ld_wait();
 #pragma unroll
             for (int k = 0; k < 32; ++k) over |= !isfinite(__uint_as_float(lo[k])) || !isfinite(__uint_as_float(hi[k]));
@@ -889,6 +882,21 @@ cudaError_t launch_backward_dq_tc(const CUtensorMap& qm, const CUtensorMap& om, 
     if (grid <= 0) return cudaSuccess;
     if (grid > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
     attn_bwd_dq_tc_kernel<<<(unsigned)grid, BT_THREADS, DT_SMEM, stream>>>(qm, om, km, vm, a);
+    return cudaGetLastError();
+}
+
+}  // namespace rk
+
+namespace rk {
+
+cudaError_t launch_backward_rotate(const BackwardArgs& a, cudaStream_t stream) {
+    const long long nq = (long long)a.B * a.Hq * a.Sq * 8, nk = (long long)a.B * a.W * PAGE * a.Hkv * 8;
+    const int grid_q = (int)std::min<long long>((nq + 255) / 256, 152 * 16);
+    const int grid_k = (int)std::min<long long>((nk + 255) / 256, 152 * 16);
+    if (grid_q > 0) rotate_q_kernel<<<grid_q, 256, 0, stream>>>(a);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    if (grid_k > 0 && a.num_pages > 0) rotate_k_kernel<<<grid_k, 256, 0, stream>>>(a);
     return cudaGetLastError();
 }
 

@@ -28,6 +28,7 @@ cudaError_t launch_backward_dkdv_tc(const CUtensorMap& qm, const CUtensorMap& om
                                     const CUtensorMap& vm, const BackwardArgs& a, cudaStream_t stream);
 cudaError_t launch_backward_dq_tc(const CUtensorMap& qm, const CUtensorMap& om, const CUtensorMap& km,
                                   const CUtensorMap& vm, const BackwardArgs& a, cudaStream_t stream);
+cudaError_t launch_backward_rotate(const BackwardArgs& a, cudaStream_t stream);
 }  // namespace rk
 
 namespace {
@@ -600,20 +601,50 @@ int rk_paged_attn_prefill(const rk_paged_plan_t* plan, const void* q, const void
     return RK_OK;
 }
 
+}  // extern "C"
+
+namespace {
+
+// Workspace of the prefill backward: RoPE-rotated q and K pages (FP16) and
+// delta (FP32), each 256-byte aligned.
+int64_t backward_ws_q(const rk_paged_plan_t* p) { return (int64_t)p->B * p->Hq * p->Sq * rk::HEAD_DIM * 2; }
+int64_t backward_ws_k(const rk_paged_plan_t* p) {
+    return (int64_t)p->num_pages * rk::PAGE * p->Hkv * rk::HEAD_DIM * 2;
+}
+int64_t align256(int64_t x) { return (x + 255) & ~(int64_t)255; }
+int64_t backward_ws_need(const rk_paged_plan_t* p) {
+    return align256(backward_ws_q(p)) + align256(backward_ws_k(p)) + align256((int64_t)p->B * p->Hq * p->Sq * 4);
+}
+
+}  // namespace
+
+extern "C" {
+
+int rk_paged_prefill_backward_workspace_bytes(const rk_paged_plan_t* plan, uint64_t* bytes) {
+    g_err.clear();
+    if (!plan || !bytes) return fail(RK_E_ARG, "plan and bytes must be non-null");
+    if (plan->abi != RK_PAGED_ABI_VERSION) return fail(RK_E_ARG, "plan ABI %u != %u", plan->abi, RK_PAGED_ABI_VERSION);
+    *bytes = (uint64_t)backward_ws_need(plan);
+    return RK_OK;
+}
+
 int rk_paged_attn_prefill_backward(const rk_paged_plan_t* plan, const void* q, const void* k_cache,
                                    const void* v_cache, const int32_t* block_table_d, const int32_t* kv_lens_d,
                                    const int32_t* position_ids_d, const void* out, const float* lse,
-                                   const void* dout, float* dq, float* dk_cache, float* dv_cache, float* delta,
-                                   int32_t* status_d, rk_stream_t stream) {
+                                   const void* dout, float* dq, float* dk_cache, float* dv_cache, void* workspace,
+                                   uint64_t workspace_bytes, int32_t* status_d, rk_stream_t stream) {
     g_err.clear();
     int rc = check_launch_common(plan, q, k_cache, v_cache, block_table_d, kv_lens_d, position_ids_d, out, lse);
     if (rc) return rc;
     if (plan->B == 0) return RK_OK;
-    if (!dout || !dq || !delta) return fail(RK_E_ARG, "dout, dq and delta must be non-null device pointers");
+    if (!dout || !dq || !workspace) return fail(RK_E_ARG, "dout, dq and workspace must be non-null device pointers");
     if (plan->num_pages > 0 && (!dk_cache || !dv_cache)) return fail(RK_E_ARG, "dk_cache / dv_cache is NULL");
     if (!aligned(dout, 16) || !aligned(dq, 16) || (dk_cache && !aligned(dk_cache, 16)) ||
-        (dv_cache && !aligned(dv_cache, 16)) || !aligned(delta, 4))
-        return fail(RK_E_ARG, "dout, dq, dk_cache and dv_cache must be 16-byte aligned, delta 4-byte aligned");
+        (dv_cache && !aligned(dv_cache, 16)) || !aligned(workspace, 256))
+        return fail(RK_E_ARG, "dout, dq, dk_cache and dv_cache must be 16-byte aligned, workspace 256-byte aligned");
+    if ((uint64_t)backward_ws_need(plan) > workspace_bytes)
+        return fail(RK_E_ARG, "backward workspace too small: %lld bytes needed, %llu given",
+                    (long long)backward_ws_need(plan), (unsigned long long)workspace_bytes);
     rk::BackwardArgs a;
     std::memset(&a, 0, sizeof a);
     a.q = q;
@@ -628,7 +659,10 @@ int rk_paged_attn_prefill_backward(const rk_paged_plan_t* plan, const void* q, c
     a.dq = dq;
     a.dk = dk_cache;
     a.dv = dv_cache;
-    a.delta = delta;
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    a.q_rot = ws;
+    a.k_rot = ws + align256(backward_ws_q(plan));
+    a.delta = reinterpret_cast<float*>(ws + align256(backward_ws_q(plan)) + align256(backward_ws_k(plan)));
     a.status = status_d;
     a.B = plan->B;
     a.Sq = plan->Sq;
@@ -651,18 +685,19 @@ int rk_paged_attn_prefill_backward(const rk_paged_plan_t* plan, const void* q, c
         const cuuint64_t strides[3] = {(cuuint64_t)rk::HEAD_DIM * 2, (cuuint64_t)plan->Sq * rk::HEAD_DIM * 2,
                                        (cuuint64_t)plan->Hq * plan->Sq * rk::HEAD_DIM * 2};
         const cuuint32_t box[4] = {64, (cuuint32_t)(rk::PF_BM / G), (cuuint32_t)G, 1};
-        if ((rc = make_map(&qm, q, 4, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B, "q"))) return rc;
+        if ((rc = make_map(&qm, a.q_rot, 4, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B, "rotated q"))) return rc;
         if ((rc = make_map(&om, dout, 4, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B, "dout"))) return rc;
     }
     const bool have = plan->num_pages > 0;
-    if ((rc = make_cache_map(&km, have ? k_cache : q, have ? plan->num_pages : 1, have ? plan->Hkv : 1, 64,
-                             CU_TENSOR_MAP_SWIZZLE_128B, "k_cache")))
+    if ((rc = make_cache_map(&km, have ? a.k_rot : q, have ? plan->num_pages : 1, have ? plan->Hkv : 1, 64,
+                             CU_TENSOR_MAP_SWIZZLE_128B, "rotated k")))
         return rc;
     if ((rc = make_cache_map(&vm, have ? v_cache : q, have ? plan->num_pages : 1, have ? plan->Hkv : 1, 64,
                              CU_TENSOR_MAP_SWIZZLE_128B, "v_cache")))
         return rc;
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-    cudaError_t e = rk::launch_backward_dq_tc(qm, om, km, vm, a, st);  // dq and delta
+    cudaError_t e = rk::launch_backward_rotate(a, st);                 // q and K rotated once
+    if (e == cudaSuccess) e = rk::launch_backward_dq_tc(qm, om, km, vm, a, st);  // dq and delta
     if (e == cudaSuccess) e = rk::launch_backward_dkdv_tc(qm, om, km, vm, a, st);
     if (e != cudaSuccess) return fail(RK_E_CUDA, "backward launch: %s", cudaGetErrorString(e));
     return RK_OK;

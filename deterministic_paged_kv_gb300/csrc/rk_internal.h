@@ -106,7 +106,9 @@ struct BackwardArgs {
     float* dq;
     float* dk;
     float* dv;
-    float* delta;
+    float* delta;                 // workspace: [B, Hq, Sq] fp32
+    void* q_rot;                  // workspace: RoPE-rotated q as FP16 [B, Hq, Sq, D]
+    void* k_rot;                  // workspace: RoPE-rotated K pages as FP16 [num_pages, 16, Hkv, D]
     int32_t* status;
     int32_t B, Sq, Hq, Hkv, G, W, num_pages;
     float sm_scale;

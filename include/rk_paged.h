@@ -338,24 +338,35 @@ int rk_paged_attn_ragged(const rk_paged_plan_t *plan, int32_t max_q_len, const i
  *                 entries are written in full (0 at slots past kv_len); no
  *                 other entry is touched.  Rows sharing a page (rejected by
  *                 rk_paged_plan) give unspecified values on it.
- *   delta         DEVICE fp32 [B, Hq, Sq], 4-byte aligned: caller-owned
- *                 workspace, left holding rowsum(dout * out).
+ *   workspace, workspace_bytes
+ *                 DEVICE, 256-byte aligned, at least
+ *                 rk_paged_prefill_backward_workspace_bytes bytes; caller-owned
+ *                 scratch: q and the rows' K pages rotated once (FP16), then
+ *                 delta = rowsum(dout * out) (FP32 [B, Hq, Sq]).
  * Deterministic and batch-invariant: every output element is accumulated by
  * one CTA in a fixed order (dq over key tiles ascending, dk / dv over query
  * blocks ascending), no atomics.  Arithmetic: FP32 accumulation on the
  * tcgen05 tensor cores (accumulators in TMEM); rotated q / k and dS rounded
- * to FP16, P to BF16 for the dV product.  Two launches on `stream` (dq with
- * delta, then dk / dv), no allocation, no host synchronisation.  Device status bits as the forward;
- * rows whose rotated operands or dS leave the FP16 range get NaN gradients
- * and RK_STATUS_RANGE.  Errors: as rk_paged_attn_prefill, plus RK_E_ARG for
- * a null or misaligned dout / dq / dk_cache / dv_cache / delta.
+ * to FP16, P to BF16 for the dV product.  Four launches on `stream` (the
+ * rotation of q and of the K pages, dq with delta, dk / dv), no allocation,
+ * no host synchronisation.  Device status bits as the forward;
+ * gradients a pre-RoPE element with |x| >= 2^15 or a dS beyond the FP16
+ * range enters come out NaN, with RK_STATUS_RANGE.  Errors: as
+ * rk_paged_attn_prefill, plus RK_E_ARG for a null or misaligned dout / dq /
+ * dk_cache / dv_cache / workspace or a workspace below the required size.
  */
 int rk_paged_attn_prefill_backward(const rk_paged_plan_t *plan, const void *q, const void *k_cache,
                                    const void *v_cache, const int32_t *block_table_d,
                                    const int32_t *kv_lens_d, const int32_t *position_ids_d,
                                    const void *out, const float *lse, const void *dout, float *dq,
-                                   float *dk_cache, float *dv_cache, float *delta, int32_t *status_d,
-                                   rk_stream_t stream);
+                                   float *dk_cache, float *dv_cache, void *workspace,
+                                   uint64_t workspace_bytes, int32_t *status_d, rk_stream_t stream);
+
+/* rk_paged_prefill_backward_workspace_bytes -- *bytes = the device workspace
+ * rk_paged_attn_prefill_backward needs for this plan (2 B Hq Sq D + 2
+ * num_pages 16 Hkv D + 4 B Hq Sq bytes, each part rounded up to 256).  Host
+ * only; RK_E_ARG for a null plan / bytes or a plan of another ABI. */
+int rk_paged_prefill_backward_workspace_bytes(const rk_paged_plan_t *plan, uint64_t *bytes);
 
 /* Message of the last failing call on this thread ("" if none).  The
  * pointer stays valid until the next library call on the same thread. */

@@ -46,9 +46,9 @@ def run_backward(w, dout, status=None, fill=float("nan")):
     dq = torch.full(w.q.shape, fill, dtype=torch.float32, device="cuda")
     dk = torch.full(w.k_cache.shape, fill, dtype=torch.float32, device="cuda")
     dv = torch.full(w.v_cache.shape, fill, dtype=torch.float32, device="cuda")
-    delta = torch.empty((w.B, w.Hq, w.Sq), dtype=torch.float32, device="cuda")
+    ws = torch.empty(binding.prefill_backward_workspace_bytes(p), dtype=torch.uint8, device="cuda")
     binding.attn_prefill_backward(p, d["q"], d["k_cache"], d["v_cache"], d["block_table"], d["kv_lens"],
-                                  d["position_ids"], out, lse, dout.cuda(), dq, dk, dv, delta, status=status)
+                                  d["position_ids"], out, lse, dout.cuda(), dq, dk, dv, ws, status=status)
     torch.cuda.synchronize()
     return dq.cpu(), dk.cpu(), dv.cpu()
 
@@ -138,9 +138,9 @@ def test_backward_flags_unsafe_page_and_writes_nothing_there():
     dq = torch.full(w.q.shape, float("nan"), dtype=torch.float32, device="cuda")
     dk = torch.full(w.k_cache.shape, float("nan"), dtype=torch.float32, device="cuda")
     dv = torch.full(w.v_cache.shape, float("nan"), dtype=torch.float32, device="cuda")
-    delta = torch.empty((w.B, w.Hq, w.Sq), dtype=torch.float32, device="cuda")
+    ws = torch.empty(binding.prefill_backward_workspace_bytes(p), dtype=torch.uint8, device="cuda")
     binding.attn_prefill_backward(p, d["q"], d["k_cache"], d["v_cache"], bt, d["kv_lens"], d["position_ids"],
-                                  out, lse, dout.cuda(), dq, dk, dv, delta, status=st)
+                                  out, lse, dout.cuda(), dq, dk, dv, ws, status=st)
     torch.cuda.synchronize()
     assert int(st.item()) & binding.STATUS_PAGE_OOB
     # row 0 is untouched by the bad entry: its gradients are the usual bits

@@ -237,3 +237,11 @@ def test_ragged_plan_counts_prefill_work_units(rk, Hq, Hkv, expect):
     # the count depends on qo_indptr alone: a shape-only ragged plan agrees
     p2, _ = rk.plan_ragged(w.B, q.shape[0], Hq, Hkv, 128, 16, w.num_pages, w.W, ind)
     assert p2.pf_units == expect and p2.validated == 0
+
+
+def test_backward_workspace_size_host_only(rk):
+    """rotated q (FP16) + rotated K pages (FP16) + delta (FP32), each rounded up to 256 bytes."""
+    p = rk.plan(2, 40, 32, 8, 128, 16, 10, 4)
+    r = lambda x: (x + 255) // 256 * 256
+    want = r(2 * 32 * 40 * 128 * 2) + r(10 * 16 * 8 * 128 * 2) + r(2 * 32 * 40 * 4)
+    assert rk.prefill_backward_workspace_bytes(p) == want
