@@ -84,6 +84,7 @@ def referenced_pages(w):
 CASES = {
     "full_prefill_200": dict(B=1, Sq=200, kv=[200], Hq=32, Hkv=8),
     "full_prefill_1000": dict(B=1, Sq=1000, kv=[1000], Hq=32, Hkv=8),
+    "full_prefill_2048": dict(B=1, Sq=2048, kv=[2048], Hq=32, Hkv=8),
     "chunks_300_170": dict(B=2, Sq=70, kv=[300, 170], Hq=32, Hkv=8),
     "mha_G1": dict(B=2, Sq=40, kv=[150, 77], Hq=8, Hkv=8),
     "gqa_G8": dict(B=2, Sq=40, kv=[150, 77], Hq=64, Hkv=8),
@@ -157,3 +158,43 @@ def test_backward_range_flag_gives_nan():
     dq, dk, dv = run_backward(w, dout, status=st)
     assert int(st.item()) & binding.STATUS_RANGE
     assert torch.isnan(dq[0, 3, 5]).all()
+
+
+def test_backward_graph_replay_with_new_contents():
+    """Captured once, replayed with new q / dout / cache contents of the same
+    shape: the same bits as an eager call on those contents."""
+    w = workloads.build("graph", 2, 48, 32, 8, 128, [200, 120], 24, 16, 241, "prefill")
+    p = binding.plan(w.B, w.Sq, w.Hq, w.Hkv, w.D, 16, w.num_pages, w.W)
+    d = to_dev(w)
+    out, lse = run_gpu(w, mode="prefill")
+    dout = _dout(w, 242).cuda()
+    dq = torch.empty(w.q.shape, dtype=torch.float32, device="cuda")
+    dk = torch.zeros(w.k_cache.shape, dtype=torch.float32, device="cuda")
+    dv = torch.zeros(w.v_cache.shape, dtype=torch.float32, device="cuda")
+    ws = torch.empty(binding.prefill_backward_workspace_bytes(p), dtype=torch.uint8, device="cuda")
+    call = lambda: binding.attn_prefill_backward(p, d["q"], d["k_cache"], d["v_cache"], d["block_table"],
+                                                 d["kv_lens"], d["position_ids"], out, lse, dout, dq, dk, dv, ws)
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        call()
+    torch.cuda.current_stream().wait_stream(s)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        call()
+    # new contents: another seed's q / caches / dout and their forward
+    w2 = workloads.build("graph2", 2, 48, 32, 8, 128, [200, 120], 24, 16, 243, "prefill")
+    w2.block_table, w2.position_ids, w2.kv_lens = w.block_table, w.position_ids, w.kv_lens
+    ref = run_backward(w2, _dout(w2, 244), fill=0.0)
+    o2, l2 = run_gpu(w2, mode="prefill")
+    d["q"].copy_(w2.q.cuda())
+    d["k_cache"].copy_(w2.k_cache.cuda())
+    d["v_cache"].copy_(w2.v_cache.cuda())
+    out.copy_(o2)
+    lse.copy_(l2)
+    dout.copy_(_dout(w2, 244).cuda())
+    g.replay()
+    torch.cuda.synchronize()
+    pages = torch.from_numpy(referenced_pages(w))
+    assert bitwise_equal(dq.cpu(), ref[0])
+    assert bitwise_equal(dk.cpu()[pages], ref[1][pages]) and bitwise_equal(dv.cpu()[pages], ref[2][pages])
