@@ -98,9 +98,11 @@ __device__ __forceinline__ void mma_ts_split(uint32_t d, uint32_t a_tmem, uint32
 
 // ---------------------------------------------------------- rotation ----
 // The backward reads every query block once per key tile and every key tile
-// once per query tile, so RoPE is applied once per call instead: q and the
-// pages of each row's keys are rotated (FP32 math, exact angles from the
-// fixed-point rates) and stored as FP16 in the caller's workspace.  A
+// once per query tile, so RoPE is applied once per call instead: q and each
+// row's keys are rotated (FP32 math, exact angles from the fixed-point rates)
+// and stored as FP16 in the caller's workspace, the keys (and a copy of V)
+// gathered from their pages into logical token order [B, Hkv, W * 16, D], so
+// that a 128-key tile is two 16 KiB copies instead of 16 page-sized ones.  A
 // pre-RoPE element with |x| >= 2^15 (whose rotation may leave the FP16 range)
 // is stored as infinity: the gradients it enters come out non-finite and are
 // reported as RK_STATUS_RANGE by the kernels below.
@@ -134,28 +136,33 @@ __global__ void __launch_bounds__(256) rotate_q_kernel(const __grid_constant__ B
     }
 }
 
-// one thread per (row, table entry, slot, KV head, chunk pair) of the keys a row
-// holds: k_rot[page, slot, kvh] = R(t) k_cache[page, slot, kvh], t = 16 entry + slot
-// (0 past kv_len); unsafe lengths or page ids are skipped (the kernels report them)
+// one thread per (row, KV head, token, chunk pair): k_lin[b, kvh, t] = R(t) K(b, t),
+// v_lin[b, kvh, t] = V(b, t) for t < kv_len, zeros up to W * 16; unsafe lengths
+// or page ids are skipped (the kernels report them)
 __global__ void __launch_bounds__(256) rotate_k_kernel(const __grid_constant__ BackwardArgs a) {
-    const long long per_row = (long long)a.W * PAGE * a.Hkv * 8;
+    const int T = a.W * PAGE;
+    const long long per_row = (long long)a.Hkv * T * 8;
     const long long n = (long long)a.B * per_row;
     for (long long it = (long long)blockIdx.x * blockDim.x + threadIdx.x; it < n; it += (long long)gridDim.x * blockDim.x) {
         const int b = (int)(it / per_row);
         const long long rem = it % per_row;
-        const int c = (int)(rem & 7), kvh = (int)((rem >> 3) % a.Hkv), t = (int)((rem >> 3) / a.Hkv);
+        const int c = (int)(rem & 7), t = (int)((rem >> 3) % T), kvh = (int)((rem >> 3) / T);
         const int kv_len = a.kv_lens[b];
-        if (kv_len < 0 || kv_len > a.W * PAGE || t >= (kv_len + PAGE - 1) / PAGE * PAGE) continue;
+        if (kv_len < 0 || kv_len > T) continue;
+        const size_t l = ((size_t)b * a.Hkv + kvh) * T + t;  // 256-byte linear row
+        uint4* kd = reinterpret_cast<uint4*>(a.k_lin) + l * 16;
+        uint4* vd = reinterpret_cast<uint4*>(a.v_lin) + l * 16;
+        if (t >= kv_len) {  // zeros: tiles read whole rows of 128 tokens, and 0 * NaN would not vanish
+            kd[c] = kd[c + 8] = vd[c] = vd[c + 8] = make_uint4(0, 0, 0, 0);
+            continue;
+        }
         const int pg = __ldg(a.block_table + (size_t)b * a.W + t / PAGE);
         if (pg < 0 || pg >= a.num_pages) continue;
-        const size_t e = ((size_t)pg * PAGE + t % PAGE) * a.Hkv + kvh;  // 256-byte row index
-        uint4* dst = reinterpret_cast<uint4*>(a.k_rot) + e * 16;
-        if (t < kv_len) {
-            rotate_store(reinterpret_cast<const uint4*>(a.k_cache) + e * 16, dst, c, t, a.rope_turns);
-        } else {
-            dst[c] = make_uint4(0, 0, 0, 0);
-            dst[c + 8] = make_uint4(0, 0, 0, 0);
-        }
+        const size_t e = ((size_t)pg * PAGE + t % PAGE) * a.Hkv + kvh;  // 256-byte cache row
+        rotate_store(reinterpret_cast<const uint4*>(a.k_cache) + e * 16, kd, c, t, a.rope_turns);
+        const uint4* vs = reinterpret_cast<const uint4*>(a.v_cache) + e * 16;
+        vd[c] = __ldg(vs + c);
+        vd[c + 8] = __ldg(vs + c + 8);
     }
 }
 
@@ -261,17 +268,15 @@ __global__ void __launch_bounds__(BT_THREADS, 1)
             prefetch_tmap(&vmap);
             prefetch_tmap(&qmap);
             prefetch_tmap(&omap);
-            // key and value tiles: two 16-token x 64-dim boxes per page (K-major tile layout)
+            // key and value tiles from the linear workspace: two 128-token x 64-dim boxes each
             const uint32_t kb = smem_u32(&bars->k_full), vb = smem_u32(&bars->v_full);
-            mbar_arrive_expect_tx(kb, (uint32_t)n_pg * 2 * 2048);
-            mbar_arrive_expect_tx(vb, (uint32_t)n_pg * 2 * 2048);
-            for (int p = 0; p < n_pg; ++p) {
-                const int pg = __ldg(bt + p);
-                tma_load_3d(s_base + BT_OFF_K + p * 2048, &kmap, kb, 0, kvh, pg * PAGE);
-                tma_load_3d(s_base + BT_OFF_K + 16384 + p * 2048, &kmap, kb, 64, kvh, pg * PAGE);
-                tma_load_3d(s_base + BT_OFF_V + p * 2048, &vmap, vb, 0, kvh, pg * PAGE);
-                tma_load_3d(s_base + BT_OFF_V + 16384 + p * 2048, &vmap, vb, 64, kvh, pg * PAGE);
-            }
+            const int lrow = b * a.Hkv + kvh;
+            mbar_arrive_expect_tx(kb, 2 * 16384);
+            mbar_arrive_expect_tx(vb, 2 * 16384);
+            tma_load_3d(s_base + BT_OFF_K, &kmap, kb, 0, t0, lrow);
+            tma_load_3d(s_base + BT_OFF_K + 16384, &kmap, kb, 64, t0, lrow);
+            tma_load_3d(s_base + BT_OFF_V, &vmap, vb, 0, t0, lrow);
+            tma_load_3d(s_base + BT_OFF_V + 16384, &vmap, vb, 64, t0, lrow);
             // query / dout blocks, two stages
             int issued = 0;
             const int h0 = kvh * G;
@@ -639,22 +644,21 @@ __global__ void __launch_bounds__(BT_THREADS, 1)
             tma_load_4d(s_base + DT_OFF_DO, &omap, qb, 0, s0, kvh * G, b);
             tma_load_4d(s_base + DT_OFF_DO + 16384, &omap, qb, 64, s0, kvh * G, b);
             int issued = 0;
+            const int lrow = b * a.Hkv + kvh;
             for (int i = 0; i < n_tiles; ++i) {
                 const int ks = i % DT_KST, vs = i % DT_VST;
                 if (!mbar_wait(smem_u32(&bars->k_empty[ks]), (((uint32_t)(i / DT_KST)) & 1u) ^ 1u, abort)) break;
                 if (!mbar_wait(smem_u32(&bars->v_empty[vs]), (((uint32_t)(i / DT_VST)) & 1u) ^ 1u, abort)) break;
-                const int np = min(BT_KEYS / PAGE, (n_keys + PAGE - 1) / PAGE - i * (BT_KEYS / PAGE));
                 const uint32_t kb = smem_u32(&bars->k_full[ks]), vb = smem_u32(&bars->v_full[vs]);
-                mbar_arrive_expect_tx(kb, (uint32_t)np * 2 * 2048);
-                mbar_arrive_expect_tx(vb, (uint32_t)np * 2 * 2048);
+                mbar_arrive_expect_tx(kb, 2 * 16384);
+                mbar_arrive_expect_tx(vb, 2 * 16384);
                 const uint32_t kt = s_base + DT_OFF_K + ks * BT_TILE, vt = s_base + DT_OFF_V + vs * BT_TILE;
-                for (int p = 0; p < np; ++p) {
-                    const int pg = __ldg(bt + i * (BT_KEYS / PAGE) + p);
-                    tma_load_3d(kt + p * 2048, &kmap, kb, 0, kvh, pg * PAGE);
-                    tma_load_3d(kt + 16384 + p * 2048, &kmap, kb, 64, kvh, pg * PAGE);
-                    tma_load_3d(vt + p * 2048, &vmap, vb, 0, kvh, pg * PAGE);
-                    tma_load_3d(vt + 16384 + p * 2048, &vmap, vb, 64, kvh, pg * PAGE);
-                }
+                // two 128-token x 64-dim boxes each from the linear workspace (tokens past the
+                // row's pages are zeros there; past the table, zero fill)
+                tma_load_3d(kt, &kmap, kb, 0, i * BT_KEYS, lrow);
+                tma_load_3d(kt + 16384, &kmap, kb, 64, i * BT_KEYS, lrow);
+                tma_load_3d(vt, &vmap, vb, 0, i * BT_KEYS, lrow);
+                tma_load_3d(vt + 16384, &vmap, vb, 64, i * BT_KEYS, lrow);
                 ++issued;
             }
             if (*abort) {
@@ -890,7 +894,7 @@ cudaError_t launch_backward_dq_tc(const CUtensorMap& qm, const CUtensorMap& om, 
 namespace rk {
 
 cudaError_t launch_backward_rotate(const BackwardArgs& a, cudaStream_t stream) {
-    const long long nq = (long long)a.B * a.Hq * a.Sq * 8, nk = (long long)a.B * a.W * PAGE * a.Hkv * 8;
+    const long long nq = (long long)a.B * a.Hq * a.Sq * 8, nk = (long long)a.B * a.Hkv * a.W * PAGE * 8;
     const int grid_q = (int)std::min<long long>((nq + 255) / 256, 152 * 16);
     const int grid_k = (int)std::min<long long>((nk + 255) / 256, 152 * 16);
     if (grid_q > 0) rotate_q_kernel<<<grid_q, 256, 0, stream>>>(a);

@@ -605,15 +605,16 @@ int rk_paged_attn_prefill(const rk_paged_plan_t* plan, const void* q, const void
 
 namespace {
 
-// Workspace of the prefill backward: RoPE-rotated q and K pages (FP16) and
-// delta (FP32), each 256-byte aligned.
+// Workspace of the prefill backward, each part 256-byte aligned: RoPE-rotated
+// q (FP16), rotated K and a copy of V in logical token order (FP16 / BF16
+// [B, Hkv, W * 16, D]), delta (FP32 [B, Hq, Sq]).
 int64_t backward_ws_q(const rk_paged_plan_t* p) { return (int64_t)p->B * p->Hq * p->Sq * rk::HEAD_DIM * 2; }
 int64_t backward_ws_k(const rk_paged_plan_t* p) {
-    return (int64_t)p->num_pages * rk::PAGE * p->Hkv * rk::HEAD_DIM * 2;
+    return (int64_t)p->B * p->Hkv * p->W * rk::PAGE * rk::HEAD_DIM * 2;
 }
 int64_t align256(int64_t x) { return (x + 255) & ~(int64_t)255; }
 int64_t backward_ws_need(const rk_paged_plan_t* p) {
-    return align256(backward_ws_q(p)) + align256(backward_ws_k(p)) + align256((int64_t)p->B * p->Hq * p->Sq * 4);
+    return align256(backward_ws_q(p)) + 2 * align256(backward_ws_k(p)) + align256((int64_t)p->B * p->Hq * p->Sq * 4);
 }
 
 }  // namespace
@@ -661,8 +662,9 @@ int rk_paged_attn_prefill_backward(const rk_paged_plan_t* plan, const void* q, c
     a.dv = dv_cache;
     uint8_t* ws = static_cast<uint8_t*>(workspace);
     a.q_rot = ws;
-    a.k_rot = ws + align256(backward_ws_q(plan));
-    a.delta = reinterpret_cast<float*>(ws + align256(backward_ws_q(plan)) + align256(backward_ws_k(plan)));
+    a.k_lin = ws + align256(backward_ws_q(plan));
+    a.v_lin = ws + align256(backward_ws_q(plan)) + align256(backward_ws_k(plan));
+    a.delta = reinterpret_cast<float*>(ws + align256(backward_ws_q(plan)) + 2 * align256(backward_ws_k(plan)));
     a.status = status_d;
     a.B = plan->B;
     a.Sq = plan->Sq;
@@ -688,13 +690,15 @@ int rk_paged_attn_prefill_backward(const rk_paged_plan_t* plan, const void* q, c
         if ((rc = make_map(&qm, a.q_rot, 4, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B, "rotated q"))) return rc;
         if ((rc = make_map(&om, dout, 4, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B, "dout"))) return rc;
     }
-    const bool have = plan->num_pages > 0;
-    if ((rc = make_cache_map(&km, have ? a.k_rot : q, have ? plan->num_pages : 1, have ? plan->Hkv : 1, 64,
-                             CU_TENSOR_MAP_SWIZZLE_128B, "rotated k")))
-        return rc;
-    if ((rc = make_cache_map(&vm, have ? v_cache : q, have ? plan->num_pages : 1, have ? plan->Hkv : 1, 64,
-                             CU_TENSOR_MAP_SWIZZLE_128B, "v_cache")))
-        return rc;
+    {  // rotated K and V in logical order: (d, token, row x KV head), box of 128 tokens x 64 dims
+        const int64_t T = (int64_t)plan->W * rk::PAGE;
+        const cuuint64_t dims[3] = {(cuuint64_t)rk::HEAD_DIM, (cuuint64_t)(T > 0 ? T : 1),
+                                    (cuuint64_t)plan->B * plan->Hkv};
+        const cuuint64_t strides[2] = {(cuuint64_t)rk::HEAD_DIM * 2, (cuuint64_t)(T > 0 ? T : 1) * rk::HEAD_DIM * 2};
+        const cuuint32_t box[3] = {64, 128, 1};
+        if ((rc = make_map(&km, a.k_lin, 3, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B, "rotated k"))) return rc;
+        if ((rc = make_map(&vm, a.v_lin, 3, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B, "linear v"))) return rc;
+    }
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     cudaError_t e = rk::launch_backward_rotate(a, st);                 // q and K rotated once
     if (e == cudaSuccess) e = rk::launch_backward_dq_tc(qm, om, km, vm, a, st);  // dq and delta

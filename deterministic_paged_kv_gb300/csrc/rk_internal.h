@@ -108,7 +108,8 @@ struct BackwardArgs {
     float* dv;
     float* delta;                 // workspace: [B, Hq, Sq] fp32
     void* q_rot;                  // workspace: RoPE-rotated q as FP16 [B, Hq, Sq, D]
-    void* k_rot;                  // workspace: RoPE-rotated K pages as FP16 [num_pages, 16, Hkv, D]
+    void* k_lin;                  // workspace: rotated K as FP16 [B, Hkv, W * 16, D], logical token order
+    void* v_lin;                  // workspace: V as BF16 [B, Hkv, W * 16, D], logical token order
     int32_t* status;
     int32_t B, Sq, Hq, Hkv, G, W, num_pages;
     float sm_scale;

@@ -341,8 +341,10 @@ int rk_paged_attn_ragged(const rk_paged_plan_t *plan, int32_t max_q_len, const i
  *   workspace, workspace_bytes
  *                 DEVICE, 256-byte aligned, at least
  *                 rk_paged_prefill_backward_workspace_bytes bytes; caller-owned
- *                 scratch: q and the rows' K pages rotated once (FP16), then
- *                 delta = rowsum(dout * out) (FP32 [B, Hq, Sq]).
+ *                 scratch: q rotated once (FP16), the rows' keys rotated and
+ *                 their values copied into logical token order (FP16 / BF16
+ *                 [B, Hkv, W * 16, D]), then delta = rowsum(dout * out) (FP32
+ *                 [B, Hq, Sq]).
  * Deterministic and batch-invariant: every output element is accumulated by
  * one CTA in a fixed order (dq over key tiles ascending, dk / dv over query
  * blocks ascending), no atomics.  Arithmetic: FP32 accumulation on the
@@ -363,9 +365,9 @@ int rk_paged_attn_prefill_backward(const rk_paged_plan_t *plan, const void *q, c
                                    uint64_t workspace_bytes, int32_t *status_d, rk_stream_t stream);
 
 /* rk_paged_prefill_backward_workspace_bytes -- *bytes = the device workspace
- * rk_paged_attn_prefill_backward needs for this plan (2 B Hq Sq D + 2
- * num_pages 16 Hkv D + 4 B Hq Sq bytes, each part rounded up to 256).  Host
- * only; RK_E_ARG for a null plan / bytes or a plan of another ABI. */
+ * rk_paged_attn_prefill_backward needs for this plan (2 B Hq Sq D + 2 x 2 B
+ * Hkv W 16 D + 4 B Hq Sq bytes, each part rounded up to 256).  Host only;
+ * RK_E_ARG for a null plan / bytes or a plan of another ABI. */
 int rk_paged_prefill_backward_workspace_bytes(const rk_paged_plan_t *plan, uint64_t *bytes);
 
 /* Message of the last failing call on this thread ("" if none).  The

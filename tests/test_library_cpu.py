@@ -240,8 +240,9 @@ def test_ragged_plan_counts_prefill_work_units(rk, Hq, Hkv, expect):
 
 
 def test_backward_workspace_size_host_only(rk):
-    """rotated q (FP16) + rotated K pages (FP16) + delta (FP32), each rounded up to 256 bytes."""
+    """rotated q (FP16) + rotated K and V in token order (2 x 2 B Hkv W 16 D) + delta (FP32),
+    each part rounded up to 256 bytes."""
     p = rk.plan(2, 40, 32, 8, 128, 16, 10, 4)
     r = lambda x: (x + 255) // 256 * 256
-    want = r(2 * 32 * 40 * 128 * 2) + r(10 * 16 * 8 * 128 * 2) + r(2 * 32 * 40 * 4)
+    want = r(2 * 32 * 40 * 128 * 2) + 2 * r(2 * 8 * 4 * 16 * 128 * 2) + r(2 * 32 * 40 * 4)
     assert rk.prefill_backward_workspace_bytes(p) == want
