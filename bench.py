@@ -510,7 +510,7 @@ def run_ours(args):
     dec_hash = source_hash("decode.cu", "rk_device.cuh", "rk_internal.h")
     roof = {"bound": "hbm", "achieved": step_bytes / (avg_launch_ms * 1e-3) / 1e9, "peak": hbm,
             "unit": "GB/s", "traffic": traffic_for("decode_kernel", dec_hash),
-            "kernel": "decode_kernel<4>", "peak_kind": peak_kind + " (copy bandwidth, burst)",
+            "kernel": "decode_kernel (one CTA per (row, KV head): 512 CTAs)", "peak_kind": peak_kind + " (copy bandwidth, burst)",
             "alg_bytes_per_launch": step_bytes}
     roof["frac"] = roof["achieved"] / roof["peak"]
 

@@ -106,6 +106,23 @@ def test_decode_batch_width_graph_invariance_bitwise():
     assert bitwise_equal(o3, go) and bitwise_equal(l3, gl)
 
 
+def test_decode_rows_in_a_multi_wave_batch_bitwise():
+    """The eight ragged invariance rows (partial last pages included) give the
+    same bits alone and repeated in a batch whose grid (8 CTAs a row) exceeds
+    the SM count, so that rows run in later waves next to other rows.
+    Repeated rows share pages, so the host plan (which rejects shared pages)
+    is skipped."""
+    w = workloads.decode_invariance(128)
+    out, lse = run_gpu(w)
+    n_sm = torch.cuda.get_device_properties(0).multi_processor_count
+    reps = (n_sm // (8 * 8)) + 2
+    big = workloads.select_rows(w, list(range(8)) * reps)
+    assert big.B * 8 > n_sm
+    o2, l2 = run_gpu(big, validate=False)
+    for r in range(reps):
+        assert bitwise_equal(out, o2[8 * r:8 * r + 8]) and bitwise_equal(lse, l2[8 * r:8 * r + 8]), r
+
+
 def test_decode_page_permutation_bitwise():
     w = workloads.decode_invariance(128)
     out, lse = run_gpu(w)
