@@ -236,19 +236,18 @@ def time_launches(fn, n, stream, flush=None):
     return out
 
 
-def measure_prefill(args, dev, stream, world, tf_burst, peak_kind):
-    """Time rk_paged_attn_prefill on the chunked-prefill workload (L2 flushed
-    between launches) and return the "prefill" object."""
+def time_prefill(args, w, dev, stream, world, tf_burst, peak_kind, n):
+    """Time rk_paged_attn_prefill on workload `w` (L2 flushed between
+    launches) and return its TFLOP/s object."""
     import torch
 
-    from deterministic_paged_kv_gb300 import binding, workloads
+    from deterministic_paged_kv_gb300 import binding
     names = ("q", "k_cache", "v_cache", "block_table", "kv_lens", "position_ids")
-    wp = workloads.prefill_chunk()
-    dp = {k: getattr(wp, k).to(dev) for k in names}
-    pp = binding.plan(wp.B, wp.Sq, wp.Hq, wp.Hkv, wp.D, 16, wp.num_pages, wp.W, wp.block_table,
-                      wp.kv_lens, wp.position_ids, wp.rope_theta, wp.rope_scale)
+    dp = {k: getattr(w, k).to(dev) for k in names}
+    pp = binding.plan(w.B, w.Sq, w.Hq, w.Hkv, w.D, 16, w.num_pages, w.W, w.block_table,
+                      w.kv_lens, w.position_ids, w.rope_theta, w.rope_scale)
     pout = torch.empty_like(dp["q"])
-    plse = torch.empty((wp.B, wp.Hq, wp.Sq), dtype=torch.float32, device=dev)
+    plse = torch.empty((w.B, w.Hq, w.Sq), dtype=torch.float32, device=dev)
 
     def pstep():
         binding.attn_prefill(pp, dp["q"], dp["k_cache"], dp["v_cache"], dp["block_table"],
@@ -258,22 +257,65 @@ def measure_prefill(args, dev, stream, world, tf_burst, peak_kind):
         pstep()
     torch.cuda.synchronize()
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)  # > 129 MB L2
-    pl = time_launches(pstep, max(10, args.steps), stream, flush=flush)
+    pl = time_launches(pstep, n, stream, flush=flush)
     p_ms = sum(pl) / len(pl)
-    pflops = prefill_alg_flops(wp)
+    pflops = prefill_alg_flops(w)
     pf_hash = source_hash("prefill.cu", "rk_device.cuh", "rk_internal.h")
-    prefill = {
+    obj = {
         "metric": "paged prefill TFLOP/s", "value": world * pflops / (p_ms * 1e-3) / 1e12,
         "unit": "TFLOP/s", "ms_per_launch": p_ms, "launches": len(pl),
-        "config": {"workload": wp.name + " page=16", "l2": "flushed (256 MB write) between launches",
+        "config": {"workload": w.name + " page=16", "l2": "flushed (256 MB write) between launches",
                    "flops": "4*D*visible_pairs*Hq = %.4g" % pflops},
         "roofline": {"bound": "tensor", "achieved": pflops / (p_ms * 1e-3) / 1e12, "peak": tf_burst,
                      "unit": "TFLOP/s", "traffic": traffic_for("prefill_kernel", pf_hash),
                      "kernel": "prefill_kernel", "peak_kind": peak_kind + " (bf16 dense, burst)"},
     }
-    prefill["roofline"]["frac"] = prefill["roofline"]["achieved"] / tf_burst
+    obj["roofline"]["frac"] = obj["roofline"]["achieved"] / tf_burst
+    return obj
 
-    return prefill
+
+def measure_prefill(args, dev, stream, world, tf_burst, peak_kind):
+    """The "prefill" object: the chunked-prefill workload."""
+    from deterministic_paged_kv_gb300 import workloads
+    return time_prefill(args, workloads.prefill_chunk(), dev, stream, world, tf_burst, peak_kind,
+                        max(10, args.steps))
+
+
+def measure_prefill_long(args, dev, stream, world, tf_burst, peak_kind):
+    """The "prefill_long" object: B=1, S=8192 full causal prefill (~0.5 ms a launch)."""
+    from deterministic_paged_kv_gb300 import workloads
+    obj = time_prefill(args, workloads.prefill_long(), dev, stream, world, tf_burst, peak_kind,
+                       max(5, min(args.steps, 20)))
+    obj["roofline"]["traffic"] = None  # the committed DRAM figure is the chunk workload's
+    return obj
+
+
+def measure_decode_graph(step, stream, n, step_bytes):
+    """The decode step captured once in a CUDA graph and replayed n times
+    back to back (inputs larger than L2): GB/s of the replays."""
+    import torch
+    s = torch.cuda.Stream()
+    s.wait_stream(stream)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(s):
+        step(s)  # warm the capture stream
+        with torch.cuda.graph(g, stream=s):
+            step(s)
+    stream.wait_stream(s)
+    for _ in range(3):
+        g.replay()
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    cur = torch.cuda.current_stream()
+    e0.record(cur)
+    for _ in range(n):
+        g.replay()
+    e1.record(cur)
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / n
+    return {"value": step_bytes / (ms * 1e-3) / 1e9, "unit": "GB/s", "ms_per_replay": ms, "replays": n,
+            "note": "one decode launch captured in a CUDA graph, replayed back to back"}
 
 
 def measure_backward(args, dev, stream, tf_burst, peak_kind):
@@ -481,9 +523,9 @@ def run_ours(args):
     out = torch.empty_like(d["q"])
     lse = torch.empty((w.B, w.Hq, 1), dtype=torch.float32, device=dev)
 
-    def step():
+    def step(st=None):
         binding.attn_decode(p, d["q"], d["k_cache"], d["v_cache"], d["block_table"], d["kv_lens"],
-                            d["position_ids"], out, lse, stream=stream)
+                            d["position_ids"], out, lse, stream=st or stream)
 
     for _ in range(args.warmup):
         step()
@@ -545,7 +587,10 @@ def run_ours(args):
                   if k not in ("k_cache", "v_cache"))
     d2h = h_out.numel() * 2 + h_lse.numel() * 4
 
+    dgraph = measure_decode_graph(step, stream, max(10, args.steps), step_bytes)
     prefill = None if args.no_prefill else measure_prefill(args, dev, stream, world, tf_burst, peak_kind)
+    plong = None if (args.no_prefill or args.no_long) else measure_prefill_long(args, dev, stream, world,
+                                                                                tf_burst, peak_kind)
     dlong = None if args.no_long else measure_decode_long(args, dev, stream, hbm, peak_kind)
     append = None if args.no_long else measure_append(args, dev, stream, hbm, peak_kind)
     ragged = None if args.no_long else measure_ragged(args, dev, stream)
@@ -577,7 +622,9 @@ def run_ours(args):
             "gpu_launches": args.steps + (0 if prefill is None else 0),
             "clocks": clocks,
             "wall_s_timed_region": wall,
+            "decode_graph": dgraph,
             "prefill": prefill,
+            "prefill_long": plong,
             "decode_long": dlong,
             "kv_append": append,
             "ragged_step": ragged,

@@ -10,16 +10,20 @@
 // One CTA per (row b, KV head); all G = Hq/Hkv query heads of the group are
 // served by one pass over the row's pages (GQA packing: every K/V byte is
 // read once).  The row's tokens are swept in ascending tiles of 128 (8 pages):
-//   warps 12 / 14 TMA producers: K pages (4-stage ring) as two 16-token x
-//                 64-dim boxes each, V pages (2-stage ring) as one 4 KiB box
-//                 each ([64-dim half][16 tokens], read by the PV MMA one page
-//                 per k-step), 128-byte swizzled, i.e. already in UMMA operand
-//                 layout; fewer, larger boxes keep more bytes in flight per SM
-//                 (the TMA unit holds a bounded number of boxes); the V
-//                 producer zeroes cache rows past kv_len in a partial last page;
-//   warps 0-7     transform: rotate each K row in FP32 (angles from an exact
-//                 fixed-point anchor plus 32-position steps) and store it as
-//                 FP16 in place; rotate the G query rows once (FP16 Q^T);
+//   warp 14       V producer: V pages (2-stage ring) by TMA, one 4 KiB box
+//                 per page ([64-dim half][16 tokens], 128-byte swizzled, read
+//                 by the PV MMA one page per k-step); zeroes cache rows past
+//                 kv_len in a partial last page;
+//   warps 0-7     transform: each thread copies the K chunks it will rotate
+//                 (its 4 token rows x 16 B of each 64-dim half) with 16-byte
+//                 cp.async, DEC_KAHEAD tiles ahead, straight into the
+//                 128-byte swizzled K-major tile of a 4-stage ring; then
+//                 rotates each K row in FP32 (angles from an exact fixed-point
+//                 anchor plus 32-position steps) and stores it as FP16 in
+//                 place; rotates the G query rows once (FP16 Q^T).  K through
+//                 the load/store path leaves the TMA unit to V: page boxes for
+//                 both cost the issuing warps ~1800-2000 cycles a tile, more
+//                 than the rest of the pipeline;
 //   warp 13       score MMA issuer: S^T = K Q^T (M = 128 tokens, N = 16 >= G
 //                 heads, FP16 operands, FP32 in TMEM, double-buffered);
 //   warp 15       PV MMA issuer: O^T += V^T P^T (M = 128 dims, N = 16, BF16,
@@ -63,11 +67,12 @@ constexpr int OFF_QT = OFF_V + DEC_VSTAGES * DEC_TILE_BYTES;  // Q^T: 16 rows x 
 constexpr int PT_BYTES = NH * DEC_BN * 2;                     // P^T: 16 rows x 128 tokens BF16
 constexpr int OFF_PT = OFF_QT + NH * HEAD_DIM * 2;            // two P^T buffers (tile parity)
 constexpr int OFF_CTRL = OFF_PT + 2 * PT_BYTES;
-static_assert(OFF_CTRL + DEC_CTRL_BYTES == DEC_SMEM_BYTES, "decode shared memory carve");
+constexpr int OFF_PGT = OFF_CTRL + DEC_CTRL_BYTES;             // page ids of the CTA's range
+static_assert(OFF_PGT + DEC_PGT_ENTRIES * 4 == DEC_SMEM_BYTES, "decode shared memory carve");
 
 struct DecCtrl {
     uint64_t q_ready;
-    uint64_t k_full[DEC_KSTAGES], k_ready[DEC_KSTAGES], k_empty[DEC_KSTAGES];
+    uint64_t k_ready[DEC_KSTAGES], k_empty[DEC_KSTAGES];
     uint64_t v_full[DEC_VSTAGES], v_empty[DEC_VSTAGES], v_tail;
     // per tile parity b: S^T buffer (s_full, s_free), P^T buffer (p_ready) and
     // the PV that read it (pv_done); a buffer is reused two tiles later, after
@@ -105,8 +110,7 @@ __device__ __forceinline__ void write_empty_row(const DecodeArgs& a, int b, int 
 }
 
 __global__ void __launch_bounds__(DEC_THREADS, 1)
-    decode_kernel(const __grid_constant__ CUtensorMap kmap, const __grid_constant__ CUtensorMap vmap,
-                  const __grid_constant__ DecodeArgs a) {
+    decode_kernel(const __grid_constant__ CUtensorMap vmap, const __grid_constant__ DecodeArgs a) {
     extern __shared__ __align__(1024) uint8_t sm[];
     // A launch that only reads what this grid reads (the prefill rows of a
     // ragged batch) may fill the SMs this grid's last wave leaves idle.
@@ -145,7 +149,7 @@ __global__ void __launch_bounds__(DEC_THREADS, 1)
     const int i0 = a.split_tiles > 0 ? split * a.split_tiles : 0;
     // The page ids of the CTA's part of the table are loaded before its length
     // is known (the metadata costs one round trip, not two) and judged against
-    // the visible range below; the producers' first page ids likewise.
+    // the visible range below.
     const int pg_lo = i0 * PPT;
     const int pg_cap = a.split_tiles > 0 ? min(a.W, (i0 + a.split_tiles) * PPT) : a.W;
     constexpr int PRE = 4;  // table entries per thread held from the early load
@@ -155,7 +159,6 @@ __global__ void __launch_bounds__(DEC_THREADS, 1)
         const int i = pg_lo + tid + e * DEC_THREADS;
         pre[e] = i < pg_cap ? __ldg(bt + i) : 0;
     }
-    const int first_pg = (lane < PPT && pg_lo + lane < a.W) ? __ldg(bt + pg_lo + lane) : 0;
     int bad = 0;
     if (kv_len < 0 || kv_len > a.W * PAGE) bad |= RK_STATUS_KVLEN;
     if (qpos < 0) bad |= RK_STATUS_POSITION;
@@ -179,12 +182,18 @@ __global__ void __launch_bounds__(DEC_THREADS, 1)
         const int pg = __ldg(bt + i);
         oob |= (pg < 0) | (pg >= a.num_pages);
     }
+    // Loads take page ids from a shared-memory copy of these entries, so no
+    // L2 round trip sits between consecutive tiles' copies; entries past the
+    // copy (rows of more than DEC_PGT_ENTRIES pages) come from the table.
+    int32_t* pgt = reinterpret_cast<int32_t*>(sm + OFF_PGT);
+    static_assert(PRE * DEC_THREADS == DEC_PGT_ENTRIES, "the early table load fills the page-id copy");
+#pragma unroll
+    for (int e = 0; e < PRE; ++e) pgt[tid + e * DEC_THREADS] = pre[e];
     if (tid == 0) {
         ctl->abort = 0;
         ctl->range_bad = 0;
         mbar_init(smem_u32(&ctl->q_ready), DEC_XFORM_THREADS);
         for (int k = 0; k < DEC_KSTAGES; ++k) {
-            mbar_init(smem_u32(&ctl->k_full[k]), 1);
             mbar_init(smem_u32(&ctl->k_ready[k]), DEC_XFORM_THREADS);
             mbar_init(smem_u32(&ctl->k_empty[k]), 1);
         }
@@ -236,43 +245,34 @@ __global__ void __launch_bounds__(DEC_THREADS, 1)
     const uint32_t tO = tmem + 32;
     volatile int* abort = &ctl->abort;
 
-    if (warp == WARP_TMA_K || warp == WARP_TMA_V) {
-        // ========================================== TMA producers ====
-        const bool is_k = warp == WARP_TMA_K;
-        const CUtensorMap* map = is_k ? &kmap : &vmap;
-        const int nst = is_k ? DEC_KSTAGES : DEC_VSTAGES;
-        if (lane == 0) prefetch_tmap(map);
+    if (warp == WARP_TMA_K) {
+        // K arrives through the transform threads' own copies: nothing to do.
+    } else if (warp == WARP_TMA_V) {
+        // ============================================ V producer (TMA) ====
+        if (lane == 0) prefetch_tmap(&vmap);
         int issued = 0;
-        int pg_next = first_pg;  // lanes past the tile's pages never use theirs
         // it: the CTA's own tile count (stages, phases); i: the row's tile index
         for (int it = 0; it < n_loc; ++it) {
             const int i = i0 + it;
-            const int k = it % nst;
-            const uint32_t use = (uint32_t)(it / nst);
+            const int k = it % DEC_VSTAGES;
+            const uint32_t use = (uint32_t)(it / DEC_VSTAGES);
             const int np = min(PPT, n_pages - i * PPT);
-            const int pg = pg_next;
-            const int nxt = (i + 1) * PPT + lane;  // the next tile's page ids, loaded ahead
-            pg_next = (it + 1 < n_loc && lane < PPT && nxt < n_pages) ? __ldg(bt + nxt) : 0;
-            const uint32_t eb = smem_u32(is_k ? &ctl->k_empty[k] : &ctl->v_empty[k]);
-            const uint32_t fb = smem_u32(is_k ? &ctl->k_full[k] : &ctl->v_full[k]);
+            const int li = it * PPT + lane;  // lane's page within the CTA's range
+            const int pg = lane >= np ? 0 : li < DEC_PGT_ENTRIES ? pgt[li] : __ldg(bt + pg_lo + li);
+            const uint32_t eb = smem_u32(&ctl->v_empty[k]);
+            const uint32_t fb = smem_u32(&ctl->v_full[k]);
             int good = 1;
             if (lane == 0) {
                 good = mbar_wait(eb, (use & 1u) ^ 1u, abort);
-                if (good) mbar_arrive_expect_tx(fb, (uint32_t)np * 2 * 2048);
+                if (good) mbar_arrive_expect_tx(fb, (uint32_t)np * 4096);
             }
             good = __shfl_sync(0xffffffffu, good, 0);
             if (!good) break;
-            if (lane < np) {
-                if (is_k) {  // two 16 x 64 boxes per page: the K-major tile layout
-                    const uint32_t t = s_base + OFF_K + k * DEC_TILE_BYTES + lane * 2048;
-                    tma_load_3d(t, map, fb, 0, kvh, pg * PAGE);
-                    tma_load_3d(t + 16384, map, fb, 64, kvh, pg * PAGE);
-                } else {     // one 4 KiB box per page: [page][half][16 rows][128 B]
-                    tma_load_4d(s_base + OFF_V + k * DEC_TILE_BYTES + lane * 4096, map, fb, 0, pg * PAGE, 0, kvh);
-                }
-            }
+            // one 4 KiB box per page: [page][half][16 rows][128 B]
+            if (lane < np)
+                tma_load_4d(s_base + OFF_V + k * DEC_TILE_BYTES + lane * 4096, &vmap, fb, 0, pg * PAGE, 0, kvh);
             __syncwarp();
-            if (!is_k && has_tail && it == n_loc - 1) {
+            if (has_tail && it == n_loc - 1) {
                 // this warp armed the phase it waits for: no parity aliasing
                 const int landed =
                     __shfl_sync(0xffffffffu, lane == 0 ? (int)mbar_wait(fb, use & 1u, abort) : 0, 0);
@@ -293,9 +293,8 @@ __global__ void __launch_bounds__(DEC_THREADS, 1)
             ++issued;
         }
         if (lane == 0 && *abort) {
-            for (int i = max(0, issued - nst); i < issued; ++i)
-                mbar_wait_drain(smem_u32(is_k ? &ctl->k_full[i % nst] : &ctl->v_full[i % nst]),
-                                (uint32_t)((i / nst) & 1));
+            for (int i = max(0, issued - DEC_VSTAGES); i < issued; ++i)
+                mbar_wait_drain(smem_u32(&ctl->v_full[i % DEC_VSTAGES]), (uint32_t)((i / DEC_VSTAGES) & 1));
         }
     } else if (warp == WARP_MMA || warp == WARP_PV) {
         // ============================================ MMA issuers ====
@@ -353,6 +352,43 @@ __global__ void __launch_bounds__(DEC_THREADS, 1)
         __syncwarp();
     } else if (warp < WARP_SOFTMAX0) {
         // ============================================= transform WGs ====
+        const int u = tid & 7, r0 = tid >> 3;  // rows r0 + XF_ROW_STEP * m
+        // K copies: the thread's rows r0 + 32 m lie on page (r0 / 16) + 2 m of
+        // a tile, row r0 % 16 of that page; chunk u of each 64-dim half.
+        const size_t row_bytes = (size_t)a.Hkv * HEAD_DIM * 2;
+        const char* ksrc = reinterpret_cast<const char*>(a.k_cache) +
+                           ((size_t)(r0 & (PAGE - 1)) * a.Hkv + kvh) * (HEAD_DIM * 2) + u * 16;
+        // Copy tile itx's chunks of this thread into ring slot itx % KSTAGES once
+        // the score MMA of its previous tile has retired; one commit group per
+        // tile (empty past the row's end), so group counts stay aligned.
+        auto issue_k = [&](int itx) -> bool {
+            bool ok_ = true;
+            if (itx < n_loc) {
+                const int kx = itx % DEC_KSTAGES;
+                ok_ = mbar_wait(smem_u32(&ctl->k_empty[kx]), (uint32_t)(((itx / DEC_KSTAGES) & 1) ^ 1), abort);
+                if (ok_) {
+                    const uint32_t kt_s = s_base + OFF_K + kx * DEC_TILE_BYTES;
+                    const int pages = n_pages - (i0 + itx) * PPT;  // pages of the tile on the row
+#pragma unroll
+                    for (int m = 0; m < XF_ROWS; ++m) {
+                        const int pit = (r0 >> 4) + 2 * m;
+                        if (pit < pages) {
+                            const int li = itx * PPT + pit;
+                            const int pg = li < DEC_PGT_ENTRIES ? pgt[li] : __ldg(bt + pg_lo + li);
+                            const char* src = ksrc + (size_t)pg * PAGE * row_bytes;
+                            const uint32_t off = sw128_off(r0 + XF_ROW_STEP * m, u);
+                            cp_async16(kt_s + off, src);
+                            cp_async16(kt_s + 16384 + off, src + 128);
+                        }
+                    }
+                }
+            }
+            cp_async_commit();
+            return ok_;
+        };
+        bool kok = true;
+#pragma unroll 1
+        for (int e = 0; e < DEC_KAHEAD && kok; ++e) kok = issue_k(e);
         uint32_t range = 0;
         {
             // Q^T: thread (h, u) rotates chunk pair u of query head h at qpos.
@@ -378,7 +414,6 @@ __global__ void __launch_bounds__(DEC_THREADS, 1)
             fence_proxy_async_smem();
             mbar_arrive(smem_u32(&ctl->q_ready));
         }
-        const int u = tid & 7, r0 = tid >> 3;  // rows r0 + XF_ROW_STEP * m
         float2 dcs[4], dsn[4];
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
@@ -391,9 +426,9 @@ __global__ void __launch_bounds__(DEC_THREADS, 1)
         // (a thread's rows are XF_ROW_STEP apart and the next tile continues the
         // sequence), so at most XF_ANCHOR_TILES * XF_ROWS steps follow an anchor.
         float2 c[4], sn[4];
-        for (int it = 0; it < n_loc; ++it) {
+        for (int it = 0; it < n_loc && kok; ++it) {
             const int i = i0 + it, k = it % DEC_KSTAGES;
-            if (!mbar_wait(smem_u32(&ctl->k_full[k]), (uint32_t)((it / DEC_KSTAGES) & 1), abort)) break;
+            cp_async_wait<DEC_KAHEAD - 1>();  // this thread's chunks of tile it have landed
             uint8_t* kt = sm + OFF_K + k * DEC_TILE_BYTES;
             const int t0 = i * DEC_BN;
             if (it == 0 || i % XF_ANCHOR_TILES == 0) {
@@ -424,9 +459,11 @@ __global__ void __launch_bounds__(DEC_THREADS, 1)
                 rope_step(c, sn, dcs, dsn);
             }
             if (range_exceeded(range)) ctl->range_bad = 1;
-            fence_proxy_async_smem();
+            fence_proxy_async_smem();  // rotated rows, and copied rows left as they are
             mbar_arrive(smem_u32(&ctl->k_ready[k]));
+            kok = issue_k(it + DEC_KAHEAD);
         }
+        cp_async_wait_all();  // no copy may land after the CTA has left
         named_bar_sync(2, DEC_XFORM_THREADS + 128);  // transform done: the range flag is final
     } else if (warp < WARP_SOFTMAX0 + 4) {
         // =============================================== softmax WG ====
@@ -627,8 +664,7 @@ __global__ void __launch_bounds__(HEAD_DIM) decode_merge_kernel(const __grid_con
 
 }  // namespace
 
-cudaError_t launch_decode(const CUtensorMap& km, const CUtensorMap& vm, const DecodeArgs& a,
-                          cudaStream_t stream) {
+cudaError_t launch_decode(const CUtensorMap& vm, const DecodeArgs& a, cudaStream_t stream) {
     static std::atomic<uint64_t> configured{0};  // one bit per device
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
@@ -642,7 +678,7 @@ cudaError_t launch_decode(const CUtensorMap& km, const CUtensorMap& vm, const De
     const long long grid = (long long)a.B * a.Hkv * (a.split_tiles > 0 ? a.n_splits : 1);
     if (grid <= 0) return cudaSuccess;
     if (grid > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
-    decode_kernel<<<(unsigned)grid, DEC_THREADS, DEC_SMEM_BYTES, stream>>>(km, vm, a);
+    decode_kernel<<<(unsigned)grid, DEC_THREADS, DEC_SMEM_BYTES, stream>>>(vm, a);
     e = cudaGetLastError();
     if (e != cudaSuccess || a.split_tiles <= 0) return e;
     decode_merge_kernel<<<(unsigned)((long long)a.B * a.Hq), HEAD_DIM, 0, stream>>>(a);

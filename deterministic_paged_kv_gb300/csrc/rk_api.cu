@@ -19,8 +19,7 @@
 #include "rk_paged.h"
 
 namespace rk {
-cudaError_t launch_decode(const CUtensorMap& km, const CUtensorMap& vm, const DecodeArgs& a,
-                          cudaStream_t stream);
+cudaError_t launch_decode(const CUtensorMap& vm, const DecodeArgs& a, cudaStream_t stream);
 cudaError_t launch_prefill(const CUtensorMap& qm, const CUtensorMap& km, const CUtensorMap& vm,
                            const PrefillArgs& a, cudaStream_t stream, bool overlap_previous = false);
 cudaError_t launch_kv_append(const AppendArgs& a, cudaStream_t stream);
@@ -385,15 +384,13 @@ int decode_common(const rk_paged_plan_t* plan, int32_t split_tokens, const void*
     }
     if (plan->B == 0) return RK_OK;
     const bool have = plan->num_pages > 0;
-    CUtensorMap km, vm;
-    if ((rc = make_cache_map(&km, have ? k_cache : q, have ? plan->num_pages : 1, have ? plan->Hkv : 1, 64,
-                             CU_TENSOR_MAP_SWIZZLE_128B, "k_cache")))
-        return rc;
+    CUtensorMap vm;
     if ((rc = make_page_map(&vm, have ? v_cache : q, have ? plan->num_pages : 1, have ? plan->Hkv : 1, "v_cache")))
         return rc;
     rk::DecodeArgs a;
     std::memset(&a, 0, sizeof a);
     a.q = q;
+    a.k_cache = k_cache;
     a.block_table = block_table_d;
     a.kv_lens = kv_lens_d;
     a.position_ids = position_ids_d;
@@ -415,7 +412,7 @@ int decode_common(const rk_paged_plan_t* plan, int32_t split_tokens, const void*
         a.lse_part = static_cast<float*>(scratch) + n * rk::HEAD_DIM;
     }
     std::memcpy(a.rope_turns, plan->rope_turns, sizeof a.rope_turns);
-    cudaError_t e = rk::launch_decode(km, vm, a, reinterpret_cast<cudaStream_t>(stream));
+    cudaError_t e = rk::launch_decode(vm, a, reinterpret_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return fail(RK_E_CUDA, "decode launch: %s", cudaGetErrorString(e));
     return RK_OK;
 }
@@ -726,16 +723,14 @@ int rk_paged_attn_ragged(const rk_paged_plan_t* plan, int32_t max_q_len, const i
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     // single-query rows: the decode kernel
     {
-        CUtensorMap km, vm;
-        if ((rc = make_cache_map(&km, have ? k_cache : q, have ? plan->num_pages : 1, have ? plan->Hkv : 1, 64,
-                                 CU_TENSOR_MAP_SWIZZLE_128B, "k_cache")))
-            return rc;
+        CUtensorMap vm;
         if ((rc = make_page_map(&vm, have ? v_cache : q, have ? plan->num_pages : 1, have ? plan->Hkv : 1,
                                 "v_cache")))
             return rc;
         rk::DecodeArgs a;
         std::memset(&a, 0, sizeof a);
         a.q = q;
+        a.k_cache = k_cache;
         a.block_table = block_table_d;
         a.kv_lens = kv_lens_d;
         a.position_ids = position_ids_d;
@@ -753,7 +748,7 @@ int rk_paged_attn_ragged(const rk_paged_plan_t* plan, int32_t max_q_len, const i
         a.total_q = total_q;
         a.max_q_len = max_q_len;
         std::memcpy(a.rope_turns, plan->rope_turns, sizeof a.rope_turns);
-        cudaError_t e = rk::launch_decode(km, vm, a, st);
+        cudaError_t e = rk::launch_decode(vm, a, st);
         if (e != cudaSuccess) return fail(RK_E_CUDA, "ragged decode launch: %s", cudaGetErrorString(e));
     }
     if (max_q_len < 2) return RK_OK;

@@ -158,6 +158,20 @@ __device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap* m, 
         : "memory");
 }
 
+// 16-byte asynchronous copy global -> shared through the load/store path,
+// cached in L2 only.  Completion is tracked per thread in commit groups; the
+// data lands in the generic proxy (fence before the tensor core reads it).
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+// Wait until at most N of this thread's committed groups are still in flight.
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+
 // Make generic-proxy writes to shared memory visible to the async proxy
 // (tensor core operand reads, TMA).
 __device__ __forceinline__ void fence_proxy_async_smem() {

@@ -22,12 +22,15 @@ constexpr int DEC_BN = 128;                           // tokens per KV tile (8 p
 constexpr int DEC_KSTAGES = 4;
 constexpr int DEC_VSTAGES = 2;
 constexpr int DEC_TILE_BYTES = DEC_BN * HEAD_DIM * 2;  // 32 KiB
+constexpr int DEC_KAHEAD = 3;                          // K tiles a transform thread keeps in flight
 constexpr int DEC_CTRL_BYTES = 2048;                   // barriers, RoPE tables, reductions
+constexpr int DEC_PGT_ENTRIES = 2048;                  // page ids of a CTA's range held in shared memory
 constexpr int DEC_SMEM_BYTES = (DEC_KSTAGES + DEC_VSTAGES) * DEC_TILE_BYTES + 16 * HEAD_DIM * 2 +
-                               2 * 16 * DEC_BN * 2 + DEC_CTRL_BYTES;
+                               2 * 16 * DEC_BN * 2 + DEC_CTRL_BYTES + DEC_PGT_ENTRIES * 4;
 
 struct DecodeArgs {
     const void* q;                // bf16 [B, Hq, 1, D]
+    const void* k_cache;          // bf16 [num_pages, 16, Hkv, D]
     const int32_t* block_table;   // [B, W]
     const int32_t* kv_lens;       // [B]
     const int32_t* position_ids;  // [B, 1]
