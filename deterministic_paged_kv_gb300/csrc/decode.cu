@@ -10,20 +10,23 @@
 // One CTA per (row b, KV head); all G = Hq/Hkv query heads of the group are
 // served by one pass over the row's pages (GQA packing: every K/V byte is
 // read once).  The row's tokens are swept in ascending tiles of 128 (8 pages):
-//   warp 14       V producer: V pages (2-stage ring) by TMA, one 4 KiB box
+//   warp 14       V producer: V pages (3-stage ring) by TMA, one 4 KiB box
 //                 per page ([64-dim half][16 tokens], 128-byte swizzled, read
 //                 by the PV MMA one page per k-step); zeroes cache rows past
 //                 kv_len in a partial last page;
 //   warps 0-7     transform: each thread copies the K chunks it will rotate
 //                 (its 4 token rows x 16 B of each 64-dim half) with 16-byte
 //                 cp.async, DEC_KAHEAD tiles ahead, straight into the
-//                 128-byte swizzled K-major tile of a 4-stage ring; then
+//                 128-byte swizzled K-major tile of a 3-stage ring; then
 //                 rotates each K row in FP32 (angles from an exact fixed-point
 //                 anchor plus 32-position steps) and stores it as FP16 in
 //                 place; rotates the G query rows once (FP16 Q^T).  K through
-//                 the load/store path leaves the TMA unit to V: page boxes for
-//                 both cost the issuing warps ~1800-2000 cycles a tile, more
-//                 than the rest of the pipeline;
+//                 the load/store path of eight warps leaves the TMA unit to V:
+//                 a warp's page boxes issue at ~20 B a cycle, so K and V boxes
+//                 took their producer warps ~1800-2000 cycles a tile, more than
+//                 the rest of the pipeline;
+//   warp 12       idle (one warp of cp.async producer could not keep enough
+//                 copies in flight);
 //   warp 13       score MMA issuer: S^T = K Q^T (M = 128 tokens, N = 16 >= G
 //                 heads, FP16 operands, FP32 in TMEM, double-buffered);
 //   warp 15       PV MMA issuer: O^T += V^T P^T (M = 128 dims, N = 16, BF16,

@@ -19,10 +19,10 @@ constexpr int ROPE_PAIRS = HEAD_DIM / 2;
 constexpr int DEC_XFORM_THREADS = 256;
 constexpr int DEC_THREADS = 16 * 32;
 constexpr int DEC_BN = 128;                           // tokens per KV tile (8 pages)
-constexpr int DEC_KSTAGES = 4;
-constexpr int DEC_VSTAGES = 2;
+constexpr int DEC_KSTAGES = 3;
+constexpr int DEC_VSTAGES = 3;
 constexpr int DEC_TILE_BYTES = DEC_BN * HEAD_DIM * 2;  // 32 KiB
-constexpr int DEC_KAHEAD = 3;                          // K tiles a transform thread keeps in flight
+constexpr int DEC_KAHEAD = 2;                          // K tiles a transform thread keeps in flight
 constexpr int DEC_CTRL_BYTES = 2048;                   // barriers, RoPE tables, reductions
 constexpr int DEC_PGT_ENTRIES = 2048;                  // page ids of a CTA's range held in shared memory
 constexpr int DEC_SMEM_BYTES = (DEC_KSTAGES + DEC_VSTAGES) * DEC_TILE_BYTES + 16 * HEAD_DIM * 2 +
