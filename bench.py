@@ -7,7 +7,10 @@ One step = one rk_paged_attn_decode call over the decode-throughput workload
 pages; 1.075 GB of algorithmic traffic, larger than L2, so no flush is needed
 between steps).  The same run also times rk_paged_attn_prefill on the chunked
 prefill workload (B=4, 1536-token prefix + 512-token chunk) with an L2 flush
-between launches, reported in the "prefill" object.
+between launches, reported in the "prefill" object, the long full-causal
+prefill (B=1, S=8192) in "prefill_long", the same decode step replayed from a
+CUDA graph in "decode_graph", and the decode_long, kv_append, ragged-step and
+prefill-backward objects.
 
 Multi-GPU (torchrun, one rank per GPU): replicas only -- every rank runs its
 own copy of the workload on its own GPU, there is no collective on the data
