@@ -154,6 +154,16 @@ def test_decode_long_context_parity():
     assert_parity(out, lse, ro, rl)
 
 
+def test_decode_row_wider_than_the_page_id_copy():
+    """A row of 40000 tokens (2500 pages): the kernel keeps the first 2048 page
+    ids of a CTA's range in shared memory and reads the rest from the table;
+    both halves of the row against the oracle, and in a batch with a short row."""
+    w = workloads.random_case(2, 1, 32, 8, 128, [40000, 333], seed=61, mode="decode")
+    out, lse = run_gpu(w)
+    ro, rl = oracle_ref(w)
+    assert_parity(out, lse, ro, rl)
+
+
 def test_decode_device_status_on_corrupt_metadata():
     """Unsafe device metadata: flagged in status, that row zeroed with NaN LSE,
     other rows untouched; no trap."""
