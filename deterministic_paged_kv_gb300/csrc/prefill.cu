@@ -15,8 +15,8 @@
 // setmaxnreg):
 //   warpgroup 0  transform: rotate both q-tiles once and each K tile in place
 //                in shared memory (FP32 math; angles from an exact fixed-point
-//                anchor plus 16-position angle-addition steps), store FP16 in
-//                the UMMA operand layout;
+//                anchor every 4 K tiles plus 16-position angle-addition steps),
+//                store FP16 in the UMMA operand layout;
 //   warpgroup 1  softmax for q-tile 0, warpgroup 2 softmax for q-tile 1: one
 //                thread per accumulator row reads its S row from TMEM, masks,
 //                runs the online softmax in the log2 domain (the running max
@@ -578,16 +578,22 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
             dcs[e] = make_float2(s0.x, s1.x);
             dsn[e] = make_float2(s0.y, s1.y);
         }
+        // Angles of the thread's next K row: an exact anchor every 4 tiles, 16-position
+        // steps in between (the rows r0 + 16 m of consecutive tiles continue one
+        // sequence), so at most 32 steps follow an anchor; anchoring every tile
+        // spent 8 sin / cos per thread and tile (about 1% of prefill_long).
+        float2 c[4], sn[4];
         for (int i = 0; i < n_tiles; ++i) {
             const int k = i % KSTAGES;
             if (!mbar_wait(smem_u32(&bars->k_full[k]), (uint32_t)((i / KSTAGES) & 1), abort)) break;
             uint8_t* kt = sm + OFF_K + k * PF_TILE_BYTES;
             const int t0 = i * PF_BN;
-            float2 c[4], sn[4];
+            if ((i & 3) == 0) {
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                rope_cos_sin((uint32_t)(t0 + r0), bars->turns[8 * u + 2 * e], c[e].x, sn[e].x);
-                rope_cos_sin((uint32_t)(t0 + r0), bars->turns[8 * u + 2 * e + 1], c[e].y, sn[e].y);
+                for (int e = 0; e < 4; ++e) {
+                    rope_cos_sin((uint32_t)(t0 + r0), bars->turns[8 * u + 2 * e], c[e].x, sn[e].x);
+                    rope_cos_sin((uint32_t)(t0 + r0), bars->turns[8 * u + 2 * e + 1], c[e].y, sn[e].y);
+                }
             }
 #pragma unroll 2
             for (int m = 0; m < 8; ++m) {
