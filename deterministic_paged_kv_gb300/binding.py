@@ -177,8 +177,42 @@ def _stream(stream):
     return stream.cuda_stream
 
 
+def _expect(t, shape, name):
+    """Raise ValueError unless tensor ``t`` has exactly ``shape``.  The C ABI
+    receives bare pointers and cannot see sizes, so a tensor smaller than the
+    plan says must be refused here, before anything is launched."""
+    if tuple(t.shape) != tuple(int(x) for x in shape):
+        raise ValueError("%s has shape %s, the plan needs %s" % (name, tuple(t.shape), tuple(shape)))
+
+
+def _check_common(p: Plan, k_cache, v_cache, block_table, kv_lens, status):
+    cache = (p.num_pages, p.page_size, p.Hkv, p.D)
+    _expect(k_cache, cache, "k_cache")
+    _expect(v_cache, cache, "v_cache")
+    _expect(block_table, (p.B, p.W), "block_table")
+    _expect(kv_lens, (p.B,), "kv_lens")
+    if status is not None and status.numel() < 1:
+        raise ValueError("status must hold at least one int32")
+
+
+def _check_shapes(p: Plan, q, k_cache, v_cache, block_table, kv_lens, position_ids, out, lse, status,
+                  ragged=False):
+    """Every tensor of a decode / prefill / ragged call against the plan's sizes
+    (ragged: q / out [total_q, Hq, D], lse [total_q, Hq], position_ids [total_q],
+    with total_q = plan.Sq)."""
+    _check_common(p, k_cache, v_cache, block_table, kv_lens, status)
+    if ragged:
+        qs, ls, ps = (p.Sq, p.Hq, p.D), (p.Sq, p.Hq), (p.Sq,)
+    else:
+        qs, ls, ps = (p.B, p.Hq, p.Sq, p.D), (p.B, p.Hq, p.Sq), (p.B, p.Sq)
+    _expect(q, qs, "q")
+    _expect(out, qs, "out")
+    _expect(lse, ls, "lse")
+    _expect(position_ids, ps, "position_ids")
+
+
 def _launch(fn, p, q, k_cache, v_cache, block_table, kv_lens, position_ids, out, lse, status,
-            stream):
+            stream, ragged=False):
     import torch
     for t, dt, name in ((q, torch.bfloat16, "q"), (k_cache, torch.bfloat16, "k_cache"),
                         (v_cache, torch.bfloat16, "v_cache"), (out, torch.bfloat16, "out"),
@@ -188,6 +222,7 @@ def _launch(fn, p, q, k_cache, v_cache, block_table, kv_lens, position_ids, out,
             raise TypeError("%s must be %s (got %s)" % (name, dt, t.dtype))
     if status is not None and status.dtype != torch.int32:
         raise TypeError("status must be int32")
+    _check_shapes(p, q, k_cache, v_cache, block_table, kv_lens, position_ids, out, lse, status, ragged)
     rc = fn(ctypes.byref(p), _dptr(q), _dptr(k_cache), _dptr(v_cache), _dptr(block_table),
             _dptr(kv_lens), _dptr(position_ids), _dptr(out), _dptr(lse), _dptr(status),
             _stream(stream))
@@ -233,6 +268,11 @@ def attn_prefill_backward(p: Plan, q, k_cache, v_cache, block_table, kv_lens, po
             raise TypeError("%s must be %s (got %s)" % (name, dt, t.dtype))
     if status is not None and status.dtype != torch.int32:
         raise TypeError("status must be int32")
+    _check_shapes(p, q, k_cache, v_cache, block_table, kv_lens, position_ids, out, lse, status)
+    _expect(dout, q.shape, "dout")
+    _expect(dq, q.shape, "dq")
+    _expect(dk_cache, k_cache.shape, "dk_cache")
+    _expect(dv_cache, v_cache.shape, "dv_cache")
     nbytes = workspace.numel() * workspace.element_size()
     rc = load().rk_paged_attn_prefill_backward(
         ctypes.byref(p), _dptr(q), _dptr(k_cache), _dptr(v_cache), _dptr(block_table), _dptr(kv_lens),
@@ -261,6 +301,7 @@ def attn_decode_split(p: Plan, split_tokens, q, k_cache, v_cache, block_table, k
             raise TypeError("%s must be %s (got %s)" % (name, dt, t.dtype))
     if status is not None and status.dtype != torch.int32:
         raise TypeError("status must be int32")
+    _check_shapes(p, q, k_cache, v_cache, block_table, kv_lens, position_ids, out, lse, status)
     nbytes = scratch.numel() * scratch.element_size()
     rc = load().rk_paged_attn_decode_split(
         ctypes.byref(p), int(split_tokens), _dptr(q), _dptr(k_cache), _dptr(v_cache), _dptr(block_table),
@@ -289,6 +330,10 @@ def kv_append(p: Plan, n_new, k_new, v_new, block_table, kv_lens, k_cache, v_cac
             raise TypeError("%s must be %s (got %s)" % (name, dt, t.dtype))
     if status is not None and status.dtype != torch.int32:
         raise TypeError("status must be int32")
+    _check_common(p, k_cache, v_cache, block_table, kv_lens, status)
+    if int(n_new) > 0:  # n_new <= 0 is judged by the library (0: nothing to do, < 0: RK_E_ARG)
+        _expect(k_new, (p.B, int(n_new), p.Hkv, p.D), "k_new")
+        _expect(v_new, (p.B, int(n_new), p.Hkv, p.D), "v_new")
     rc = load().rk_paged_kv_append(ctypes.byref(p), int(n_new), _dptr(k_new), _dptr(v_new), _dptr(block_table),
                                    _dptr(kv_lens), _dptr(k_cache), _dptr(v_cache), _dptr(status),
                                    _stream(stream))
@@ -316,8 +361,9 @@ def attn_ragged(p: Plan, max_q_len, qo_indptr, q, k_cache, v_cache, block_table,
     import torch
     if qo_indptr.dtype != torch.int32:
         raise TypeError("qo_indptr must be int32")
+    _expect(qo_indptr, (p.B + 1,), "qo_indptr")
     _launch(lambda pp, *r: load().rk_paged_attn_ragged(pp, int(max_q_len), _dptr(qo_indptr), *r), p, q,
-            k_cache, v_cache, block_table, kv_lens, position_ids, out, lse, status, stream)
+            k_cache, v_cache, block_table, kv_lens, position_ids, out, lse, status, stream, ragged=True)
 
 
 def run(mode: str, q, k_cache, v_cache, block_table, kv_lens, position_ids, plan_obj=None,

@@ -11,7 +11,8 @@
 // before its attention runs, "Current Implementation", trailing positions).
 //
 // One warp per (row, new token): a token is Hkv * D * 2 bytes of K and the same
-// of V, copied with 16-byte loads and stores.  Memory-safe: a token whose
+// of V, copied with 16-byte loads and stores, all loads of a lane issued before
+// its stores.  Memory-safe: a token whose
 // position or page is out of range is not written and flags the status word.
 #include <atomic>
 
@@ -43,10 +44,27 @@ __global__ void __launch_bounds__(256) kv_append_kernel(const __grid_constant__ 
     const uint4* vs = reinterpret_cast<const uint4*>(a.v_new) + ((size_t)b * a.n_new + j) * row16;
     uint4* kd = reinterpret_cast<uint4*>(a.k_cache) + ((size_t)pg * PAGE + t % PAGE) * row16;
     uint4* vd = reinterpret_cast<uint4*>(a.v_cache) + ((size_t)pg * PAGE + t % PAGE) * row16;
-    for (size_t c = lane; c < row16; c += 32) {
-        const uint4 kx = __ldg(ks + c), vx = __ldg(vs + c);
-        kd[c] = kx;
-        vd[c] = vx;
+    // Every load of a pass is issued before its stores, so a lane keeps
+    // 2 x APPEND_UNROLL 16-byte loads in flight (the whole token for Hkv = 8).
+    constexpr int APPEND_UNROLL = 4;
+    for (size_t c0 = lane; c0 < row16; c0 += 32 * APPEND_UNROLL) {
+        uint4 kx[APPEND_UNROLL], vx[APPEND_UNROLL];
+#pragma unroll
+        for (int u = 0; u < APPEND_UNROLL; ++u) {
+            const size_t c = c0 + 32 * u;
+            if (c < row16) {
+                kx[u] = __ldcs(ks + c);  // the new tokens are read once: streaming loads
+                vx[u] = __ldcs(vs + c);
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < APPEND_UNROLL; ++u) {
+            const size_t c = c0 + 32 * u;
+            if (c < row16) {
+                kd[c] = kx[u];
+                vd[c] = vx[u];
+            }
+        }
     }
 }
 

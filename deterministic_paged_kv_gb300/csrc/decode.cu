@@ -128,6 +128,10 @@ __global__ void __launch_bounds__(DEC_THREADS, 1)
     const int G = a.G, h0 = kvh * G;
     if (s_base & 1023u) {  // the swizzled operand layout needs a 1024-byte aligned base
         if (tid == 0 && a.status) atomicOr(a.status, RK_STATUS_TIMEOUT);
+        // Nothing was computed: padded rows (and split partials, which the merge
+        // then turns into out = 0, lse = NaN) are written as failed.  A ragged
+        // row's packed index is not known here; the status bit reports it.
+        if (!a.qo_indptr) write_empty_row(a, b, b, h0, split, __int_as_float(0x7fc00000));
         return;
     }
 

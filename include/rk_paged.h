@@ -80,7 +80,8 @@ enum rk_status {
 #define RK_STATUS_KVLEN (1 << 1)    /* kv_len outside [0, W * page_size] */
 #define RK_STATUS_POSITION (1 << 2) /* a negative query position */
 #define RK_STATUS_TIMEOUT (1 << 3)  /* an internal pipeline wait gave up (kernel returned early) */
-#define RK_STATUS_RANGE (1 << 4)    /* prefill: a pre-RoPE q or k element of the tile has |x| >= 2^15 */
+#define RK_STATUS_RANGE (1 << 4)    /* decode, prefill, ragged, backward: a pre-RoPE q or k element the
+                                       kernel reads has |x| >= 2^15 (the FP16 score operand limit) */
 
 /* Opaque stream handle; identical to cudaStream_t / CUstream. */
 typedef struct CUstream_st *rk_stream_t;
@@ -143,6 +144,10 @@ int rk_paged_plan(rk_paged_plan_t *plan, int32_t B, int32_t Sq, int32_t Hq, int3
  *   in the file header.  Every pointer is DEVICE memory of the current
  *   device; q, k_cache, v_cache, out 16-byte aligned.  status_d: int32 the
  *   kernel ORs RK_STATUS_* bits into (may be NULL); never cleared here.
+ * The score MMA takes the rotated q and k as FP16 (FP32 accumulation), so
+ * pre-RoPE q / k elements must stay below 2^15 in magnitude: a (row, KV head)
+ * whose query heads or visible keys hold a larger value is not computed; its
+ * query heads get out = 0, lse = NaN and RK_STATUS_RANGE is set.
  * Returns RK_E_ARG for a null/misaligned pointer or a plan that is not a
  * decode plan, RK_E_DEVICE off sm_103, RK_E_CUDA if the launch fails.
  */
@@ -217,9 +222,15 @@ int rk_paged_attn_decode_split(const rk_paged_plan_t *plan, int32_t split_tokens
  * rk_paged_attn_decode_split_static -- rk_paged_attn_decode_split without a
  * caller scratch buffer and without any allocation: the partials live in one
  * file-scope device array of RK_PAGED_SPLIT_STATIC_SCRATCH_BYTES inside the
- * library (its address is looked up once per device, with that device
- * current).  Arguments, results and errors as rk_paged_attn_decode_split,
- * and in addition:
+ * library.  For callers that may not allocate device memory at all (a
+ * process whose memory is handed out by another owner, or code that must not
+ * call cudaMalloc while another stream is being captured).  The first call on
+ * a device looks the array's device address up (cudaGetSymbolAddress, with
+ * that device current, which may load the module): make that first call
+ * before any stream capture.  The address is then kept for the life of the
+ * process, which assumes the device's context is not reset (cudaDeviceReset)
+ * while the library is loaded.  Arguments, results and errors as
+ * rk_paged_attn_decode_split, and in addition:
  *   RK_E_ARG   rk_paged_decode_split_scratch_bytes(plan, split_tokens) is
  *              above RK_PAGED_SPLIT_STATIC_SCRATCH_BYTES (nothing launched);
  *   RK_E_CUDA  the device address of the array could not be obtained.

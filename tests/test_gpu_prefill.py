@@ -18,7 +18,8 @@ def _lib():
 
 @pytest.mark.parametrize("Hq,Hkv", [(32, 8), (8, 8), (16, 8), (64, 8), (4, 1)])
 def test_prefill_small_ragged_parity(Hq, Hkv):
-    """Two q-tiles (one partial), ragged prefixes, early positions (split-bf16 scores)."""
+    """Two q-tiles (one partial), ragged prefixes, early positions (few keys per
+    query, where the FP16 score operands matter most for the LSE bound)."""
     kv = [300, 77, 41]
     w = workloads.random_case(3, 40, Hq, Hkv, 128, kv, seed=13 + Hq, mode="prefill")
     out, lse = run_gpu(w)
@@ -26,8 +27,9 @@ def test_prefill_small_ragged_parity(Hq, Hkv):
     assert_parity(out, lse, ro, rl)
 
 
-def test_prefill_late_positions_bf16_path():
-    """Positions past 1024: plain BF16 score MMA, several KV tiles, ragged tail."""
+def test_prefill_late_positions():
+    """Positions past 1024: several KV tiles per q-tile, RoPE anchors and angle
+    steps across tiles, a ragged last page."""
     kv = [1100, 1333]
     w = workloads.random_case(2, 70, 32, 8, 128, kv, seed=17, mode="prefill")
     out, lse = run_gpu(w)

@@ -246,3 +246,95 @@ def test_backward_workspace_size_host_only(rk):
     r = lambda x: (x + 255) // 256 * 256
     want = r(2 * 32 * 40 * 128 * 2) + 2 * r(2 * 8 * 4 * 16 * 128 * 2) + r(2 * 32 * 40 * 4)
     assert rk.prefill_backward_workspace_bytes(p) == want
+
+
+def _tensors(B=2, Sq=3, Hq=32, Hkv=8, NP=6, W=3, ragged=False):
+    import torch
+    bf, i32, f32 = torch.bfloat16, torch.int32, torch.float32
+    if ragged:
+        q = torch.zeros((Sq, Hq, 128), dtype=bf)
+        lse = torch.zeros((Sq, Hq), dtype=f32)
+        pos = torch.zeros((Sq,), dtype=i32)
+    else:
+        q = torch.zeros((B, Hq, Sq, 128), dtype=bf)
+        lse = torch.zeros((B, Hq, Sq), dtype=f32)
+        pos = torch.zeros((B, Sq), dtype=i32)
+    cache = torch.zeros((NP, 16, Hkv, 128), dtype=bf)
+    return dict(q=q, k_cache=cache, v_cache=cache.clone(), block_table=torch.zeros((B, W), dtype=i32),
+                kv_lens=torch.zeros((B,), dtype=i32), position_ids=pos, out=q.clone(), lse=lse)
+
+
+_ORDER = ("q", "k_cache", "v_cache", "block_table", "kv_lens", "position_ids", "out", "lse")
+
+
+@pytest.mark.parametrize("name,bad_prefill,bad_decode", [
+    ("q", (2, 32, 2, 128), (2, 32, 1, 64)), ("out", (2, 32, 3, 64), (1, 32, 1, 128)),
+    ("lse", (2, 32, 2), (2, 16, 1)), ("k_cache", (5, 16, 8, 128), (6, 16, 8, 64)),
+    ("v_cache", (6, 16, 4, 128), (6, 8, 8, 128)), ("block_table", (2, 2), (2, 4)),
+    ("kv_lens", (1,), (3,)), ("position_ids", (2, 2), (2, 2))])
+def test_binding_refuses_tensors_smaller_than_the_plan(rk, name, bad_prefill, bad_decode):
+    """The C ABI sees only pointers: the binding compares every tensor with the
+    plan and raises before any call into the library (here on CPU tensors, so
+    a call that got through would fail on the CUDA check instead)."""
+    import torch
+    p = rk.plan(2, 3, 32, 8, 128, 16, 6, 3)
+    t = _tensors()
+    with pytest.raises(ValueError, match="expected a CUDA tensor"):  # shapes right: stops at the device check
+        rk.attn_prefill(p, *[t[k] for k in _ORDER])
+    t[name] = torch.zeros(bad_prefill, dtype=t[name].dtype)
+    with pytest.raises(ValueError, match="the plan needs"):
+        rk.attn_prefill(p, *[t[k] for k in _ORDER])
+    pd = rk.plan(2, 1, 32, 8, 128, 16, 6, 3)
+    td = _tensors(Sq=1)
+    td[name] = torch.zeros(bad_decode, dtype=td[name].dtype)
+    args = [td[k] for k in _ORDER]
+    with pytest.raises(ValueError, match="the plan needs"):
+        rk.attn_decode(pd, *args)
+    with pytest.raises(ValueError, match="the plan needs"):
+        rk.attn_decode_split(pd, 1024, *args, torch.zeros(1 << 20, dtype=torch.uint8))
+    with pytest.raises(ValueError, match="the plan needs"):
+        rk.attn_decode_split_static(pd, 1024, *args)
+
+
+def test_binding_refuses_wrong_ragged_append_and_backward_shapes(rk):
+    import torch
+    p, mq = rk.plan_ragged(2, 5, 32, 8, 128, 16, 6, 3, [0, 2, 5])
+    t = _tensors(Sq=5, ragged=True)
+    ind = torch.tensor([0, 2, 5], dtype=torch.int32)
+    with pytest.raises(ValueError, match="expected a CUDA tensor"):
+        rk.attn_ragged(p, mq, ind, *[t[k] for k in _ORDER])
+    with pytest.raises(ValueError, match="the plan needs"):
+        rk.attn_ragged(p, mq, ind[:2], *[t[k] for k in _ORDER])
+    t["position_ids"] = torch.zeros((4,), dtype=torch.int32)
+    with pytest.raises(ValueError, match="the plan needs"):
+        rk.attn_ragged(p, mq, ind, *[t[k] for k in _ORDER])
+    # kv_append: new tokens [B, n_new, Hkv, D]
+    pa = rk.plan(2, 1, 32, 8, 128, 16, 6, 3)
+    ta = _tensors(Sq=1)
+    kn = torch.zeros((2, 4, 8, 128), dtype=torch.bfloat16)
+    with pytest.raises(ValueError, match="expected a CUDA tensor"):
+        rk.kv_append(pa, 4, kn, kn, ta["block_table"], ta["kv_lens"], ta["k_cache"], ta["v_cache"])
+    with pytest.raises(ValueError, match="the plan needs"):
+        rk.kv_append(pa, 5, kn, kn, ta["block_table"], ta["kv_lens"], ta["k_cache"], ta["v_cache"])
+    with pytest.raises(ValueError, match="the plan needs"):
+        rk.kv_append(pa, 4, kn, kn, ta["block_table"], ta["kv_lens"], ta["k_cache"][:5], ta["v_cache"])
+    # backward: dout / dq like q, dk / dv like the caches
+    pb = rk.plan(2, 3, 32, 8, 128, 16, 6, 3)
+    tb = _tensors()
+    f32 = torch.float32
+    good = dict(dout=tb["q"].clone(), dq=torch.zeros(tb["q"].shape, dtype=f32),
+                dk=torch.zeros(tb["k_cache"].shape, dtype=f32), dv=torch.zeros(tb["k_cache"].shape, dtype=f32))
+    ws = torch.zeros(1 << 20, dtype=torch.uint8)
+
+    def call(g):
+        rk.attn_prefill_backward(pb, tb["q"], tb["k_cache"], tb["v_cache"], tb["block_table"], tb["kv_lens"],
+                                 tb["position_ids"], tb["out"], tb["lse"], g["dout"], g["dq"], g["dk"], g["dv"], ws)
+
+    with pytest.raises(ValueError, match="expected a CUDA tensor"):
+        call(good)
+    for k, shape in (("dout", (2, 32, 2, 128)), ("dq", (2, 32, 3, 127)), ("dk", (6, 16, 8, 64)),
+                     ("dv", (5, 16, 8, 128))):
+        g = dict(good)
+        g[k] = torch.zeros(shape, dtype=good[k].dtype)
+        with pytest.raises(ValueError, match="the plan needs"):
+            call(g)
