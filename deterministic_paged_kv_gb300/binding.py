@@ -31,7 +31,7 @@ ERRORS = {
 }
 CODES = {v: k for k, v in ERRORS.items()}
 STATUS_PAGE_OOB, STATUS_KVLEN, STATUS_POSITION, STATUS_TIMEOUT, STATUS_RANGE = 1, 2, 4, 8, 16
-ABI_VERSION = 2
+ABI_VERSION = 3
 SPLIT_STATIC_SCRATCH_BYTES = 16 << 20  # RK_PAGED_SPLIT_STATIC_SCRATCH_BYTES
 
 
@@ -54,6 +54,7 @@ class Plan(ctypes.Structure):
         ("sm_scale", ctypes.c_float), ("validated", ctypes.c_int32), ("pf_units", ctypes.c_int32),
         ("rope_theta", ctypes.c_double), ("rope_scale", ctypes.c_double),
         ("rope_turns", ctypes.c_uint64 * 64),
+        ("wait_limit_ns", ctypes.c_uint32), ("timeout_drill", ctypes.c_int32),
     ]
 
 

@@ -67,8 +67,9 @@ struct BtBars {
     uint64_t k_full, v_full;
     uint64_t q_full[2], q_ready[2], q_empty[2];
     uint64_t s_full, p_ready, done;
+    uint64_t never;  // nothing arrives: the timeout drill's wait
     uint32_t tmem_base;
-    int abort;
+    PipeCtl pipe;
     int range_bad;
     int first_block;
     uint64_t turns[ROPE_PAIRS];
@@ -205,8 +206,10 @@ __global__ void __launch_bounds__(BT_THREADS, 1)
     const int n_pg = (n_rows + PAGE - 1) / PAGE;
     const int32_t* bt = a.block_table + (size_t)b * a.W + t0 / PAGE;  // this tile's table entries
     if (tid == 0) {
-        bars->abort = 0;
+        bars->pipe.abort = 0;
+        bars->pipe.limit_ns = wait_limit(a.wait_limit_ns);
         bars->range_bad = 0;
+        mbar_init(smem_u32(&bars->never), 1);
         mbar_init(smem_u32(&bars->k_full), 1);
         mbar_init(smem_u32(&bars->v_full), 1);
         for (int j = 0; j < 2; ++j) {
@@ -257,7 +260,7 @@ __global__ void __launch_bounds__(BT_THREADS, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = bars->tmem_base;
-    volatile int* abort = &bars->abort;
+    PipeCtl* abort = &bars->pipe;
     const float nanv = __int_as_float(0x7fc00000);
 
     if (wg == 3) {
@@ -293,7 +296,7 @@ __global__ void __launch_bounds__(BT_THREADS, 1)
                 tma_load_4d(dq + 2 * BT_TILE + 16384, &omap, fb, 64, s0, h0, b);
                 ++issued;
             }
-            if (*abort) {  // let the copies in flight land before the CTA's shared memory is released
+            if (pipe_aborted(abort)) {  // let the copies in flight land before the CTA's shared memory is released
                 mbar_wait_drain(kb, 0);
                 mbar_wait_drain(vb, 0);
                 for (int jj = max(0, issued - 2); jj < issued; ++jj)
@@ -309,7 +312,8 @@ __global__ void __launch_bounds__(BT_THREADS, 1)
             const uint32_t idK = (1u << 4) | (1u << 16) | ((uint32_t)(HEAD_DIM >> 3) << 17) |
                                  ((uint32_t)(BT_KEYS >> 4) << 24);
             const uint32_t dK = desc_lo(s_base + BT_OFF_K, 16), dV = desc_lo(s_base + BT_OFF_V, 16);
-            bool ok = mbar_wait(smem_u32(&bars->k_full), 0, abort) && mbar_wait(smem_u32(&bars->v_full), 0, abort);
+            bool ok = (!a.timeout_drill || drill_wait(smem_u32(&bars->never), abort)) &&
+                      mbar_wait(smem_u32(&bars->k_full), 0, abort) && mbar_wait(smem_u32(&bars->v_full), 0, abort);
             for (int jj = 0; jj < nblk && ok; ++jj) {
                 const int st = jj & 1;
                 if (!(ok = mbar_wait(smem_u32(&bars->q_ready[st]), (uint32_t)((jj >> 1) & 1), abort))) break;
@@ -530,8 +534,9 @@ struct DqBars {
     uint64_t q_full;
     uint64_t k_full[DT_KST], k_empty[DT_KST], v_full[DT_VST], v_empty[DT_VST];
     uint64_t s_full, p_ready, done;
+    uint64_t never;  // nothing arrives: the timeout drill's wait
     uint32_t tmem_base;
-    int abort;
+    PipeCtl pipe;
     int range_bad;
     int n_keys;
     int flags;
@@ -563,8 +568,10 @@ __global__ void __launch_bounds__(BT_THREADS, 1)
     const int32_t* bt = a.block_table + (size_t)b * a.W;
     const int32_t* pos_row = a.position_ids + (size_t)b * a.Sq;
     if (tid == 0) {
-        bars->abort = 0;
+        bars->pipe.abort = 0;
+        bars->pipe.limit_ns = wait_limit(a.wait_limit_ns);
         bars->range_bad = 0;
+        mbar_init(smem_u32(&bars->never), 1);
         mbar_init(smem_u32(&bars->q_full), 1);
         for (int j = 0; j < DT_KST; ++j) {
             mbar_init(smem_u32(&bars->k_full[j]), 1);
@@ -627,7 +634,7 @@ __global__ void __launch_bounds__(BT_THREADS, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = bars->tmem_base;
-    volatile int* abort = &bars->abort;
+    PipeCtl* abort = &bars->pipe;
 
     if (wg == 3) {
         asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(BT_REG_CTRL));
@@ -661,7 +668,7 @@ __global__ void __launch_bounds__(BT_THREADS, 1)
                 tma_load_3d(vt + 16384, &vmap, vb, 64, i * BT_KEYS, lrow);
                 ++issued;
             }
-            if (*abort) {
+            if (pipe_aborted(abort)) {  // let the copies in flight land before the CTA's shared memory is released
                 mbar_wait_drain(qb, 0);
                 for (int i = max(0, issued - DT_KST); i < issued; ++i)
                     mbar_wait_drain(smem_u32(&bars->k_full[i % DT_KST]), (uint32_t)((i / DT_KST) & 1));
@@ -676,7 +683,8 @@ __global__ void __launch_bounds__(BT_THREADS, 1)
                                  ((uint32_t)(BT_QB >> 4) << 24);
             const uint32_t dQa = desc_lo(s_base + DT_OFF_Q, 16), dOa = desc_lo(s_base + DT_OFF_DO, 16);
             // pipe order: S(0), dP(0), S(1), dQ'(0), dP(1), S(2), dQ'(1), ...
-            bool ok = mbar_wait(smem_u32(&bars->q_full), 0, abort) && mbar_wait(smem_u32(&bars->k_full[0]), 0, abort);
+            bool ok = (!a.timeout_drill || drill_wait(smem_u32(&bars->never), abort)) &&
+                      mbar_wait(smem_u32(&bars->q_full), 0, abort) && mbar_wait(smem_u32(&bars->k_full[0]), 0, abort);
             if (ok) {
                 tc_fence_after();
                 mma_ss_steps<0, 8, K_MAJOR_128, K_MAJOR_128>(tmem, dQa, desc_lo(s_base + DT_OFF_K, 16), idS, 0u);
@@ -754,7 +762,9 @@ __global__ void __launch_bounds__(BT_THREADS, 1)
         if (hsel == 1) bars->dpart[r] = dl;
         named_bar_sync(3, 256);
         const float delta = bars->dpart[r];
-        if (hsel == 1 && valid) a.delta[o] = delta;
+        // (without the staged dout tile delta is unknown: NaN, so the dk / dv
+        // kernel's gradients that use it come out NaN too)
+        if (hsel == 1 && valid) a.delta[o] = ok ? delta : nanv;
         bool over = false;
         for (int i = 0; i < n_tiles && ok; ++i) {
             if (!(ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&bars->s_full), (uint32_t)(i & 1), abort)))) break;

@@ -81,8 +81,9 @@ struct DecCtrl {
     // the PV that read it (pv_done); a buffer is reused two tiles later, after
     // its previous phase has been observed, so a wait never meets a later phase
     uint64_t s_full[2], s_free[2], p_ready[2], pv_done[2], o_done;
+    uint64_t never;  // nothing arrives: the timeout drill's wait
     uint32_t tmem_base;
-    int abort;
+    PipeCtl pipe;
     int range_bad;
     uint64_t turns[ROPE_PAIRS];
     float2 step[ROPE_PAIRS];  // cos/sin of an XF_ROW_STEP-position turn per pair
@@ -197,8 +198,10 @@ __global__ void __launch_bounds__(DEC_THREADS, 1)
 #pragma unroll
     for (int e = 0; e < PRE; ++e) pgt[tid + e * DEC_THREADS] = pre[e];
     if (tid == 0) {
-        ctl->abort = 0;
+        ctl->pipe.abort = 0;
+        ctl->pipe.limit_ns = wait_limit(a.wait_limit_ns);
         ctl->range_bad = 0;
+        mbar_init(smem_u32(&ctl->never), 1);
         mbar_init(smem_u32(&ctl->q_ready), DEC_XFORM_THREADS);
         for (int k = 0; k < DEC_KSTAGES; ++k) {
             mbar_init(smem_u32(&ctl->k_ready[k]), DEC_XFORM_THREADS);
@@ -250,7 +253,7 @@ __global__ void __launch_bounds__(DEC_THREADS, 1)
     tc_fence_after();
     const uint32_t tmem = ctl->tmem_base;
     const uint32_t tO = tmem + 32;
-    volatile int* abort = &ctl->abort;
+    PipeCtl* abort = &ctl->pipe;
 
     if (warp == WARP_TMA_K) {
         // K arrives through the transform threads' own copies: nothing to do.
@@ -299,7 +302,7 @@ __global__ void __launch_bounds__(DEC_THREADS, 1)
             }
             ++issued;
         }
-        if (lane == 0 && *abort) {
+        if (lane == 0 && pipe_aborted(abort)) {
             for (int i = max(0, issued - DEC_VSTAGES); i < issued; ++i)
                 mbar_wait_drain(smem_u32(&ctl->v_full[i % DEC_VSTAGES]), (uint32_t)((i / DEC_VSTAGES) & 1));
         }
@@ -317,7 +320,8 @@ __global__ void __launch_bounds__(DEC_THREADS, 1)
             if (warp == WARP_MMA) {
                 const uint32_t idS = idesc_f16_f32(DEC_BN, NH);
                 const uint32_t dK0 = desc_lo(s_base + OFF_K, 16), dQT = desc_lo(s_base + OFF_QT, 16);
-                ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&ctl->q_ready), 0, abort));
+                ok = __all_sync(0xffffffffu, (!a.timeout_drill || drill_wait(smem_u32(&ctl->never), abort)) &&
+                                                 mbar_wait(smem_u32(&ctl->q_ready), 0, abort));
                 for (int it = 0; it < n_loc && ok; ++it) {
                     const int k = it % DEC_KSTAGES, sb = it & 1;
                     ok = __all_sync(0xffffffffu,
@@ -621,8 +625,12 @@ __global__ void __launch_bounds__(DEC_THREADS, 1)
                         range_bad ? __int_as_float(0x7fc00000)
                                   : (L[h] > 0.0f ? (m[h] + log2f(L[h])) * 0.693147180559945309f : -INFINITY);
             if (range_bad && t == 0 && a.status) atomicOr(a.status, RK_STATUS_RANGE);
-        } else if (t == 0 && a.status) {
-            atomicOr(a.status, RK_STATUS_TIMEOUT);
+        } else {  // a wait gave up: the group's rows are written as failed
+#pragma unroll
+            for (int h = 0; h < 8; ++h)
+                if (h < G) out[((size_t)tq * a.Hq + h0 + h) * HEAD_DIM + t] = __float2bfloat16_rn(0.0f);
+            if (t < G) a.lse[(size_t)tq * a.Hq + h0 + t] = __int_as_float(0x7fc00000);
+            if (t == 0 && a.status) atomicOr(a.status, RK_STATUS_TIMEOUT);
         }
     }
 

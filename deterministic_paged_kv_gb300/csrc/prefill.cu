@@ -73,8 +73,9 @@ struct PfBars {
     uint64_t k_full[KSTAGES], k_ready[KSTAGES], k_empty[KSTAGES];
     uint64_t v_full[VSTAGES], v_empty[VSTAGES], v_tail;
     uint64_t s_full[2], p_ready[2], o_done[2];
+    uint64_t never;  // nothing arrives: the timeout drill's wait
     uint32_t tmem_base;
-    int abort;
+    PipeCtl pipe;
     int range_bad;
     uint64_t turns[ROPE_PAIRS];
     float2 step16[ROPE_PAIRS];  // cos/sin of a 16-position turn per pair
@@ -307,8 +308,10 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
         }
     }
     if (tid == 0) {
-        bars->abort = 0;
+        bars->pipe.abort = 0;
+        bars->pipe.limit_ns = wait_limit(a.wait_limit_ns);
         bars->range_bad = 0;
+        mbar_init(smem_u32(&bars->never), 1);
         mbar_init(smem_u32(&bars->q_full), 1);
         mbar_init(smem_u32(&bars->q_ready), 128);
         for (int k = 0; k < KSTAGES; ++k) {
@@ -381,7 +384,7 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = bars->tmem_base;
-    volatile int* abort = &bars->abort;
+    PipeCtl* abort = &bars->pipe;
 
     if (wg == 3) {
         asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(REG_CTRL));
@@ -456,7 +459,9 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
                 }
                 ++issued;
             }
-            if (lane == 0 && *abort) {
+            if (lane == 0 && pipe_aborted(abort)) {
+                // the copies this warp issued land before the CTA's shared memory is released
+                if (is_k) mbar_wait_drain(smem_u32(&bars->q_full), 0);  // Q, issued unconditionally above
                 for (int i = max(0, issued - nst); i < issued; ++i)
                     mbar_wait_drain(smem_u32(is_k ? &bars->k_full[i % nst] : &bars->v_full[i % nst]),
                                     (uint32_t)((i / nst) & 1));
@@ -473,7 +478,8 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
             const uint32_t dQ0 = desc_lo(s_base + OFF_Q, 16);
             const uint32_t dK0 = desc_lo(s_base + OFF_K, 16);
             const uint32_t dV0 = desc_lo(s_base + OFF_V, 2048);
-            bool ok = mbar_wait(smem_u32(&bars->q_ready), 0, abort);
+            bool ok = (!a.timeout_drill || drill_wait(smem_u32(&bars->never), abort)) &&
+                      mbar_wait(smem_u32(&bars->q_ready), 0, abort);
             int v_seen = -1;  // last V tile whose arrival (and tail zeroing) was observed
             // O_j += P_j(i) V(i).  implied: P_j(i) was published after K(i+1) was
             // ready, which the transform published after V(i) landed, so only
@@ -743,8 +749,12 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
         } else if (nt == 0 && valid) {
             for (int d = 0; d < HEAD_DIM / 8; ++d) o[d] = make_uint4(0, 0, 0, 0);
             a.lse[rm.at(a, h, s)] = -INFINITY;
-        } else if (!ok && r == 0 && a.status) {
-            atomicOr(a.status, RK_STATUS_TIMEOUT);
+        } else if (!ok) {  // a wait gave up: the q-tile's rows are written as failed
+            if (valid) {
+                for (int d = 0; d < HEAD_DIM / 8; ++d) o[d] = make_uint4(0, 0, 0, 0);
+                a.lse[rm.at(a, h, s)] = __int_as_float(0x7fc00000);
+            }
+            if (r == 0 && a.status) atomicOr(a.status, RK_STATUS_TIMEOUT);
         }
         named_bar_sync(2, PF_THREADS);
     }

@@ -287,6 +287,8 @@ int rk_paged_plan(rk_paged_plan_t* plan, int32_t B, int32_t Sq, int32_t Hq, int3
     plan->validated = check ? 1 : 0;
     plan->rope_theta = rope_theta;
     plan->rope_scale = rope_scale;
+    plan->wait_limit_ns = (uint32_t)RK_WAIT_LIMIT_NS;
+    plan->timeout_drill = 0;
     for (int i = 0; i < D / 2; ++i) {
         // Turns per position of pair i: theta^(-2i/D) / (2 pi scale), in [0, 1/(2 pi)].
         const double w = std::pow(rope_theta, -2.0 * (double)i / (double)D) / (kTwoPi * rope_scale);
@@ -404,6 +406,8 @@ int decode_common(const rk_paged_plan_t* plan, int32_t split_tokens, const void*
     a.W = plan->W;
     a.num_pages = plan->num_pages;
     a.qk_scale_log2 = (float)((1.0 / std::sqrt((double)plan->D)) * 1.4426950408889634074);
+    a.wait_limit_ns = plan->wait_limit_ns;
+    a.timeout_drill = plan->timeout_drill;
     if (split_tokens > 0) {
         const int64_t n = (int64_t)plan->B * plan->Hq * split_count(plan, split_tokens);
         a.split_tiles = split_tokens / rk::DEC_BN;
@@ -592,6 +596,8 @@ int rk_paged_attn_prefill(const rk_paged_plan_t* plan, const void* q, const void
     a.rows_per_head = rph;
     a.n_qtiles = (plan->Sq + rph - 1) / rph;
     a.qk_scale_log2 = (float)((1.0 / std::sqrt((double)plan->D)) * 1.4426950408889634074);
+    a.wait_limit_ns = plan->wait_limit_ns;
+    a.timeout_drill = plan->timeout_drill;
     std::memcpy(a.rope_turns, plan->rope_turns, sizeof a.rope_turns);
     cudaError_t e = rk::launch_prefill(qm, km, vm, a, reinterpret_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return fail(RK_E_CUDA, "prefill launch: %s", cudaGetErrorString(e));
@@ -672,6 +678,8 @@ int rk_paged_attn_prefill_backward(const rk_paged_plan_t* plan, const void* q, c
     a.num_pages = plan->num_pages;
     a.sm_scale = (float)(1.0 / std::sqrt((double)plan->D));
     a.qk_scale_log2 = (float)((1.0 / std::sqrt((double)plan->D)) * 1.4426950408889634074);
+    a.wait_limit_ns = plan->wait_limit_ns;
+    a.timeout_drill = plan->timeout_drill;
     std::memcpy(a.rope_turns, plan->rope_turns, sizeof a.rope_turns);
     // tensor maps of the dk / dv kernel: q and dout [B, Hq, Sq, D] as 4-D (d, position, head, row) with
     // a box of one 64-column half of a query block (64, 128/G positions, G heads, 1 row); both caches
@@ -747,6 +755,8 @@ int rk_paged_attn_ragged(const rk_paged_plan_t* plan, int32_t max_q_len, const i
         a.qo_indptr = qo_indptr_d;
         a.total_q = total_q;
         a.max_q_len = max_q_len;
+        a.wait_limit_ns = plan->wait_limit_ns;
+        a.timeout_drill = plan->timeout_drill;
         std::memcpy(a.rope_turns, plan->rope_turns, sizeof a.rope_turns);
         cudaError_t e = rk::launch_decode(vm, a, st);
         if (e != cudaSuccess) return fail(RK_E_CUDA, "ragged decode launch: %s", cudaGetErrorString(e));
@@ -805,6 +815,8 @@ int rk_paged_attn_ragged(const rk_paged_plan_t* plan, int32_t max_q_len, const i
     a.total_q = total_q;
     a.max_q_len = max_q_len;
     a.ragged_units = (int32_t)units;
+    a.wait_limit_ns = plan->wait_limit_ns;
+    a.timeout_drill = plan->timeout_drill;
     std::memcpy(a.rope_turns, plan->rope_turns, sizeof a.rope_turns);
     // started while the decode launch drains: the two write disjoint rows
     cudaError_t e = rk::launch_prefill(qm, km, vm, a, st, true);

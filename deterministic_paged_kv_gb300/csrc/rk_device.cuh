@@ -88,24 +88,48 @@ __device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity) {
     return ok != 0;
 }
 
+// Shared state of one CTA's pipeline waits: the abort flag every wait
+// watches, and the wall time after which a wait gives up (the launch's wait
+// limit, at most RK_WAIT_LIMIT_NS).
+struct PipeCtl {
+    int abort;
+    uint32_t limit_ns;
+};
+__device__ __forceinline__ bool pipe_aborted(PipeCtl* pc) { return *reinterpret_cast<volatile int*>(&pc->abort) != 0; }
+
 // Wait for phase `parity` of an mbarrier to complete.  Gives up (returns
-// false) after RK_WAIT_LIMIT_NS of wall time or as soon as *abort is set by
-// another warp, so that a pipeline that lost a participant cannot hang.
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort) {
+// false) once it has waited limit_ns of wall time past its first 32 probes,
+// or as soon as another warp has set the abort flag, so that a pipeline that
+// lost a participant cannot hang.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, PipeCtl* pc) {
 #pragma unroll 1
     for (int i = 0; i < 32; ++i)
         if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = global_timer_ns();
+    const uint64_t lim = pc->limit_ns;
 #pragma unroll 1
     while (true) {
         if (mbar_try_wait(bar, parity)) return true;
-        if (*abort) return false;
-        if (global_timer_ns() - t0 > RK_WAIT_LIMIT_NS) {
-            *abort = 1;
+        if (pipe_aborted(pc)) return false;
+        if (global_timer_ns() - t0 > lim) {
+            *reinterpret_cast<volatile int*>(&pc->abort) = 1;
             return false;
         }
     }
 }
+
+// Launch wait limit as the kernels use it: 0 means the default, and nothing
+// above the default or below 1 us.
+__device__ __forceinline__ uint32_t wait_limit(uint32_t ns) {
+    return ns == 0 ? (uint32_t)RK_WAIT_LIMIT_NS : (ns < 1000u ? 1000u : (ns > (uint32_t)RK_WAIT_LIMIT_NS ? (uint32_t)RK_WAIT_LIMIT_NS : ns));
+}
+
+// Test of the timeout exit (a launch's timeout_drill flag): the calling thread
+// waits on an mbarrier of its CTA that nothing arrives at, so the wait runs
+// out after the launch's limit, sets the abort flag and returns false; every
+// other wait of the CTA then gives up and the CTA takes its drain-and-exit
+// path.  `never` must be initialised with an arrival count of 1.
+__device__ __forceinline__ bool drill_wait(uint32_t never, PipeCtl* pc) { return mbar_wait(never, 0, pc); }
 
 // Wait with a time limit only (used on the way out after an abort).
 __device__ __forceinline__ void mbar_wait_drain(uint32_t bar, uint32_t parity) {

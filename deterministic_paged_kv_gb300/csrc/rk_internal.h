@@ -54,6 +54,8 @@ struct DecodeArgs {
     const int32_t* qo_indptr;
     int32_t total_q;
     int32_t max_q_len;            // rows with more queries are flagged (RK_STATUS_POSITION)
+    uint32_t wait_limit_ns;       // pipeline wait limit (0: RK_WAIT_LIMIT_NS)
+    int32_t timeout_drill;        // nonzero: the score MMA issuer first waits on a barrier nothing completes
     uint64_t rope_turns[ROPE_PAIRS];
 };
 constexpr int DEC_SPLIT_GRAIN = 1024;  // split lengths are multiples of this many tokens (8 KV tiles)
@@ -84,6 +86,8 @@ struct PrefillArgs {
     int32_t total_q;
     int32_t max_q_len;            // ragged: rows with more queries are not computed
     int32_t ragged_units;         // ragged: work units of the grid (grid = ragged_units x Hkv)
+    uint32_t wait_limit_ns;       // pipeline wait limit (0: RK_WAIT_LIMIT_NS)
+    int32_t timeout_drill;        // nonzero: the MMA issuer first waits on a barrier nothing completes
     int32_t pad0;
     uint64_t rope_turns[ROPE_PAIRS];
 };
@@ -117,6 +121,8 @@ struct BackwardArgs {
     int32_t B, Sq, Hq, Hkv, G, W, num_pages;
     float sm_scale;
     float qk_scale_log2;          // sm_scale * log2(e)
+    uint32_t wait_limit_ns;       // pipeline wait limit (0: RK_WAIT_LIMIT_NS)
+    int32_t timeout_drill;        // nonzero: each tcgen05 kernel's MMA issuer first waits on a barrier nothing completes
     uint64_t rope_turns[ROPE_PAIRS];
 };
 

@@ -57,7 +57,7 @@
 extern "C" {
 #endif
 
-#define RK_PAGED_ABI_VERSION 2u
+#define RK_PAGED_ABI_VERSION 3u
 #define RK_PAGED_MAX_ROPE_PAIRS 64
 
 /* Status codes returned by the entry points. */
@@ -106,6 +106,22 @@ typedef struct rk_paged_plan {
     /* Rotation rate of pair i in turns per position as a 0.64 fixed-point
      * fraction: round(2^64 * theta^(-2i/D) / (2 pi rope_scale)), i < D/2. */
     uint64_t rope_turns[RK_PAGED_MAX_ROPE_PAIRS];
+    /* Fail-closed waits.  Every pipeline wait inside a kernel gives up once it
+     * has waited wait_limit_ns of wall time (past its first 32 probes of the
+     * barrier, each of which may sleep up to 20 us); the CTA then waits out
+     * the copies it has in flight (those waits keep the 2 s limit), frees its
+     * tensor memory, writes its rows as failed (out = 0, lse = NaN; NaN
+     * gradients) and sets RK_STATUS_TIMEOUT.  rk_paged_plan sets 2000000000
+     * (2 s); the launch calls read 0 as 2 s and clamp other values to
+     * [1000, 2000000000]. */
+    uint32_t wait_limit_ns;
+    /* Test of that exit path, for callers that must see it work on their
+     * device: when nonzero, the MMA-issuing warp of every CTA of the
+     * tensor-core kernels first waits on a barrier of its CTA that nothing
+     * completes, so that wait runs out after wait_limit_ns and every CTA takes
+     * the timeout exit above (nothing is computed; the call returns RK_OK and
+     * the status word says RK_STATUS_TIMEOUT).  rk_paged_plan sets 0. */
+    int32_t timeout_drill;
 } rk_paged_plan_t;
 
 /*

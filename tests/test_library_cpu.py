@@ -338,3 +338,11 @@ def test_binding_refuses_wrong_ragged_append_and_backward_shapes(rk):
         g[k] = torch.zeros(shape, dtype=good[k].dtype)
         with pytest.raises(ValueError, match="the plan needs"):
             call(g)
+
+
+def test_plan_wait_limit_defaults(rk):
+    """Plans start with the 2 s wait limit and no timeout drill."""
+    p = rk.plan(2, 1, 32, 8, 128, 16, 6, 3)
+    assert p.wait_limit_ns == 2_000_000_000 and p.timeout_drill == 0
+    pr, _ = rk.plan_ragged(2, 5, 32, 8, 128, 16, 6, 3, [0, 2, 5])
+    assert pr.wait_limit_ns == 2_000_000_000 and pr.timeout_drill == 0
