@@ -384,10 +384,12 @@ def measure_backward(args, dev, stream, tf_burst, peak_kind):
             "note": "four launches per call (rotation of q and K into the workspace, dq with delta, dk/dv); deterministic, no atomics"}
 
 
-def measure_decode_long(args, dev, stream, hbm, peak_kind, split_tokens=2048):
+def measure_decode_long(args, dev, stream, hbm, peak_kind, splits=(1024, 1728, 2048)):
     """Time decode_long (B=1, kv 32768: 8 CTAs without splitting) through the
-    split-free entry point and the fixed-split entry point; L2 flushed between
-    launches.  Returns the "decode_long" object."""
+    split-free entry point and the fixed-split entry point at several split
+    lengths (1728 tokens: 19 splits x 8 KV heads = 152 CTAs, one per SM); L2
+    flushed between launches.  Returns the "decode_long" object with the best
+    split named."""
     import torch
 
     from deterministic_paged_kv_gb300 import binding, workloads
@@ -398,20 +400,21 @@ def measure_decode_long(args, dev, stream, hbm, peak_kind, split_tokens=2048):
                      w.position_ids, w.rope_theta, w.rope_scale)
     out = torch.empty_like(d["q"])
     lse = torch.empty((w.B, w.Hq, 1), dtype=torch.float32, device=dev)
-    scratch = torch.empty(binding.decode_split_scratch_bytes(p, split_tokens), dtype=torch.uint8, device=dev)
+    scratch = torch.empty(max(binding.decode_split_scratch_bytes(p, n) for n in splits), dtype=torch.uint8,
+                          device=dev)
     args_d = (d["q"], d["k_cache"], d["v_cache"], d["block_table"], d["kv_lens"], d["position_ids"], out, lse)
 
     def free():
         binding.attn_decode(p, *args_d, stream=stream)
 
-    def split():
-        binding.attn_decode_split(p, split_tokens, *args_d, scratch, stream=stream)
+    def split_fn(n):
+        return lambda: binding.attn_decode_split(p, n, *args_d, scratch, stream=stream)
 
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
     byt = decode_alg_bytes(w)
     res = {"config": {"workload": w.name + " page=16", "l2": "flushed (256 MB write) between launches",
-                      "alg_bytes_per_launch": byt, "split_tokens": split_tokens}}
-    for name, fn in (("split_free", free), ("split_%d" % split_tokens, split)):
+                      "alg_bytes_per_launch": byt, "split_tokens": list(splits)}}
+    for name, fn in [("split_free", free)] + [("split_%d" % n, split_fn(n)) for n in splits]:
         for _ in range(max(3, args.warmup)):
             fn()
         torch.cuda.synchronize()
@@ -419,6 +422,7 @@ def measure_decode_long(args, dev, stream, hbm, peak_kind, split_tokens=2048):
         ms = sum(t) / len(t)
         res[name] = {"value": byt / (ms * 1e-3) / 1e9, "unit": "GB/s", "ms_per_launch": ms,
                      "frac_of_peak": byt / (ms * 1e-3) / 1e9 / hbm, "peak_kind": peak_kind}
+    res["best_split"] = max(("split_%d" % n for n in splits), key=lambda k: res[k]["value"])
     return res
 
 

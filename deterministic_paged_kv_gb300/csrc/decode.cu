@@ -97,7 +97,7 @@ static_assert(sizeof(DecCtrl) <= DEC_CTRL_BYTES, "decode control block exceeds i
 // row's NaN / empty result).
 __device__ __forceinline__ void write_empty_row(const DecodeArgs& a, int b, int tq, int h0, int split,
                                                 float lse_val) {
-    if (a.split_tiles > 0) {
+    if (a.split_tokens > 0) {
         for (int i = threadIdx.x; i < a.G * HEAD_DIM; i += blockDim.x) {
             const int hh = i / HEAD_DIM, d = i % HEAD_DIM;
             a.o_part[(((size_t)b * a.Hq + h0 + hh) * a.n_splits + split) * HEAD_DIM + d] = 0.0f;
@@ -154,12 +154,15 @@ __global__ void __launch_bounds__(DEC_THREADS, 1)
     const int qpos = a.position_ids[tq];
     const int32_t* bt = a.block_table + (size_t)b * a.W;
     constexpr int PPT = DEC_BN / PAGE;  // pages per tile
-    const int i0 = a.split_tiles > 0 ? split * a.split_tiles : 0;
+    // This CTA's keys start at token t_begin: 0, or split * split_tokens (a
+    // multiple of the page size) for a fixed split.  Its tiles are 128 tokens
+    // counted from there.
+    const int t_begin = a.split_tokens > 0 ? split * a.split_tokens : 0;
     // The page ids of the CTA's part of the table are loaded before its length
     // is known (the metadata costs one round trip, not two) and judged against
     // the visible range below.
-    const int pg_lo = i0 * PPT;
-    const int pg_cap = a.split_tiles > 0 ? min(a.W, (i0 + a.split_tiles) * PPT) : a.W;
+    const int pg_lo = t_begin / PAGE;
+    const int pg_cap = a.split_tokens > 0 ? min(a.W, pg_lo + a.split_tokens / PAGE) : a.W;
     constexpr int PRE = 4;  // table entries per thread held from the early load
     int pre[PRE];
 #pragma unroll
@@ -171,16 +174,16 @@ __global__ void __launch_bounds__(DEC_THREADS, 1)
     if (kv_len < 0 || kv_len > a.W * PAGE) bad |= RK_STATUS_KVLEN;
     if (qpos < 0) bad |= RK_STATUS_POSITION;
     const int n_vis = bad ? 0 : (qpos >= kv_len ? kv_len : qpos + 1);
-    const int n_pages = (n_vis + PAGE - 1) / PAGE;
-    const int n_tiles = (n_vis + DEC_BN - 1) / DEC_BN;
-    // This CTA's KV tiles [i0, i0 + n_loc): the whole row, or one fixed split.
-    const int n_loc = a.split_tiles > 0 ? max(0, min(n_tiles, i0 + a.split_tiles) - i0) : n_tiles;
+    // This CTA's keys [t_begin, t_end): the row's visible keys, or those of one
+    // fixed split, in n_loc tiles of 128 tokens from t_begin.
+    const int t_end = a.split_tokens > 0 ? min(n_vis, t_begin + a.split_tokens) : n_vis;
+    const int n_loc = t_end > t_begin ? (t_end - t_begin + DEC_BN - 1) / DEC_BN : 0;
     // Last page partly filled and inside the visible range: its rows past
     // kv_len hold arbitrary bits and are zeroed in V after the copy lands
-    // (by the CTA that holds the row's last tile).
-    const bool has_tail = n_vis == kv_len && (kv_len & (PAGE - 1)) != 0 && n_loc > 0 && i0 + n_loc == n_tiles;
+    // (by the CTA that holds the row's last key).
+    const bool has_tail = n_vis == kv_len && (kv_len & (PAGE - 1)) != 0 && n_loc > 0 && t_end == n_vis;
     int oob = 0;
-    const int pg_end = min(n_pages, (i0 + n_loc) * PPT);  // the pages this CTA reads
+    const int pg_end = (t_end + PAGE - 1) / PAGE;  // the pages this CTA reads: [pg_lo, pg_end)
 #pragma unroll
     for (int e = 0; e < PRE; ++e) {
         const int i = pg_lo + tid + e * DEC_THREADS;
@@ -263,10 +266,9 @@ __global__ void __launch_bounds__(DEC_THREADS, 1)
         int issued = 0;
         // it: the CTA's own tile count (stages, phases); i: the row's tile index
         for (int it = 0; it < n_loc; ++it) {
-            const int i = i0 + it;
             const int k = it % DEC_VSTAGES;
             const uint32_t use = (uint32_t)(it / DEC_VSTAGES);
-            const int np = min(PPT, n_pages - i * PPT);
+            const int np = min(PPT, pg_end - (pg_lo + it * PPT));
             const int li = it * PPT + lane;  // lane's page within the CTA's range
             const int pg = lane >= np ? 0 : li < DEC_PGT_ENTRIES ? pgt[li] : __ldg(bt + pg_lo + li);
             const uint32_t eb = smem_u32(&ctl->v_empty[k]);
@@ -287,7 +289,7 @@ __global__ void __launch_bounds__(DEC_THREADS, 1)
                 const int landed =
                     __shfl_sync(0xffffffffu, lane == 0 ? (int)mbar_wait(fb, use & 1u, abort) : 0, 0);
                 if (landed) {
-                    const int tail = kv_len - i * DEC_BN;
+                    const int tail = kv_len - (t_begin + it * DEC_BN);
                     const int r_end = min(DEC_BN, (tail + PAGE - 1) & ~(PAGE - 1));
                     uint8_t* vt = sm + OFF_V + k * DEC_TILE_BYTES;
                     for (int idx = lane; idx < (r_end - tail) * 16; idx += 32) {
@@ -379,7 +381,7 @@ __global__ void __launch_bounds__(DEC_THREADS, 1)
                 ok_ = mbar_wait(smem_u32(&ctl->k_empty[kx]), (uint32_t)(((itx / DEC_KSTAGES) & 1) ^ 1), abort);
                 if (ok_) {
                     const uint32_t kt_s = s_base + OFF_K + kx * DEC_TILE_BYTES;
-                    const int pages = n_pages - (i0 + itx) * PPT;  // pages of the tile on the row
+                    const int pages = pg_end - (pg_lo + itx * PPT);  // pages of the tile in the CTA's range
 #pragma unroll
                     for (int m = 0; m < XF_ROWS; ++m) {
                         const int pit = (r0 >> 4) + 2 * m;
@@ -438,11 +440,11 @@ __global__ void __launch_bounds__(DEC_THREADS, 1)
         // sequence), so at most XF_ANCHOR_TILES * XF_ROWS steps follow an anchor.
         float2 c[4], sn[4];
         for (int it = 0; it < n_loc && kok; ++it) {
-            const int i = i0 + it, k = it % DEC_KSTAGES;
+            const int k = it % DEC_KSTAGES;
             cp_async_wait<DEC_KAHEAD - 1>();  // this thread's chunks of tile it have landed
             uint8_t* kt = sm + OFF_K + k * DEC_TILE_BYTES;
-            const int t0 = i * DEC_BN;
-            if (it == 0 || i % XF_ANCHOR_TILES == 0) {
+            const int t0 = t_begin + it * DEC_BN;
+            if (it % XF_ANCHOR_TILES == 0) {
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
                     rope_cos_sin((uint32_t)(t0 + r0), ctl->turns[8 * u + 2 * e], c[e].x, sn[e].x);
@@ -461,7 +463,7 @@ __global__ void __launch_bounds__(DEC_THREADS, 1)
 #pragma unroll
             for (int m = 0; m < XF_ROWS; ++m) {
                 const int r = r0 + XF_ROW_STEP * m;
-                if (t0 + r < n_vis) {
+                if (t0 + r < t_end) {
                     range = rotate_regs_f16(lo[m], hi[m], c, sn, range);
                     const uint32_t off = sw128_off(r, u);
                     *reinterpret_cast<uint4*>(kt + off) = lo[m];
@@ -493,7 +495,7 @@ __global__ void __launch_bounds__(DEC_THREADS, 1)
         // at a barrier; a thread whose wait gave up skips its work until then.
         bool ok = true, failed = false;
         for (int it = 0; it < n_loc; ++it) {
-            const int i = i0 + it, sb = it & 1;
+            const int sb = it & 1;
             const bool got = mbar_wait(smem_u32(&ctl->s_full[sb]), (uint32_t)((it >> 1) & 1), abort);
             if (named_bar_or(1, 128, failed || !got)) {
                 ok = false;
@@ -505,7 +507,7 @@ __global__ void __launch_bounds__(DEC_THREADS, 1)
             tmem_ld_wait();
             tc_fence_before();
             mbar_arrive(smem_u32(&ctl->s_free[sb]));
-            const bool vis = i * DEC_BN + t < n_vis;
+            const bool vis = t_begin + it * DEC_BN + t < t_end;
             float x[8];
 #pragma unroll
             for (int h = 0; h < 8; ++h) {
@@ -585,7 +587,7 @@ __global__ void __launch_bounds__(DEC_THREADS, 1)
         for (int h = 0; h < 8; ++h) L[h] = ((ctl->lred[0][h] + ctl->lred[1][h]) + ctl->lred[2][h]) + ctl->lred[3][h];
         const bool range_bad = ctl->range_bad != 0;
         __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(a.out);
-        if (a.split_tiles > 0) {
+        if (a.split_tokens > 0) {
             // split partial: O / l in FP32 and m + log2(l) (log2 domain); the
             // merge rescales and sums the splits in ascending order
             uint32_t orow[16];
@@ -690,12 +692,12 @@ cudaError_t launch_decode(const CUtensorMap& vm, const DecodeArgs& a, cudaStream
         if (e != cudaSuccess) return e;
         configured.fetch_or(bit);
     }
-    const long long grid = (long long)a.B * a.Hkv * (a.split_tiles > 0 ? a.n_splits : 1);
+    const long long grid = (long long)a.B * a.Hkv * (a.split_tokens > 0 ? a.n_splits : 1);
     if (grid <= 0) return cudaSuccess;
     if (grid > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
     decode_kernel<<<(unsigned)grid, DEC_THREADS, DEC_SMEM_BYTES, stream>>>(vm, a);
     e = cudaGetLastError();
-    if (e != cudaSuccess || a.split_tiles <= 0) return e;
+    if (e != cudaSuccess || a.split_tokens <= 0) return e;
     decode_merge_kernel<<<(unsigned)((long long)a.B * a.Hq), HEAD_DIM, 0, stream>>>(a);
     return cudaGetLastError();
 }

@@ -248,7 +248,7 @@ const char* rk_paged_policy(void) {
            "pv_mma=bf16_operands_fp32_acc,l_merge=fixed_tree;"
            "prefill_tile=2xq128xkv128,score_mma=fp16_operands_fp32_acc,pv_mma=bf16_operands_fp32_acc;"
            "batch_invariant=1;page_size=16;head_dim=128;"
-           "decode_split_entry=fixed_splits_of_1024k_tokens,ordered_fp32_merge,separate_policy";
+           "decode_split_entry=fixed_splits_of_16k_tokens,ordered_fp32_merge,separate_policy";
 }
 
 int rk_paged_plan(rk_paged_plan_t* plan, int32_t B, int32_t Sq, int32_t Hq, int32_t Hkv, int32_t D,
@@ -410,7 +410,7 @@ int decode_common(const rk_paged_plan_t* plan, int32_t split_tokens, const void*
     a.timeout_drill = plan->timeout_drill;
     if (split_tokens > 0) {
         const int64_t n = (int64_t)plan->B * plan->Hq * split_count(plan, split_tokens);
-        a.split_tiles = split_tokens / rk::DEC_BN;
+        a.split_tokens = split_tokens;
         a.n_splits = (int32_t)split_count(plan, split_tokens);
         a.o_part = static_cast<float*>(scratch);
         a.lse_part = static_cast<float*>(scratch) + n * rk::HEAD_DIM;

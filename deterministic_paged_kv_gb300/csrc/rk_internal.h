@@ -39,11 +39,11 @@ struct DecodeArgs {
     int32_t* status;              // may be null
     int32_t B, Hq, Hkv, G, W, num_pages;
     float qk_scale_log2;          // sm_scale * log2(e)
-    // Fixed split of each row's KV range (0 = no split): split s covers KV
-    // tiles [s * split_tiles, (s + 1) * split_tiles); the CTA writes its
+    // Fixed split of each row's KV range (0 = no split): split s covers the
+    // keys [s * split_tokens, (s + 1) * split_tokens); the CTA writes its
     // partial O / l (FP32 [B, Hq, n_splits, D]) and log2-domain partial LSE
     // (FP32 [B, Hq, n_splits]; -inf when empty, NaN when unsafe) instead of out.
-    int32_t split_tiles;
+    int32_t split_tokens;         // a multiple of the page size
     int32_t n_splits;
     float* o_part;
     float* lse_part;
@@ -58,7 +58,7 @@ struct DecodeArgs {
     int32_t timeout_drill;        // nonzero: the score MMA issuer first waits on a barrier nothing completes
     uint64_t rope_turns[ROPE_PAIRS];
 };
-constexpr int DEC_SPLIT_GRAIN = 1024;  // split lengths are multiples of this many tokens (8 KV tiles)
+constexpr int DEC_SPLIT_GRAIN = PAGE;  // split lengths are multiples of the page size
 
 // ----------------------------------------------------------- prefill ----
 // One CTA per (row, KV head, q-tile).  A q-tile is 128 accumulator rows =

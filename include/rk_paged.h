@@ -203,7 +203,11 @@ int rk_paged_attn_prefill(const rk_paged_plan_t *plan, const void *q, const void
  * index) and "flashinfer_fa2 backend for Ada (SM89)", the no-split vs split
  * kernel table (the cost of disabling splits on long, low-batch rows).
  *
- *   split_tokens  a positive multiple of 1024 (RK_E_ARG otherwise).
+ *   split_tokens  a positive multiple of page_size = 16 (RK_E_ARG otherwise),
+ *                 as "WS2 PR7 ...", "Split-KV Policy" defines fixed:<N> in
+ *                 logical tokens.  Each split's CTA sweeps 128-token tiles from
+ *                 its first token, with exact RoPE angles at that token, so a
+ *                 split may start and end inside a 128-token tile.
  *   n_splits      = ceil(W * page_size / split_tokens), at least 1.
  *
  * rk_paged_decode_split_scratch_bytes -- *bytes = the device scratch the

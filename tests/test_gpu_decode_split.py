@@ -19,10 +19,12 @@ def _lib():
     binding.load()
 
 
-@pytest.mark.parametrize("split", [1024, 2048, 3072])
+@pytest.mark.parametrize("split", [16, 528, 1024, 2048, 3072])
 def test_split_decode_ragged_parity(split):
     """Rows shorter than, equal to and several times the split length, with a
-    ragged last page; every row against the oracle."""
+    ragged last page; every row against the oracle.  Split lengths are any
+    multiple of the page size: 16 (one page per split), 528 (splits that start
+    and end inside 128-token tiles), multiples of 1024."""
     kv = [1, 1000, 1024, 2048, 3000, 5003]
     w = workloads.random_case(len(kv), 1, 32, 8, 128, kv, seed=41, mode="decode", extra_pages=16)
     out, lse = run_gpu(w, split_tokens=split)
@@ -56,11 +58,11 @@ def test_split_decode_close_to_split_free():
     assert float((a_lse - b_lse).abs().max()) <= 1e-3
 
 
-def test_split_decode_batch_width_graph_invariance_bitwise():
+@pytest.mark.parametrize("split", [16, 528, 1024])
+def test_split_decode_batch_width_graph_invariance_bitwise(split):
     """For a fixed split length: the same row alone, reversed in the batch, at
     table widths 128 / 256 (more, empty splits), and under CUDA graph replay
     with new metadata contents -- bitwise equal."""
-    split = 1024
     w128 = workloads.decode_invariance(128)
     out, lse = run_gpu(w128, split_tokens=split)
     ro, rl = oracle_ref(w128)
@@ -152,7 +154,7 @@ def test_split_decode_argument_checks():
         binding.attn_decode_split(p, 1024, *args, small)
     assert e.value.name == "RK_E_ARG"
     ok = torch.empty(need, dtype=torch.uint8, device="cuda")
-    for bad in (0, 512, 1000, -1024):
+    for bad in (0, 8, 1000, -1024, 24 + 1):
         with pytest.raises(binding.RkError) as e:
             binding.attn_decode_split(p, bad, *args, ok)
         assert e.value.name == "RK_E_ARG"

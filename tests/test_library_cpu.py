@@ -186,15 +186,15 @@ def test_launch_without_gpu_fails_closed(rk):
 
 def test_split_decode_scratch_bytes_host_only(rk):
     """rk_paged_decode_split_scratch_bytes: B * Hq * ceil(W * 16 / split) *
-    (D + 1) * 4 bytes; split lengths that are not positive multiples of 1024
-    are rejected.  Host only."""
+    (D + 1) * 4 bytes; split lengths that are not positive multiples of the
+    page size (16) are rejected.  Host only."""
     p = rk.plan(3, 1, 32, 8, 128, 16, 600, 200)
-    for split in (1024, 2048, 3072):
+    for split in (16, 528, 1024, 2048, 3072):
         n_splits = -(-200 * 16 // split)
         assert rk.decode_split_scratch_bytes(p, split) == 3 * 32 * n_splits * 129 * 4
     p0 = rk.plan(2, 1, 32, 8, 128, 16, 0, 0)
     assert rk.decode_split_scratch_bytes(p0, 1024) == 2 * 32 * 1 * 129 * 4
-    for bad in (0, -1024, 512, 1500):
+    for bad in (0, -1024, 8, 1500, 1001):
         with pytest.raises(rk.RkError) as e:
             rk.decode_split_scratch_bytes(p, bad)
         assert e.value.name == "RK_E_ARG"

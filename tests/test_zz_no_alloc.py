@@ -34,7 +34,9 @@ def _run_both(w, split, d, p, scratch):
 
 def test_static_scratch_matches_caller_scratch_two_calls_in_a_row():
     for call, (kv, split, seed) in enumerate((([3000, 1100, 5003, 700], 1024, 61),
-                                             ([2048, 9000, 1], 2048, 67))):
+                                             ([2048, 9000, 1], 2048, 67),
+                                             ([300, 77, 1000], 528, 71),
+                                             ([300, 41], 16, 73))):
         w = workloads.random_case(len(kv), 1, 32, 8, 128, kv, seed=seed, mode="decode")
         d = to_dev(w)
         p = binding.plan(w.B, 1, w.Hq, w.Hkv, w.D, 16, w.num_pages, w.W, w.block_table, w.kv_lens,
