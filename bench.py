@@ -436,11 +436,11 @@ def measure_decode_long(args, dev, stream, hbm, peak_kind, splits=(1024, 1728, 2
 def measure_append(args, dev, stream, hbm, peak_kind):
     """Time rk_paged_kv_append for the prefill-chunk shape (4 rows x 512 new
     tokens) and the decode-step shape (64 rows x 1 token).  Inputs larger than
-    L2 instead of a flush: the launches cycle over enough distinct new-token
-    buffers that their K / V add up to more than the 129 MB L2, each launch
-    captured in its own CUDA graph and replayed back to back (a write flush
-    between launches would leave the L2 full of dirty lines that this small
-    kernel then pays to write back).  Bytes = new K and V read once and
+    L2 instead of a flush: one CUDA graph holds a launch per distinct
+    new-token buffer, enough of them that their K / V add up to more than the
+    129 MB L2 (a write flush between launches would leave the L2 full of dirty
+    lines that this small kernel then pays to write back), and the time of a
+    replay is divided by its launches.  Bytes = new K and V read once and
     written once."""
     import torch
 
@@ -460,30 +460,27 @@ def measure_append(args, dev, stream, hbm, peak_kind):
         for i in range(max(3, args.warmup)):
             binding.kv_append(p, n_new, k_new[i % n_sets], v_new[i % n_sets], bt, kl, kc, vc, stream=stream)
         torch.cuda.synchronize()
-        graphs = []
+        # all n_sets launches in one CUDA graph, each on its own input set: the
+        # graph runs them back to back (no per-launch host or graph overhead)
+        g = torch.cuda.CUDAGraph()
         s = torch.cuda.Stream()
         s.wait_stream(stream)
         with torch.cuda.stream(s):
-            for i in range(n_sets):
-                gi = torch.cuda.CUDAGraph()
-                with torch.cuda.graph(gi, stream=s):
+            with torch.cuda.graph(g, stream=s):
+                for i in range(n_sets):
                     binding.kv_append(p, n_new, k_new[i], v_new[i], bt, kl, kc, vc, stream=s)
-                graphs.append(gi)
         stream.wait_stream(s)
-        for gi in graphs:
-            gi.replay()
+        g.replay()
         torch.cuda.synchronize()
-        it = iter(range(10 ** 9))
-        t = time_launches(lambda: graphs[next(it) % n_sets].replay(), max(40, 2 * n_sets),
-                          torch.cuda.current_stream(dev))
+        t = [x / n_sets for x in time_launches(g.replay, 5, torch.cuda.current_stream(dev))]
         ms = sum(t) / len(t)
         byt = 2 * 2 * w.B * n_new * w.Hkv * w.D * 2
         res[name] = {"rows": w.B, "new_tokens_per_row": n_new, "bytes_per_launch": byt, "ms_per_launch": ms,
-                     "timing": "one launch per CUDA-graph replay, back to back over %d distinct input sets "
-                               "(%.1f MB of new K / V)" % (n_sets, n_sets * one / 1e6),
+                     "timing": "%d launches in one CUDA graph, back to back, each on its own input set "
+                               "(%.1f MB of new K / V in all); time per launch" % (n_sets, n_sets * one / 1e6),
                      "value": byt / (ms * 1e-3) / 1e9, "unit": "GB/s", "frac_of_peak": byt / (ms * 1e-3) / 1e9 / hbm,
                      "peak_kind": peak_kind}
-        del kc, vc, k_new, v_new, graphs
+        del kc, vc, k_new, v_new, g
     return res
 
 
