@@ -97,7 +97,7 @@ struct PfUnit {
 struct PfBars {
     uint64_t q_full, q_ready, q_empty;
     uint64_t k_full[KSTAGES], k_ready[KSTAGES], k_empty[KSTAGES];
-    uint64_t v_full[VSTAGES], v_empty[VSTAGES], v_tail;
+    uint64_t v_full[VSTAGES], v_empty[VSTAGES], v_land;  // v_land: the copy of a row's last V tile
     uint64_t s_full[2], p_ready[2], o_done[2], o_free[2];
     uint64_t u_full[2], u_empty[2];  // unit descriptor ring
     uint64_t r_full[2], r_empty[2];  // per-unit FP16 range verdict, transform -> softmax epilogues
@@ -422,7 +422,7 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
             mbar_init(smem_u32(&bars->v_full[k]), 1);
             mbar_init(smem_u32(&bars->v_empty[k]), 1);
         }
-        mbar_init(smem_u32(&bars->v_tail), 1);
+        mbar_init(smem_u32(&bars->v_land), 1);
         for (int j = 0; j < 2; ++j) {
             mbar_init(smem_u32(&bars->s_full[j]), 1);
             mbar_init(smem_u32(&bars->p_ready[j]), 128);
@@ -541,6 +541,8 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
             const int nst = is_k ? KSTAGES : VSTAGES;
             int n = 0;
             int v_owner0 = -1, v_owner1 = -1;  // unit that last loaded V stage 0 / 1
+            int nl = 0;                        // V tail tiles copied through v_land
+            bool land_open = false;            // the last of them was not seen landing
             bool ok = true;
             for (int k = 0; ok; ++k) {
                 PfUnit u;
@@ -552,7 +554,9 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
                 // The row's last page is in this unit's last tile and only partly
                 // filled: its cache rows past kv_len hold arbitrary bits and are
                 // zeroed in V after the copy lands (they meet P = 0, which would not
-                // cancel a non-finite value).
+                // cancel a non-finite value).  That copy lands on v_land, and v_full
+                // is completed (one plain arrival) only after the zeroing, so the
+                // MMA side waits on v_full alone whatever the tile holds.
                 const bool has_tail = u.n_keys == u.kv_len && (u.kv_len & (PAGE - 1)) != 0;
                 for (int i = 0; i < n_tiles; ++i, ++n) {
                     const int st = n % nst;
@@ -575,40 +579,47 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
                         fence_proxy_async_smem();
                         __syncwarp();
                     }
-                    if (lane == 0) mbar_arrive_expect_tx(fb, (uint32_t)np * 2 * 2048);
+                    const bool tail_tile = !is_k && has_tail && i == n_tiles - 1;
+                    const uint32_t lb = tail_tile ? smem_u32(&bars->v_land) : fb;
+                    if (lane == 0) mbar_arrive_expect_tx(lb, (uint32_t)np * 2 * 2048);
                     __syncwarp();
                     if (lane < np) {
                         if (is_k) {  // two 16 x 64 boxes per page: the K-major tile layout
                             const uint32_t t = s_base + OFF_K + st * PF_TILE_BYTES + lane * 2048;
-                            tma_load_3d(t, map, fb, 0, u.kvh, pg * PAGE);
-                            tma_load_3d(t + 16384, map, fb, 64, u.kvh, pg * PAGE);
+                            tma_load_3d(t, map, lb, 0, u.kvh, pg * PAGE);
+                            tma_load_3d(t + 16384, map, lb, 64, u.kvh, pg * PAGE);
                         } else {     // one 4 KiB box per page: [page][half][16 rows][128 B]
-                            tma_load_4d(s_base + OFF_V + st * PF_TILE_BYTES + lane * 4096, map, fb, 0, pg * PAGE, 0,
+                            tma_load_4d(s_base + OFF_V + st * PF_TILE_BYTES + lane * 4096, map, lb, 0, pg * PAGE, 0,
                                         u.kvh);
                         }
                     }
                     __syncwarp();
-                    if (!is_k && has_tail && i == n_tiles - 1) {
-                        // this warp armed the phase it waits for: no parity aliasing
-                        const int ok_full =
-                            __shfl_sync(0xffffffffu, lane == 0 ? (int)mbar_wait(fb, use & 1u, abort) : 0, 0);
-                        if (ok_full) {
-                            const int tail = u.kv_len - i * PF_BN;
-                            const int r_end = min(PF_BN, (tail + PAGE - 1) & ~(PAGE - 1));
-                            for (int idx = lane; idx < (r_end - tail) * 16; idx += 32) {
-                                const int rr = tail + (idx >> 4), ch = idx & 15;
-                                *reinterpret_cast<uint4*>(vt + (rr >> 4) * 4096 + (ch >> 3) * 2048 + (rr & 15) * 128 +
-                                                          (ch & 7) * 16) = make_uint4(0, 0, 0, 0);
-                            }
-                            fence_proxy_async_smem();
-                            __syncwarp();
-                            if (lane == 0) mbar_arrive(smem_u32(&bars->v_tail));
+                    if (tail_tile) {
+                        // this warp is v_land's only waiter and waits each phase it armed
+                        const int landed =
+                            __shfl_sync(0xffffffffu, lane == 0 ? (int)mbar_wait(lb, (uint32_t)(nl & 1), abort) : 0, 0);
+                        ++nl;
+                        if (!landed) {
+                            land_open = true;
+                            ok = false;
+                            break;
                         }
+                        const int tail = u.kv_len - i * PF_BN;
+                        const int r_end = min(PF_BN, (tail + PAGE - 1) & ~(PAGE - 1));
+                        for (int idx = lane; idx < (r_end - tail) * 16; idx += 32) {
+                            const int rr = tail + (idx >> 4), ch = idx & 15;
+                            *reinterpret_cast<uint4*>(vt + (rr >> 4) * 4096 + (ch >> 3) * 2048 + (rr & 15) * 128 +
+                                                      (ch & 7) * 16) = make_uint4(0, 0, 0, 0);
+                        }
+                        fence_proxy_async_smem();
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(fb);
                     }
                 }
             }
             if (lane == 0 && pipe_aborted(abort)) {
                 // the copies this warp issued land before the CTA's shared memory is released
+                if (land_open) mbar_wait_drain(smem_u32(&bars->v_land), (uint32_t)((nl - 1) & 1));
                 for (int i = max(0, n - nst); i < n; ++i)
                     mbar_wait_drain(smem_u32(is_k ? &bars->k_full[i % nst] : &bars->v_full[i % nst]),
                                     (uint32_t)((i / nst) & 1));
@@ -626,8 +637,8 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
             const uint32_t dK0 = desc_lo(s_base + OFF_K, 16);
             const uint32_t dV0 = desc_lo(s_base + OFF_V, 2048);
             // Phase state over the CTA's units, packed: g = KV tiles before the
-            // unit (stage and phase of the K and V rings); ph bit 0 q_ready, bit 1
-            // v_tail, bits 2 + j s_full / p_ready of q-tile j, bits 4 + j o_free.
+            // unit (stage and phase of the K and V rings); ph bit 0 q_ready, bits
+            // 2 + j s_full / p_ready of q-tile j, bits 4 + j o_free.
             int g0 = 0;
             uint32_t ph = 0;
             bool ok = !a.timeout_drill || drill_wait(smem_u32(&bars->never), abort);
@@ -637,7 +648,6 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
                 const int n_tiles = max(u.nt0, u.nt1);
                 if (u.bad || n_tiles == 0) continue;
                 const int nt0 = u.nt0, nt1 = u.nt1;
-                const bool has_tail = u.n_keys == u.kv_len && (u.kv_len & (PAGE - 1)) != 0;
                 if (!(ok = mbar_wait(smem_u32(&bars->q_ready), ph & 1u, abort))) break;
                 int v_seen = -1;  // last V tile whose arrival (and tail zeroing) was observed
                 // O_j += P_j(i) V(i).  implied: P_j(i) was published after K(i+1) was
@@ -653,8 +663,6 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
                     const int g = g0 + i;
                     if (!implied && v_seen != i) {
                         if (!mbar_wait(smem_u32(&bars->v_full[g % VSTAGES]), (uint32_t)((g / VSTAGES) & 1), abort))
-                            return false;
-                        if (has_tail && i == n_tiles - 1 && !mbar_wait(smem_u32(&bars->v_tail), (ph >> 1) & 1u, abort))
                             return false;
                         v_seen = i;
                     }
@@ -704,7 +712,7 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
                 }
                 if (!ok) break;
                 umma_commit(smem_u32(&bars->v_empty[(g0 + n_tiles - 1) % VSTAGES]));  // V(last) read by the last PVs
-                ph ^= 1u | (has_tail ? 2u : 0u) | ((uint32_t)(nt0 & 1) << 2) | ((uint32_t)(nt1 & 1) << 3) |
+                ph ^= 1u | ((uint32_t)(nt0 & 1) << 2) | ((uint32_t)(nt1 & 1) << 3) |
                       (nt0 > 0 ? 16u : 0u) | (nt1 > 0 ? 32u : 0u);
                 g0 += n_tiles;
             }

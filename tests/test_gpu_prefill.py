@@ -54,6 +54,22 @@ def test_prefill_single_query_and_empty_row():
     assert_parity(out, lse, ro, rl)
 
 
+def test_prefill_back_to_back_tail_units():
+    """Many short rows: every unit is a single KV tile whose last page is partly
+    filled, and each CTA of the persistent grid runs several of them in a row,
+    so the zeroing of one unit's V tail overlaps the next unit's copies."""
+    rng = np.random.default_rng(31)
+    kv = [int(x) for x in rng.integers(40, 128, size=48)]
+    kv = [x + 1 if x % 16 == 0 else x for x in kv]
+    w = workloads.random_case(len(kv), 40, 32, 8, 128, kv, seed=37, mode="prefill")
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    out, lse = run_gpu(w, status=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    ro, rl = oracle_ref(w)
+    assert_parity(out, lse, ro, rl)
+
+
 def test_prefill_chunk_config_parity():
     """B=4, 1536-token prefix + 512-token chunk: every output vs the oracle."""
     w = workloads.prefill_chunk()
