@@ -765,7 +765,7 @@ __global__ void __launch_bounds__(PF_THREADS, 1)
                         rope_cos_sin((uint32_t)(t0 + r0), bars->turns[8 * u8 + 2 * e + 1], c[e].y, sn[e].y);
                     }
                 }
-#pragma unroll 2
+#pragma unroll 1
                 for (int m = 0; m < 8; ++m) {
                     const int r = r0 + 16 * m;
                     const uint32_t off = sw_off(r, u8);
