@@ -11,7 +11,9 @@ Names mirror the C ABI in ``include/rk_paged.h``:
 ``attn_prefill`` (rk_paged_attn_prefill), ``decode_split_scratch_bytes``
 (rk_paged_decode_split_scratch_bytes), ``attn_decode_split``
 (rk_paged_attn_decode_split), ``attn_decode_split_static``
-(rk_paged_attn_decode_split_static), ``kv_append`` (rk_paged_kv_append),
+(rk_paged_attn_decode_split_static), ``decode_balanced_scratch_bytes``
+(rk_paged_decode_balanced_scratch_bytes), ``attn_decode_balanced``
+(rk_paged_attn_decode_balanced), ``kv_append`` (rk_paged_kv_append),
 ``plan_ragged`` (rk_paged_plan_ragged), ``attn_ragged`` (rk_paged_attn_ragged),
 ``last_error``, ``policy``, ``abi_version``.
 """
@@ -33,6 +35,7 @@ CODES = {v: k for k, v in ERRORS.items()}
 STATUS_PAGE_OOB, STATUS_KVLEN, STATUS_POSITION, STATUS_TIMEOUT, STATUS_RANGE = 1, 2, 4, 8, 16
 ABI_VERSION = 3
 SPLIT_STATIC_SCRATCH_BYTES = 16 << 20  # RK_PAGED_SPLIT_STATIC_SCRATCH_BYTES
+BALANCED_SCRATCH_BYTES = 4096 + 512 * 3088 * 4  # RK_PAGED_BALANCED_SCRATCH_BYTES
 
 
 class RkError(RuntimeError):
@@ -87,6 +90,10 @@ def load(path: str | None = None):
         lib.rk_paged_attn_decode_split.restype = ctypes.c_int
         lib.rk_paged_attn_decode_split.argtypes = [ctypes.POINTER(Plan), ctypes.c_int32] + [vp] * 9 + \
             [ctypes.c_uint64, vp, vp]
+        lib.rk_paged_decode_balanced_scratch_bytes.restype = ctypes.c_int
+        lib.rk_paged_decode_balanced_scratch_bytes.argtypes = [ctypes.POINTER(Plan), ctypes.POINTER(ctypes.c_uint64)]
+        lib.rk_paged_attn_decode_balanced.restype = ctypes.c_int
+        lib.rk_paged_attn_decode_balanced.argtypes = [ctypes.POINTER(Plan)] + [vp] * 9 + [ctypes.c_uint64, vp, vp]
         lib.rk_paged_attn_decode_split_static.restype = ctypes.c_int
         lib.rk_paged_attn_decode_split_static.argtypes = [ctypes.POINTER(Plan), ctypes.c_int32] + [vp] * 10
         lib.rk_paged_kv_append.restype = ctypes.c_int
@@ -308,6 +315,37 @@ def attn_decode_split(p: Plan, split_tokens, q, k_cache, v_cache, block_table, k
         ctypes.byref(p), int(split_tokens), _dptr(q), _dptr(k_cache), _dptr(v_cache), _dptr(block_table),
         _dptr(kv_lens), _dptr(position_ids), _dptr(out), _dptr(lse), _dptr(scratch), nbytes, _dptr(status),
         _stream(stream))
+    _check(rc)
+
+
+def decode_balanced_scratch_bytes(p: Plan) -> int:
+    """rk_paged_decode_balanced_scratch_bytes: device scratch bytes of the balanced decode."""
+    n = ctypes.c_uint64(0)
+    _check(load().rk_paged_decode_balanced_scratch_bytes(ctypes.byref(p), ctypes.byref(n)))
+    return int(n.value)
+
+
+def attn_decode_balanced(p: Plan, q, k_cache, v_cache, block_table, kv_lens, position_ids, out, lse, scratch,
+                         status=None, stream=None):
+    """rk_paged_attn_decode_balanced on device tensors: the split-free decode on a
+    balanced schedule (results bitwise equal to ``attn_decode``).  ``scratch`` is
+    a CUDA tensor of at least ``decode_balanced_scratch_bytes`` bytes (any dtype,
+    256-byte aligned), zeroed once before its first use and then reused by one
+    call at a time."""
+    import torch
+    for t, dt, name in ((q, torch.bfloat16, "q"), (k_cache, torch.bfloat16, "k_cache"),
+                        (v_cache, torch.bfloat16, "v_cache"), (out, torch.bfloat16, "out"),
+                        (lse, torch.float32, "lse"), (block_table, torch.int32, "block_table"),
+                        (kv_lens, torch.int32, "kv_lens"), (position_ids, torch.int32, "position_ids")):
+        if t.dtype != dt:
+            raise TypeError("%s must be %s (got %s)" % (name, dt, t.dtype))
+    if status is not None and status.dtype != torch.int32:
+        raise TypeError("status must be int32")
+    _check_shapes(p, q, k_cache, v_cache, block_table, kv_lens, position_ids, out, lse, status)
+    nbytes = scratch.numel() * scratch.element_size()
+    rc = load().rk_paged_attn_decode_balanced(
+        ctypes.byref(p), _dptr(q), _dptr(k_cache), _dptr(v_cache), _dptr(block_table), _dptr(kv_lens),
+        _dptr(position_ids), _dptr(out), _dptr(lse), _dptr(scratch), nbytes, _dptr(status), _stream(stream))
     _check(rc)
 
 

@@ -89,6 +89,12 @@ struct DecCtrl {
     float2 step[ROPE_PAIRS];  // cos/sin of an XF_ROW_STEP-position turn per pair
     float red[2][4][8];  // per-warp tile maxima, double-buffered by tile parity
     float lred[4][8];    // per-warp partial l at the end
+    // balanced schedule
+    uint32_t epoch;                     // this launch's epoch (hand-off flags carry epoch + 1)
+    int imp_ok;                         // the imported state arrived
+    int n_seg;                          // the CTA's segments, in processing order:
+    int seg[DEC_BAL_MAX_SEGS][4];       // (row * Hkv + KV head, first tile, end tile, flags)
+    int scan[DEC_THREADS / 32];         // per-warp block counts (set-up scan)
 };
 static_assert(sizeof(DecCtrl) <= DEC_CTRL_BYTES, "decode control block exceeds its reservation");
 
@@ -113,29 +119,169 @@ __device__ __forceinline__ void write_empty_row(const DecodeArgs& a, int b, int 
     if (threadIdx.x < a.G) a.lse[(size_t)tq * a.Hq + h0 + threadIdx.x] = lse_val;
 }
 
-__global__ void __launch_bounds__(DEC_THREADS, 1)
-    decode_kernel(const __grid_constant__ CUtensorMap vmap, const __grid_constant__ DecodeArgs a) {
-    extern __shared__ __align__(1024) uint8_t sm[];
-    // A launch that only reads what this grid reads (the prefill rows of a
-    // ragged batch) may fill the SMs this grid's last wave leaves idle.
-    griddep_launch_dependents();
-    DecCtrl* ctl = reinterpret_cast<DecCtrl*>(sm + OFF_CTRL);
-    const uint32_t s_base = smem_u32(sm);
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    // work unit: (split, row, KV head), split-major; split = 0 without splitting
-    const int rows_heads = a.B * a.Hkv;
-    const int split = (int)(blockIdx.x / rows_heads), unit = (int)(blockIdx.x % rows_heads);
-    const int kvh = unit % a.Hkv, b = unit / a.Hkv;
-    const int G = a.G, h0 = kvh * G;
-    if (s_base & 1023u) {  // the swizzled operand layout needs a 1024-byte aligned base
-        if (tid == 0 && a.status) atomicOr(a.status, RK_STATUS_TIMEOUT);
-        // Nothing was computed: padded rows (and split partials, which the merge
-        // then turns into out = 0, lse = NaN) are written as failed.  A ragged
-        // row's packed index is not known here; the status bit reports it.
-        if (!a.qo_indptr) write_empty_row(a, b, b, h0, split, __int_as_float(0x7fc00000));
-        return;
-    }
+// ------------------------------------------------ balanced schedule ----
+constexpr int DEC_SEG_IMPORT = 1, DEC_SEG_EXPORT = 2;  // segment flags
 
+__device__ __forceinline__ uint32_t ld_acquire_u32(const uint32_t* p) {
+    uint32_t v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+__device__ __forceinline__ void st_release_u32(uint32_t* p, uint32_t v) {
+    asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+// Wait until a hand-off flag holds `want`, within the launch's wait limit (then
+// the CTA's pipeline is aborted and 0 returned).
+__device__ __forceinline__ int bal_wait(const uint32_t* flag, uint32_t want, PipeCtl* pc) {
+    if (ld_acquire_u32(flag) == want) return 1;
+    const uint64_t t0 = global_timer_ns();
+    while (true) {
+        __nanosleep(256);
+        if (ld_acquire_u32(flag) == want) return 1;
+        if (pipe_aborted(pc)) return 0;
+        if (global_timer_ns() - t0 > pc->limit_ns) {
+            *reinterpret_cast<volatile int*>(&pc->abort) = 1;
+            return 0;
+        }
+    }
+}
+
+// A segment that hands its row on but could not compute it (unsafe metadata):
+// the hand-off says so, and the segment that ends the row writes it as failed.
+__device__ __forceinline__ void export_failed(const DecodeArgs& a, const DecCtrl* ctl) {
+    if (threadIdx.x == 0) {
+        float* st = a.bal_state + (size_t)blockIdx.x * DEC_BAL_STATE_FLOATS;
+        __stcg(st + DEC_BAL_INFO, 0.0f);
+        __threadfence();
+        st_release_u32(a.bal_sync + DEC_BAL_SYNC_WORDS + blockIdx.x, ctl->epoch + 1u);
+    }
+}
+
+// Called once by every CTA of a balanced launch as it leaves: the last one
+// resets the count and advances the epoch, so the next launch's flags (epoch
+// + 1 then) never match a flag this launch left.
+__device__ __forceinline__ void bal_done(const DecodeArgs& a) {
+    __threadfence();
+    if (atomicAdd(a.bal_sync + 1, 1u) == (uint32_t)gridDim.x - 1u) {
+        *reinterpret_cast<volatile uint32_t*>(a.bal_sync + 1) = 0u;
+        __threadfence();
+        atomicAdd(a.bal_sync, 1u);
+    }
+}
+
+// This CTA's segments.  The grid is Hkv chains of grid / Hkv CTAs: CTA c
+// serves KV head h = c % Hkv as member g = c / Hkv of its chain.  Every row gets
+// max(1, ceil(tiles / 8)) blocks (the tiles of its visible keys, 8 to a block),
+// laid end to end in row order; member g takes blocks [g L, (g + 1) L), L =
+// ceil(total / members), of head h.  All heads of a row have the same blocks,
+// so the Hkv CTAs of a member index read the same pages (the heads share them)
+// at the same time.  A row cut at g L is taken over from member g - 1 (import,
+// done last: by then that CTA has handed it on, having done it first); a row
+// cut at (g + 1) L is handed to member g + 1 (export, done first).  The rows'
+// block counts use the K ring as scratch (it is not in use yet).
+__device__ __forceinline__ void bal_schedule(const DecodeArgs& a, uint8_t* sm, DecCtrl* ctl) {
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    int* nbs = reinterpret_cast<int*>(sm + OFF_K);  // blocks of row b
+    int* pre = nbs + DEC_BAL_MAX_ROWS;               // blocks of the rows before b
+    static_assert(2 * DEC_BAL_MAX_ROWS * 4 <= DEC_KSTAGES * DEC_TILE_BYTES, "set-up scratch exceeds the K ring");
+    static_assert(DEC_BAL_BLOCK_TILES % XF_ANCHOR_TILES == 0, "segments must start on a RoPE anchor tile");
+    const int B = a.B <= DEC_BAL_MAX_ROWS ? a.B : 0;  // more rows are ruled out by the host; none taken here
+    const int per = (B + DEC_THREADS - 1) / DEC_THREADS;  // contiguous rows per thread
+    const int r0 = min(B, tid * per), r1 = min(B, r0 + per);
+    int sum = 0;
+    for (int r = r0; r < r1; ++r) {
+        const int kv = a.kv_lens[r], qp = a.position_ids[r];
+        const int nv = (kv < 0 || kv > a.W * PAGE || qp < 0) ? 0 : (qp >= kv ? kv : qp + 1);
+        const int nt = (nv + DEC_BN - 1) / DEC_BN;
+        const int nb = max(1, (nt + DEC_BAL_BLOCK_TILES - 1) / DEC_BAL_BLOCK_TILES);
+        nbs[r] = nb;
+        sum += nb;
+    }
+    int inc = sum;  // inclusive scan over the warp, then over the warps
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+        const int v = __shfl_up_sync(0xffffffffu, inc, off);
+        if (lane >= off) inc += v;
+    }
+    if (lane == 31) ctl->scan[warp] = inc;
+    if (tid == 0) ctl->epoch = __ldcg(a.bal_sync);  // the previous launch's last CTA advanced it in L2
+    __syncthreads();
+    int wbase = 0, total = 0;
+#pragma unroll 1
+    for (int w = 0; w < DEC_THREADS / 32; ++w) {
+        const int v = ctl->scan[w];
+        if (w < warp) wbase += v;
+        total += v;
+    }
+    int base = wbase + inc - sum;
+    for (int r = r0; r < r1; ++r) {
+        pre[r] = base;
+        base += nbs[r];
+    }
+    __syncthreads();
+    if (tid == 0) {
+        const int Hkv = a.Hkv, members = (int)gridDim.x / Hkv;
+        const int h = (int)blockIdx.x % Hkv, g = (int)blockIdx.x / Hkv;
+        const long long T = total;
+        const long long L = members > 0 ? (T + members - 1) / members : 0;
+        const long long lo = g < members ? (long long)g * L : T, hi = min(T, lo + L);
+        int sg[DEC_BAL_MAX_SEGS][4];
+        int n = 0;
+        if (B != a.B && blockIdx.x == 0 && a.status) atomicOr(a.status, RK_STATUS_TIMEOUT);
+        if (lo < hi) {
+            int bl = 0, bh = B - 1;  // the last row b with pre[b] <= lo
+            while (bl < bh) {
+                const int mid = (bl + bh + 1) >> 1;
+                if ((long long)pre[mid] <= lo) bl = mid; else bh = mid - 1;
+            }
+            int b = bl;
+            long long P = pre[b];  // first block of row b
+            while (P < hi && n < DEC_BAL_MAX_SEGS) {
+                const int nb = nbs[b];
+                const long long blo = P > lo ? P : lo, bhi = P + nb < hi ? P + nb : hi;
+                sg[n][0] = b * Hkv + h;
+                sg[n][1] = (int)(blo - P) * DEC_BAL_BLOCK_TILES;
+                sg[n][2] = (int)(bhi - P) * DEC_BAL_BLOCK_TILES;
+                sg[n][3] = (P < lo ? DEC_SEG_IMPORT : 0) | (P + nb > hi ? DEC_SEG_EXPORT : 0);
+                ++n;
+                P += nb;
+                ++b;
+            }
+            if (P < hi) {  // more segments than a CTA holds: ruled out by the host; reported, not computed
+                n = 0;
+                if (a.status) atomicOr(a.status, RK_STATUS_TIMEOUT);
+            }
+        }
+        // processing order: the one handed on, the whole ones, the one taken over
+        int k = 0;
+        const bool ex_last = n > 1 && (sg[n - 1][3] & DEC_SEG_EXPORT);
+        const bool im_first = n > 1 && (sg[0][3] & DEC_SEG_IMPORT);
+        auto put = [&](int i) {
+#pragma unroll
+            for (int q = 0; q < 4; ++q) ctl->seg[k][q] = sg[i][q];
+            ++k;
+        };
+        if (ex_last) put(n - 1);
+        for (int i = 0; i < n; ++i)
+            if (!(i == n - 1 && ex_last) && !(i == 0 && im_first)) put(i);
+        if (im_first) put(0);
+        ctl->n_seg = n;
+    }
+    __syncthreads();
+}
+
+// One segment of one (row, KV head): the keys [t_begin, min(visible, t_cap))
+// swept in tiles of 128 tokens by the whole CTA, with the row's result written
+// at the end, or (flags) the running state taken over from the previous CTA
+// and / or handed to the next.  The CTA's barriers are set up afresh for each
+// segment; TMEM is the CTA's for its whole life.
+__device__ __forceinline__ void decode_segment(const CUtensorMap& vmap, const DecodeArgs& a, uint8_t* sm,
+                                               DecCtrl* ctl, const uint32_t s_base, const uint32_t tmem,
+                                               const int b, const int kvh, const int split, const int t_begin,
+                                               const int t_cap, const int flags) {
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int G = a.G, h0 = kvh * G;
     // ---- row metadata (device copy) and memory-safety checks ----
     int tq = b;  // the row's query: padded row b, or its packed row in a ragged batch
     if (a.qo_indptr) {
@@ -154,15 +300,14 @@ __global__ void __launch_bounds__(DEC_THREADS, 1)
     const int qpos = a.position_ids[tq];
     const int32_t* bt = a.block_table + (size_t)b * a.W;
     constexpr int PPT = DEC_BN / PAGE;  // pages per tile
-    // This CTA's keys start at token t_begin: 0, or split * split_tokens (a
-    // multiple of the page size) for a fixed split.  Its tiles are 128 tokens
-    // counted from there.
-    const int t_begin = a.split_tokens > 0 ? split * a.split_tokens : 0;
-    // The page ids of the CTA's part of the table are loaded before its length
-    // is known (the metadata costs one round trip, not two) and judged against
-    // the visible range below.
+    // This segment's keys start at token t_begin (0, a fixed split's first
+    // token, or a balanced segment's first tile) and end before t_cap, both
+    // multiples of the page size.  Its tiles are 128 tokens counted from t_begin.
+    // The page ids of the segment's part of the table are loaded before its
+    // length is known (the metadata costs one round trip, not two) and judged
+    // against the visible range below.
     const int pg_lo = t_begin / PAGE;
-    const int pg_cap = a.split_tokens > 0 ? min(a.W, pg_lo + a.split_tokens / PAGE) : a.W;
+    const int pg_cap = min(a.W, t_cap / PAGE);
     constexpr int PRE = 4;  // table entries per thread held from the early load
     int pre[PRE];
 #pragma unroll
@@ -174,13 +319,12 @@ __global__ void __launch_bounds__(DEC_THREADS, 1)
     if (kv_len < 0 || kv_len > a.W * PAGE) bad |= RK_STATUS_KVLEN;
     if (qpos < 0) bad |= RK_STATUS_POSITION;
     const int n_vis = bad ? 0 : (qpos >= kv_len ? kv_len : qpos + 1);
-    // This CTA's keys [t_begin, t_end): the row's visible keys, or those of one
-    // fixed split, in n_loc tiles of 128 tokens from t_begin.
-    const int t_end = a.split_tokens > 0 ? min(n_vis, t_begin + a.split_tokens) : n_vis;
+    // The segment's keys [t_begin, t_end), in n_loc tiles of 128 tokens from t_begin.
+    const int t_end = min(n_vis, t_cap);
     const int n_loc = t_end > t_begin ? (t_end - t_begin + DEC_BN - 1) / DEC_BN : 0;
     // Last page partly filled and inside the visible range: its rows past
     // kv_len hold arbitrary bits and are zeroed in V after the copy lands
-    // (by the CTA that holds the row's last key).
+    // (by the segment that holds the row's last key).
     const bool has_tail = n_vis == kv_len && (kv_len & (PAGE - 1)) != 0 && n_loc > 0 && t_end == n_vis;
     int oob = 0;
     const int pg_end = (t_end + PAGE - 1) / PAGE;  // the pages this CTA reads: [pg_lo, pg_end)
@@ -237,24 +381,18 @@ __global__ void __launch_bounds__(DEC_THREADS, 1)
         reinterpret_cast<uint4*>(sm + OFF_V)[i] = make_uint4(0, 0, 0, 0);
     fence_proxy_async_smem();
     if (__syncthreads_or(oob)) bad |= RK_STATUS_PAGE_OOB;
-    if (bad) {
-        if (tid == 0 && a.status) atomicOr(a.status, bad);
-        write_empty_row(a, b, tq, h0, split, __int_as_float(0x7fc00000));
+    const bool imp = (flags & DEC_SEG_IMPORT) != 0, exp_ = (flags & DEC_SEG_EXPORT) != 0;
+    if (bad || n_loc == 0) {
+        // unsafe metadata: the row is written as failed (here, or by the
+        // segment that ends it, told through the hand-off); no visible key: empty
+        if (bad && tid == 0 && a.status) atomicOr(a.status, bad);
+        if (exp_)
+            export_failed(a, ctl);
+        else
+            write_empty_row(a, b, tq, h0, split, (bad || imp) ? __int_as_float(0x7fc00000) : -INFINITY);
+        __syncthreads();
         return;
     }
-    if (n_loc == 0) {
-        write_empty_row(a, b, tq, h0, split, -INFINITY);
-        return;
-    }
-
-    if (warp == WARP_MMA) {
-        tmem_alloc(smem_u32(&ctl->tmem_base), TMEM_COLS);
-        tmem_relinquish();
-    }
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
-    const uint32_t tmem = ctl->tmem_base;
     const uint32_t tO = tmem + 32;
     PipeCtl* abort = &ctl->pipe;
 
@@ -337,6 +475,11 @@ __global__ void __launch_bounds__(DEC_THREADS, 1)
                     umma_commit_elect(smem_u32(&ctl->s_full[sb]));
                     umma_commit_elect(smem_u32(&ctl->k_empty[k]));
                 }
+                // every commit of this thread has arrived before the barriers are
+                // set up again for the CTA's next segment
+                for (int it = max(0, n_loc - DEC_KSTAGES); it < n_loc && ok; ++it)
+                    ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&ctl->k_empty[it % DEC_KSTAGES]),
+                                                           (uint32_t)((it / DEC_KSTAGES) & 1), abort));
             } else {
                 const uint32_t idO = idesc_bf16_f32(HEAD_DIM, NH, 1, 0);
                 const uint32_t dV0 = desc_lo(s_base + OFF_V, 2048), dPT = desc_lo(s_base + OFF_PT, 16);
@@ -350,11 +493,17 @@ __global__ void __launch_bounds__(DEC_THREADS, 1)
                     tc_fence_after();
                     mma_ss_steps<0, 8, MN_MAJOR_PAGE, K_MAJOR_16, true>(tO, dV0 + (uint32_t)(it % DEC_VSTAGES) * TILE_DESC,
                                                              dPT + (uint32_t)(it & 1) * (PT_BYTES >> 4), idO,
-                                                             it > 0 ? 1u : 0u);
+                                                             (it > 0 || imp) ? 1u : 0u);
                     umma_commit_elect(smem_u32(&ctl->pv_done[it & 1]));
                     umma_commit_elect(smem_u32(&ctl->v_empty[it % DEC_VSTAGES]));
                 }
                 if (ok) umma_commit_elect(smem_u32(&ctl->o_done));
+                for (int it = max(0, n_loc - DEC_VSTAGES); it < n_loc && ok; ++it)
+                    ok = __all_sync(0xffffffffu, mbar_wait(smem_u32(&ctl->v_empty[it % DEC_VSTAGES]),
+                                                           (uint32_t)((it / DEC_VSTAGES) & 1), abort));
+                for (int it = max(0, n_loc - 2); it < n_loc && ok; ++it)
+                    ok = __all_sync(0xffffffffu,
+                                    mbar_wait(smem_u32(&ctl->pv_done[it & 1]), (uint32_t)((it >> 1) & 1), abort));
             }
             if (!ok) {
                 const uint64_t t0 = global_timer_ns();  // let issued MMAs drain before TMEM is released
@@ -493,7 +642,37 @@ __global__ void __launch_bounds__(DEC_THREADS, 1)
         // Every wait result is OR-reduced over the warpgroup at named barrier 1,
         // so the four warps leave the loop together and never strand one another
         // at a barrier; a thread whose wait gave up skips its work until then.
-        bool ok = true, failed = false;
+        bool ok = true, failed = false, quiet = false;
+        if (imp) {
+            // The previous CTA's hand-off of this row: m, this lane's l partial
+            // and this output dim's O^T row (into TMEM, where the PVs go on
+            // accumulating).  The wait is bounded like every other.
+            if (t == 0)
+                ctl->imp_ok = bal_wait(a.bal_sync + DEC_BAL_SYNC_WORDS + (blockIdx.x - a.Hkv), ctl->epoch + 1u, abort);
+            named_bar_sync(1, 128);
+            const bool arrived = ctl->imp_ok != 0;
+            const float* st = a.bal_state + (size_t)(blockIdx.x - a.Hkv) * DEC_BAL_STATE_FLOATS;
+            if (arrived) (void)ld_acquire_u32(a.bal_sync + DEC_BAL_SYNC_WORDS + (blockIdx.x - a.Hkv));
+            if (arrived && __ldcg(st + DEC_BAL_INFO) != 0.0f) {
+#pragma unroll
+                for (int h = 0; h < 8; ++h) {
+                    m[h] = __ldcg(st + DEC_BAL_M + h);
+                    lp[h] = __ldcg(st + DEC_BAL_LP + t * 8 + h);
+                }
+                uint32_t orow[16];
+#pragma unroll
+                for (int c = 0; c < 16; ++c) orow[c] = __float_as_uint(__ldcg(st + DEC_BAL_O + t * 16 + c));
+                tmem_st16(tO + lane_addr, orow);
+                tmem_st_wait();
+                if (t == 0 && __ldcg(st + DEC_BAL_INFO + 1) != 0.0f) ctl->range_bad = 1;
+            } else {
+                // the row failed before this segment (reported there) or its state
+                // never came (reported here): the pipeline stops at once
+                failed = true;
+                quiet = arrived;
+                *reinterpret_cast<volatile int*>(&abort->abort) = 1;
+            }
+        }
         for (int it = 0; it < n_loc; ++it) {
             const int sb = it & 1;
             const bool got = mbar_wait(smem_u32(&ctl->s_full[sb]), (uint32_t)((it >> 1) & 1), abort);
@@ -552,7 +731,7 @@ __global__ void __launch_bounds__(DEC_THREADS, 1)
                 continue;
             }
             tc_fence_after();
-            if (resc && it >= 1) {
+            if (resc && (it >= 1 || imp)) {  // O^T of earlier tiles (this segment's or imported)
                 uint32_t orow[16];
                 tmem_ld16(tO + lane_addr, orow);
                 tmem_ld_wait();
@@ -587,7 +766,34 @@ __global__ void __launch_bounds__(DEC_THREADS, 1)
         for (int h = 0; h < 8; ++h) L[h] = ((ctl->lred[0][h] + ctl->lred[1][h]) + ctl->lred[2][h]) + ctl->lred[3][h];
         const bool range_bad = ctl->range_bad != 0;
         __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(a.out);
-        if (a.split_tokens > 0) {
+        if (exp_) {
+            // hand the running state to the next CTA, which goes on with the row
+            float* st = a.bal_state + (size_t)blockIdx.x * DEC_BAL_STATE_FLOATS;
+            uint32_t orow[16];
+#pragma unroll
+            for (int c = 0; c < 16; ++c) orow[c] = 0u;
+            if (ok) {
+                tc_fence_after();
+                tmem_ld16(tO + lane_addr, orow);
+                tmem_ld_wait();
+            }
+#pragma unroll
+            for (int h = 0; h < 8; ++h) __stcg(st + DEC_BAL_LP + t * 8 + h, lp[h]);
+#pragma unroll
+            for (int c = 0; c < 16; ++c) __stcg(st + DEC_BAL_O + t * 16 + c, __uint_as_float(orow[c]));
+            if (t == 0) {
+#pragma unroll
+                for (int h = 0; h < 8; ++h) __stcg(st + DEC_BAL_M + h, m[h]);
+                __stcg(st + DEC_BAL_INFO, ok ? 1.0f : 0.0f);
+                __stcg(st + DEC_BAL_INFO + 1, range_bad ? 1.0f : 0.0f);
+            }
+            __threadfence();
+            named_bar_sync(1, 128);
+            if (t == 0) {
+                st_release_u32(a.bal_sync + DEC_BAL_SYNC_WORDS + blockIdx.x, ctl->epoch + 1u);
+                if (!ok && !quiet && a.status) atomicOr(a.status, RK_STATUS_TIMEOUT);
+            }
+        } else if (a.split_tokens > 0) {
             // split partial: O / l in FP32 and m + log2(l) (log2 domain); the
             // merge rescales and sums the splits in ascending order
             uint32_t orow[16];
@@ -627,15 +833,70 @@ __global__ void __launch_bounds__(DEC_THREADS, 1)
                         range_bad ? __int_as_float(0x7fc00000)
                                   : (L[h] > 0.0f ? (m[h] + log2f(L[h])) * 0.693147180559945309f : -INFINITY);
             if (range_bad && t == 0 && a.status) atomicOr(a.status, RK_STATUS_RANGE);
-        } else {  // a wait gave up: the group's rows are written as failed
+        } else {  // a wait gave up (or the row failed earlier): the group's rows are written as failed
 #pragma unroll
             for (int h = 0; h < 8; ++h)
                 if (h < G) out[((size_t)tq * a.Hq + h0 + h) * HEAD_DIM + t] = __float2bfloat16_rn(0.0f);
             if (t < G) a.lse[(size_t)tq * a.Hq + h0 + t] = __int_as_float(0x7fc00000);
-            if (t == 0 && a.status) atomicOr(a.status, RK_STATUS_TIMEOUT);
+            if (t == 0 && !quiet && a.status) atomicOr(a.status, RK_STATUS_TIMEOUT);
         }
     }
 
+    // ---- all roles done with the segment; no MMA, copy or TMEM access in flight ----
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+}
+
+
+__global__ void __launch_bounds__(DEC_THREADS, 1)
+    decode_kernel(const __grid_constant__ CUtensorMap vmap, const __grid_constant__ DecodeArgs a) {
+    extern __shared__ __align__(1024) uint8_t sm[];
+    // A launch that only reads what this grid reads (the prefill rows of a
+    // ragged batch) may fill the SMs this grid's last wave leaves idle.
+    griddep_launch_dependents();
+    DecCtrl* ctl = reinterpret_cast<DecCtrl*>(sm + OFF_CTRL);
+    const uint32_t s_base = smem_u32(sm);
+    const int tid = threadIdx.x, warp = tid >> 5;
+    if (s_base & 1023u) {  // the swizzled operand layout needs a 1024-byte aligned base
+        if (tid == 0 && a.status) atomicOr(a.status, RK_STATUS_TIMEOUT);
+        // Nothing was computed: padded rows (and split partials, which the merge
+        // then turns into out = 0, lse = NaN) are written as failed.  A ragged
+        // row's packed index is not known here; the status bit reports it.  (A
+        // balanced launch's rows are left to the segments' bounded waits.)
+        if (!a.qo_indptr && !a.balanced) {
+            const int rows_heads = a.B * a.Hkv;
+            const int split = (int)(blockIdx.x / rows_heads), unit = (int)(blockIdx.x % rows_heads);
+            write_empty_row(a, unit / a.Hkv, unit / a.Hkv, (unit % a.Hkv) * a.G, split, __int_as_float(0x7fc00000));
+        }
+        if (a.balanced && tid == 0) bal_done(a);
+        return;
+    }
+    if (warp == WARP_MMA) {
+        tmem_alloc(smem_u32(&ctl->tmem_base), TMEM_COLS);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = ctl->tmem_base;
+    if (!a.balanced) {
+        // one (split, row, KV head) per CTA, split-major; split = 0 without splitting
+        const int rows_heads = a.B * a.Hkv;
+        const int split = (int)(blockIdx.x / rows_heads), unit = (int)(blockIdx.x % rows_heads);
+        const int t_begin = a.split_tokens > 0 ? split * a.split_tokens : 0;
+        const int t_cap = a.split_tokens > 0 ? t_begin + a.split_tokens : a.W * PAGE;
+        decode_segment(vmap, a, sm, ctl, s_base, tmem, unit / a.Hkv, unit % a.Hkv, split, t_begin, t_cap, 0);
+    } else {
+        bal_schedule(a, sm, ctl);
+        const int n_seg = ctl->n_seg;
+        for (int sg = 0; sg < n_seg; ++sg) {
+            const int unit = ctl->seg[sg][0];
+            decode_segment(vmap, a, sm, ctl, s_base, tmem, unit / a.Hkv, unit % a.Hkv, 0, ctl->seg[sg][1] * DEC_BN,
+                           ctl->seg[sg][2] * DEC_BN, ctl->seg[sg][3]);
+        }
+        if (tid == 0) bal_done(a);
+    }
     // ---- teardown: all roles done; no MMA or TMEM access in flight ----
     tc_fence_before();
     __syncthreads();
@@ -681,7 +942,9 @@ __global__ void __launch_bounds__(HEAD_DIM) decode_merge_kernel(const __grid_con
 
 }  // namespace
 
-cudaError_t launch_decode(const CUtensorMap& vm, const DecodeArgs& a, cudaStream_t stream) {
+namespace {
+// Sets the kernel's dynamic shared memory limit once per device.
+cudaError_t configure_decode() {
     static std::atomic<uint64_t> configured{0};  // one bit per device
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
@@ -691,6 +954,42 @@ cudaError_t launch_decode(const CUtensorMap& vm, const DecodeArgs& a, cudaStream
         e = cudaFuncSetAttribute(decode_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, DEC_SMEM_BYTES);
         if (e != cudaSuccess) return e;
         configured.fetch_or(bit);
+    }
+    return cudaSuccess;
+}
+}  // namespace
+
+cudaError_t decode_resident_ctas(int* ctas) {
+    cudaError_t e = configure_decode();
+    if (e != cudaSuccess) return e;
+    int dev = 0, sms = 0, per = 0;
+    if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+    if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
+    if ((e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per, decode_kernel, DEC_THREADS, DEC_SMEM_BYTES)) !=
+        cudaSuccess)
+        return e;
+    *ctas = sms * per;
+    return cudaSuccess;
+}
+
+cudaError_t launch_decode(const CUtensorMap& vm, const DecodeArgs& a, cudaStream_t stream) {
+    cudaError_t e = configure_decode();
+    if (e != cudaSuccess) return e;
+    if (a.balanced) {
+        // every CTA resident at once (a CTA may wait for its predecessor's hand-off)
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3((unsigned)a.bal_grid);
+        cfg.blockDim = dim3(DEC_THREADS);
+        cfg.dynamicSmemBytes = DEC_SMEM_BYTES;
+        cfg.stream = stream;
+        cudaLaunchAttribute at[1];
+        at[0].id = cudaLaunchAttributeCooperative;
+        at[0].val.cooperative = 1;
+        cfg.attrs = at;
+        cfg.numAttrs = 1;
+        e = cudaLaunchKernelEx(&cfg, decode_kernel, vm, a);
+        if (e != cudaSuccess) return e;
+        return cudaGetLastError();
     }
     const long long grid = (long long)a.B * a.Hkv * (a.split_tokens > 0 ? a.n_splits : 1);
     if (grid <= 0) return cudaSuccess;

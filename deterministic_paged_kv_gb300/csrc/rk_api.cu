@@ -20,6 +20,7 @@
 
 namespace rk {
 cudaError_t launch_decode(const CUtensorMap& vm, const DecodeArgs& a, cudaStream_t stream);
+cudaError_t decode_resident_ctas(int* ctas);
 cudaError_t launch_prefill(const CUtensorMap& qm, const CUtensorMap& km, const CUtensorMap& vm,
                            const PrefillArgs& a, cudaStream_t stream, bool overlap_previous = false);
 cudaError_t launch_kv_append(const AppendArgs& a, cudaStream_t stream);
@@ -366,7 +367,7 @@ int64_t split_scratch_need(const rk_paged_plan_t* plan, int32_t split_tokens) {
 int decode_common(const rk_paged_plan_t* plan, int32_t split_tokens, const void* q, const void* k_cache,
                   const void* v_cache, const int32_t* block_table_d, const int32_t* kv_lens_d,
                   const int32_t* position_ids_d, void* out, float* lse, void* scratch, uint64_t scratch_bytes,
-                  int32_t* status_d, rk_stream_t stream) {
+                  int32_t* status_d, rk_stream_t stream, bool balanced = false) {
     g_err.clear();
     int rc = check_launch_common(plan, q, k_cache, v_cache, block_table_d, kv_lens_d, position_ids_d,
                                  out, lse);
@@ -383,6 +384,13 @@ int decode_common(const rk_paged_plan_t* plan, int32_t split_tokens, const void*
             return fail(RK_E_ARG, "split decode scratch too small: %lld bytes needed, %llu given", (long long)need,
                         (unsigned long long)scratch_bytes);
         if (split_count(plan, split_tokens) > 0x7fffffffLL) return fail(RK_E_ARG, "too many splits");
+    }
+    if (balanced) {
+        if (!scratch || !aligned(scratch, 256))
+            return fail(RK_E_ARG, "balanced decode scratch must be a non-null 256-byte aligned device pointer");
+        if (scratch_bytes < RK_PAGED_BALANCED_SCRATCH_BYTES)
+            return fail(RK_E_ARG, "balanced decode scratch too small: %llu bytes needed, %llu given",
+                        (unsigned long long)RK_PAGED_BALANCED_SCRATCH_BYTES, (unsigned long long)scratch_bytes);
     }
     if (plan->B == 0) return RK_OK;
     const bool have = plan->num_pages > 0;
@@ -416,6 +424,23 @@ int decode_common(const rk_paged_plan_t* plan, int32_t split_tokens, const void*
         a.lse_part = static_cast<float*>(scratch) + n * rk::HEAD_DIM;
     }
     std::memcpy(a.rope_turns, plan->rope_turns, sizeof a.rope_turns);
+    if (balanced) {
+        int ctas = 0;
+        cudaError_t e = rk::decode_resident_ctas(&ctas);
+        if (e != cudaSuccess) return fail(RK_E_CUDA, "decode occupancy: %s", cudaGetErrorString(e));
+        // Hkv chains of `members` CTAs (one per KV head)
+        const int members = std::min(ctas, RK_PAGED_BALANCED_MAX_CTAS) / plan->Hkv;
+        // blocks of 8 tiles a row can have, and the most one CTA could get
+        const int64_t row_blocks = std::max<int64_t>(1, ((int64_t)plan->W * rk::PAGE + 1023) / 1024);
+        const int64_t per_cta = members > 0 ? ((int64_t)plan->B * row_blocks + members - 1) / members : 0;
+        if (members >= 2 && plan->B >= members && plan->B <= rk::DEC_BAL_MAX_ROWS &&
+            per_cta + 2 <= rk::DEC_BAL_MAX_SEGS) {
+            a.balanced = 1;
+            a.bal_grid = members * plan->Hkv;
+            a.bal_sync = static_cast<uint32_t*>(scratch);
+            a.bal_state = reinterpret_cast<float*>(static_cast<char*>(scratch) + 4096);
+        }
+    }
     cudaError_t e = rk::launch_decode(vm, a, reinterpret_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return fail(RK_E_CUDA, "decode launch: %s", cudaGetErrorString(e));
     return RK_OK;
@@ -429,6 +454,27 @@ int rk_paged_attn_decode(const rk_paged_plan_t* plan, const void* q, const void*
                          rk_stream_t stream) {
     return decode_common(plan, 0, q, k_cache, v_cache, block_table_d, kv_lens_d, position_ids_d, out, lse,
                          nullptr, 0, status_d, stream);
+}
+
+static_assert((rk::DEC_BAL_SYNC_WORDS + RK_PAGED_BALANCED_MAX_CTAS) * 4 <= 4096 &&
+                  RK_PAGED_BALANCED_SCRATCH_BYTES ==
+                      4096ull + (uint64_t)RK_PAGED_BALANCED_MAX_CTAS * rk::DEC_BAL_STATE_FLOATS * 4,
+              "balanced scratch layout: 4 KiB of flags, then one hand-off state per CTA");
+
+int rk_paged_decode_balanced_scratch_bytes(const rk_paged_plan_t* plan, uint64_t* bytes) {
+    g_err.clear();
+    if (!plan || !bytes) return fail(RK_E_ARG, "plan and bytes must be non-null");
+    if (plan->abi != RK_PAGED_ABI_VERSION) return fail(RK_E_ARG, "plan ABI %u != %u", plan->abi, RK_PAGED_ABI_VERSION);
+    *bytes = RK_PAGED_BALANCED_SCRATCH_BYTES;
+    return RK_OK;
+}
+
+int rk_paged_attn_decode_balanced(const rk_paged_plan_t* plan, const void* q, const void* k_cache,
+                                  const void* v_cache, const int32_t* block_table_d, const int32_t* kv_lens_d,
+                                  const int32_t* position_ids_d, void* out, float* lse, void* scratch,
+                                  uint64_t scratch_bytes, int32_t* status_d, rk_stream_t stream) {
+    return decode_common(plan, 0, q, k_cache, v_cache, block_table_d, kv_lens_d, position_ids_d, out, lse,
+                         scratch, scratch_bytes, status_d, stream, true);
 }
 
 int rk_paged_decode_split_scratch_bytes(const rk_paged_plan_t* plan, int32_t split_tokens, uint64_t* bytes) {

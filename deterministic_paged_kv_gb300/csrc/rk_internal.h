@@ -23,7 +23,7 @@ constexpr int DEC_KSTAGES = 3;
 constexpr int DEC_VSTAGES = 3;
 constexpr int DEC_TILE_BYTES = DEC_BN * HEAD_DIM * 2;  // 32 KiB
 constexpr int DEC_KAHEAD = 2;                          // K tiles a transform thread keeps in flight
-constexpr int DEC_CTRL_BYTES = 2048;                   // barriers, RoPE tables, reductions
+constexpr int DEC_CTRL_BYTES = 3072;                   // barriers, RoPE tables, reductions, segment list
 constexpr int DEC_PGT_ENTRIES = 2048;                  // page ids of a CTA's range held in shared memory
 constexpr int DEC_SMEM_BYTES = (DEC_KSTAGES + DEC_VSTAGES) * DEC_TILE_BYTES + 16 * HEAD_DIM * 2 +
                                2 * 16 * DEC_BN * 2 + DEC_CTRL_BYTES + DEC_PGT_ENTRIES * 4;
@@ -56,9 +56,28 @@ struct DecodeArgs {
     int32_t max_q_len;            // rows with more queries are flagged (RK_STATUS_POSITION)
     uint32_t wait_limit_ns;       // pipeline wait limit (0: RK_WAIT_LIMIT_NS)
     int32_t timeout_drill;        // nonzero: the score MMA issuer first waits on a barrier nothing completes
+    // Balanced schedule (balanced != 0; padded split-free decode only): each
+    // (row, KV head)'s tiles are cut in blocks of DEC_BAL_BLOCK_TILES, the blocks
+    // of all of them laid end to end in (row, KV head) order and dealt to the
+    // CTAs in equal contiguous runs.  A row whose blocks cross from CTA c's run
+    // into CTA c + 1's hands its running softmax state (m, l, O) over through
+    // bal_state slot c: the row is still reduced tile after tile in ascending
+    // order, with the same operations as by a single CTA.
+    int32_t balanced;
+    uint32_t* bal_sync;           // [0] launch epoch, [1] CTAs done, [2 + c] hand-off flag of slot c
+    float* bal_state;             // [grid - 1][DEC_BAL_STATE_FLOATS]
+    int32_t bal_grid;             // CTAs of a balanced launch (all resident at once)
     uint64_t rope_turns[ROPE_PAIRS];
 };
 constexpr int DEC_SPLIT_GRAIN = PAGE;  // split lengths are multiples of the page size
+constexpr int DEC_BAL_BLOCK_TILES = 8;       // tiles per block (a multiple of the RoPE anchor spacing)
+constexpr int DEC_BAL_MAX_SEGS = 32;         // segments one CTA can hold
+constexpr int DEC_BAL_MAX_ROWS = 12288;      // rows whose block counts fit the set-up scratch
+// Hand-off state of one row: m per head [8], info [8] (ok, range_bad), l
+// partial per (token lane, head) [128][8], O^T row per output dim [128][16].
+constexpr int DEC_BAL_M = 0, DEC_BAL_INFO = 8, DEC_BAL_LP = 16, DEC_BAL_O = DEC_BAL_LP + 128 * 8;
+constexpr int DEC_BAL_STATE_FLOATS = DEC_BAL_O + 128 * 16;  // 3088 floats, 64-byte multiple
+constexpr int DEC_BAL_SYNC_WORDS = 2;        // epoch, done; then one flag per slot
 
 // ----------------------------------------------------------- prefill ----
 // One CTA per (row, KV head, q-tile).  A q-tile is 128 accumulator rows =

@@ -269,6 +269,57 @@ int rk_paged_attn_decode_split_static(const rk_paged_plan_t *plan, int32_t split
                                       int32_t *status_d, rk_stream_t stream);
 
 /*
+ * Balanced split-free decode: the same operation and the same arithmetic as
+ * rk_paged_attn_decode (split-KV disabled: each (row, KV head) is reduced in
+ * one ascending-KV pass, "flashinfer_fa2 backend for Ada (SM89)", "Split-KV
+ * is disabled" design note), on a schedule that keeps every SM busy to the
+ * end.  One CTA per SM (a cooperative launch: all resident at once), the
+ * CTAs in Hkv chains, one per KV head.  The tiles of every row are grouped in
+ * blocks of 8 (1024 tokens), the rows' blocks laid end to end in row order and
+ * dealt to a chain's CTAs in equal contiguous runs (the same runs for every
+ * head, so the CTAs serving a row's heads read its pages together); where a
+ * row crosses from one CTA's run to the next, the first CTA hands its running
+ * state (running max, per-lane partial sums of l, the FP32 O accumulator) to
+ * the second through the scratch buffer, and the second goes on from the next
+ * tile.  The row is therefore reduced tile
+ * after tile, in ascending order, by exactly the operations of the one-CTA
+ * path: out and lse are bitwise identical to rk_paged_attn_decode's for every
+ * row, whatever the batch, the table width or the grid.  (A CTA does the row
+ * it hands on first and the row it takes over last, so a hand-off is
+ * normally ready long before it is read; the read waits at most the plan's
+ * wait limit and then fails closed like any other wait.)
+ *
+ * rk_paged_decode_balanced_scratch_bytes -- *bytes = the device scratch the
+ * balanced entry point needs (RK_PAGED_BALANCED_SCRATCH_BYTES: hand-off
+ * flags and states for up to 512 CTAs; independent of the plan).  Host only.
+ *
+ * rk_paged_attn_decode_balanced -- as rk_paged_attn_decode, plus:
+ *   scratch        DEVICE memory owned by the caller, 256-byte aligned, at
+ *                  least rk_paged_decode_balanced_scratch_bytes bytes, ZEROED
+ *                  ONCE before its first use and then left to the library
+ *                  (each launch leaves it ready for the next: a launch epoch
+ *                  in its first word makes earlier hand-off flags stale, so
+ *                  graph replays of one captured launch are fine).  Two
+ *                  launches in flight at once must not share a scratch buffer.
+ *   scratch_bytes  its size.
+ * The balanced schedule is used when it can help and is safe: each chain has
+ * at least two CTAs and at most as many as the batch has rows, the batch has at
+ * most 12288 rows, and no CTA would hold more than 32 segments (B * ceil(W /
+ * 64) blocks at most 30 per chain member); otherwise the call runs
+ * rk_paged_attn_decode's one-CTA-per-(row, KV head) launch (same results;
+ * scratch untouched).
+ * Returns RK_E_ARG for a missing / small / misaligned scratch, otherwise as
+ * rk_paged_attn_decode; RK_E_CUDA also if the cooperative launch is refused.
+ */
+#define RK_PAGED_BALANCED_MAX_CTAS 512
+#define RK_PAGED_BALANCED_SCRATCH_BYTES (4096ull + 512ull * 3088ull * 4ull)
+int rk_paged_decode_balanced_scratch_bytes(const rk_paged_plan_t *plan, uint64_t *bytes);
+int rk_paged_attn_decode_balanced(const rk_paged_plan_t *plan, const void *q, const void *k_cache,
+                                  const void *v_cache, const int32_t *block_table_d, const int32_t *kv_lens_d,
+                                  const int32_t *position_ids_d, void *out, float *lse, void *scratch,
+                                  uint64_t scratch_bytes, int32_t *status_d, rk_stream_t stream);
+
+/*
  * rk_paged_kv_append -- write new tokens' K and V into their pages, as the
  * cache holds them: pre-RoPE (the attention calls rotate K when they read
  * it; "WS2 PR7 ...", "FlashInfer RoPE Fusion").  The page walk is the one of
