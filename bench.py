@@ -2,10 +2,12 @@
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
-One step = one rk_paged_attn_decode call over the decode-throughput workload
-(B=64 rows, kv_len 4096 each, Hq=32/Hkv=8, d=128, page 16, 16384 shuffled
-pages; 1.075 GB of algorithmic traffic, larger than L2, so no flush is needed
-between steps).  The same run also times rk_paged_attn_prefill on the chunked
+One step = one rk_paged_attn_decode_balanced call over the decode-throughput
+workload (B=64 rows, kv_len 4096 each, Hq=32/Hkv=8, d=128, page 16, 16384
+shuffled pages; 1.075 GB of algorithmic traffic, larger than L2, so no flush is
+needed between steps): the split-free decode on its balanced schedule, bitwise
+identical to rk_paged_attn_decode, whose one-CTA-per-(row, KV head) launch is
+timed beside it in "decode_one_cta_per_pair".  The same run also times rk_paged_attn_prefill on the chunked
 prefill workload (B=4, 1536-token prefix + 512-token chunk) with an L2 flush
 between launches, reported in the "prefill" object, the long full-causal
 prefill (B=1, S=8192) in "prefill_long", the same decode step replayed from a
@@ -567,12 +569,17 @@ def run_ours(args):
     out = torch.empty_like(d["q"])
     lse = torch.empty((w.B, w.Hq, 1), dtype=torch.float32, device=dev)
 
-    calls = [0]  # rk_paged_attn_decode calls made; each launches one decode_kernel
+    calls = [0]  # rk_paged_attn_decode_balanced calls made; each launches one decode_bal_kernel
+    scratch = torch.zeros(binding.decode_balanced_scratch_bytes(p), dtype=torch.uint8, device=dev)
 
     def step(st=None):
-        binding.attn_decode(p, d["q"], d["k_cache"], d["v_cache"], d["block_table"], d["kv_lens"],
-                            d["position_ids"], out, lse, stream=st or stream)
+        binding.attn_decode_balanced(p, d["q"], d["k_cache"], d["v_cache"], d["block_table"], d["kv_lens"],
+                                     d["position_ids"], out, lse, scratch, stream=st or stream)
         calls[0] += 1
+
+    def step_one_cta():
+        binding.attn_decode(p, d["q"], d["k_cache"], d["v_cache"], d["block_table"], d["kv_lens"],
+                            d["position_ids"], out, lse, stream=stream)
 
     for _ in range(args.warmup):
         step()
@@ -600,10 +607,18 @@ def run_ours(args):
     avg_launch_ms = sum(per_launch) / len(per_launch)
     dec_hash = source_hash("decode.cu", "rk_device.cuh", "rk_internal.h")
     roof = {"bound": "hbm", "achieved": step_bytes / (avg_launch_ms * 1e-3) / 1e9, "peak": hbm,
-            "unit": "GB/s", "traffic": traffic_for("decode_kernel", dec_hash),
-            "kernel": "decode_kernel (one CTA per (row, KV head): 512 CTAs)", "peak_kind": peak_kind + " (copy bandwidth, burst)",
-            "alg_bytes_per_launch": step_bytes}
+            "unit": "GB/s", "traffic": traffic_for("decode_bal_kernel", dec_hash),
+            "kernel": "decode_bal_kernel (balanced: one CTA per SM, Hkv chains, state hand-off)",
+            "peak_kind": peak_kind + " (copy bandwidth, burst)", "alg_bytes_per_launch": step_bytes}
     roof["frac"] = roof["achieved"] / roof["peak"]
+    for _ in range(3):
+        step_one_cta()
+    one_cta = time_launches(step_one_cta, max(10, args.steps), stream)
+    one_ms = sum(one_cta) / len(one_cta)
+    one_cta_obj = {"value": step_bytes / (one_ms * 1e-3) / 1e9, "unit": "GB/s", "ms_per_launch": one_ms,
+                   "frac_of_peak": step_bytes / (one_ms * 1e-3) / 1e9 / hbm, "peak_kind": peak_kind,
+                   "traffic": traffic_for("decode_kernel", dec_hash),
+                   "kernel": "decode_kernel (rk_paged_attn_decode: one CTA per (row, KV head), 512 CTAs)"}
 
     # ---------------- e2e: host buffers through the public API ----------------
     pinned = {k: getattr(w, k).pin_memory() for k in names}
@@ -672,6 +687,7 @@ def run_ours(args):
             "clocks": clocks,
             "wall_s_timed_region": wall,
             "decode_graph": dgraph,
+            "decode_one_cta_per_pair": one_cta_obj,
             "prefill": prefill,
             "prefill_long": plong,
             "decode_long": dlong,

@@ -23,10 +23,14 @@ constexpr int DEC_KSTAGES = 3;
 constexpr int DEC_VSTAGES = 3;
 constexpr int DEC_TILE_BYTES = DEC_BN * HEAD_DIM * 2;  // 32 KiB
 constexpr int DEC_KAHEAD = 2;                          // K tiles a transform thread keeps in flight
-constexpr int DEC_CTRL_BYTES = 3072;                   // barriers, RoPE tables, reductions, segment list
+constexpr int DEC_CTRL_BYTES = 2048;                   // barriers, RoPE tables, reductions
 constexpr int DEC_PGT_ENTRIES = 2048;                  // page ids of a CTA's range held in shared memory
 constexpr int DEC_SMEM_BYTES = (DEC_KSTAGES + DEC_VSTAGES) * DEC_TILE_BYTES + 16 * HEAD_DIM * 2 +
                                2 * 16 * DEC_BN * 2 + DEC_CTRL_BYTES + DEC_PGT_ENTRIES * 4;
+// The balanced (persistent) decode: two Q^T buffers and a segment list.
+constexpr int DEC_BAL_CTRL_BYTES = 4096;
+constexpr int DEC_BAL_SMEM_BYTES = (DEC_KSTAGES + DEC_VSTAGES) * DEC_TILE_BYTES + 2 * 16 * HEAD_DIM * 2 +
+                                   2 * 16 * DEC_BN * 2 + DEC_BAL_CTRL_BYTES + DEC_PGT_ENTRIES * 4;
 
 struct DecodeArgs {
     const void* q;                // bf16 [B, Hq, 1, D]
