@@ -116,6 +116,22 @@ def test_balanced_gqa_groups(scratch, Hq, Hkv, B):
     assert_parity(o2, l2, ro, rl)
 
 
+def test_balanced_long_row_crosses_many_ctas(scratch):
+    """One row of 20000 keys among 18 short ones: its 20 blocks span several
+    CTAs of each KV head's chain, so middle segments both take the row over and
+    hand it on (a chain of hand-offs, each waiting for the one before); bitwise
+    equal to the one-CTA launch and within the oracle tolerance."""
+    kv = [20000] + [100 + 37 * i for i in range(18)]
+    w = workloads.random_case(len(kv), 1, 32, 8, 128, kv, seed=331, mode="decode")
+    e0, _ = _epoch(scratch)
+    (o1, l1, s1), (o2, l2, s2) = _both(w, scratch)
+    assert _epoch(scratch)[0] == e0 + 1
+    assert s1 == s2 == 0
+    assert bitwise_equal(o1, o2) and bitwise_equal(l1, l2)
+    ro, rl = oracle_ref(w)
+    assert_parity(o2, l2, ro, rl)
+
+
 def test_balanced_unsafe_rows_fail_like_the_one_cta_launch(scratch):
     """An out-of-range page id deep inside a long row (a segment other than the
     row's last one meets it) and a kv_len past the table: the same failed rows
