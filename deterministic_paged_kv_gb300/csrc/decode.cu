@@ -48,14 +48,17 @@
 // Balanced schedule (decode_bal_kernel, rk_paged_attn_decode_balanced): the
 // same roles and the same arithmetic on a persistent cooperative grid, one CTA
 // per SM in Hkv chains (one per KV head).  Each row's tiles are grouped in
-// blocks of 8 (1024 tokens: segments start on a RoPE anchor tile) and a chain's
-// CTAs take equal contiguous runs of the rows' blocks, so a batch whose
+// blocks of 1, 2, 4 or 8 tiles (the coarsest that still gives every CTA of a
+// chain work) and a chain's CTAs take equal contiguous runs of the rows' blocks,
+// so a batch whose
 // (row, KV head) count is not a multiple of the SM count keeps every SM busy to
 // the end.  A row cut between two CTAs is handed over exactly: the first CTA
 // writes its running max, per-lane partial sums of l and its FP32 O^T row
 // (read from TMEM) to the scratch buffer and releases a flag; the second, which
 // takes that row last (the first did it first), waits (bounded) for the flag,
-// loads the state (O^T back into TMEM) and goes on with the next tile.  So
+// loads the state (O^T back into TMEM) and goes on with the next tile.  A
+// segment that starts between two RoPE anchor tiles takes the exact angles at
+// the anchor before it and replays the angle steps of the tiles in between.  So
 // every row is reduced tile after tile in ascending order by the operations of
 // the one-CTA launch, and out / lse are bitwise identical to it.  The CTA's
 // pipeline runs on across its segments: the ring phases count the CTA's tiles,
@@ -821,9 +824,12 @@ __device__ __forceinline__ void bal_done(const DecodeArgs& a) {
 
 // This CTA's segments.  The grid is Hkv chains of grid / Hkv CTAs: CTA c
 // serves KV head h = c % Hkv as member g = c / Hkv of its chain.  Every row gets
-// max(1, ceil(tiles / 8)) blocks (the tiles of its visible keys, 8 to a block),
-// laid end to end in row order; member g takes blocks [g L, (g + 1) L), L =
-// ceil(total / members), of head h.  All heads of a row have the same blocks,
+// max(1, ceil(tiles / bt)) blocks (the tiles of its visible keys, bt to a
+// block), laid end to end in row order; member g takes blocks [g L, (g + 1) L),
+// L = ceil(total / members), of head h.  bt is the coarsest power of two, from
+// the host's finest (whose worst case keeps a CTA's segment list within
+// DEC_BAL_MAX_SEGS) up to DEC_BAL_MAX_BLOCK_TILES, that still leaves the last
+// member a block.  All heads of a row have the same blocks,
 // so the Hkv CTAs of a member index read the same pages (the heads share them)
 // at the same time.  A row cut at g L is taken over from member g - 1 (import,
 // done last: by then that CTA has handed it on, having done it first); a row
@@ -834,16 +840,55 @@ __device__ __noinline__ void bal_schedule(const DecodeArgs& a, uint8_t* sm, DecC
     int* nbs = reinterpret_cast<int*>(sm + OFF_K);  // blocks of row b
     int* pre = nbs + DEC_BAL_MAX_ROWS;               // blocks of the rows before b
     static_assert(2 * DEC_BAL_MAX_ROWS * 4 <= DEC_KSTAGES * DEC_TILE_BYTES, "set-up scratch exceeds the K ring");
-    static_assert(DEC_BAL_BLOCK_TILES % XF_ANCHOR_TILES == 0, "segments must start on a RoPE anchor tile");
     const int B = a.B <= DEC_BAL_MAX_ROWS ? a.B : 0;  // more rows are ruled out by the host; none taken here
+    // The finest block the host allows (its worst-case bound on a CTA's
+    // segments), and the coarsest power of two from there up to
+    // DEC_BAL_MAX_BLOCK_TILES that still gives every member of a chain work
+    // (finer cuts only pay while some member would otherwise sit idle).
+    const int bt_min = (a.bal_block_tiles >= 1 && a.bal_block_tiles <= DEC_BAL_MAX_BLOCK_TILES)
+                           ? a.bal_block_tiles
+                           : DEC_BAL_MAX_BLOCK_TILES;
     const int per = (B + DEC_THREADS - 1) / DEC_THREADS;  // contiguous rows per thread
     const int r0 = min(B, tid * per), r1 = min(B, r0 + per);
-    int sum = 0;
+    // the previous launch's last CTA advanced the epoch in L2 (its load overlaps the rows')
+    if (tid == DEC_THREADS - 1) ctl->epoch = __ldcg(a.bal_sync);
+    int cnt[4] = {0, 0, 0, 0};  // blocks of the thread's rows at 1, 2, 4, 8 tiles a block
     for (int r = r0; r < r1; ++r) {
         const int kv = a.kv_lens[r], qp = a.position_ids[r];
         const int nv = (kv < 0 || kv > a.W * PAGE || qp < 0) ? 0 : (qp >= kv ? kv : qp + 1);
         const int nt = (nv + DEC_BN - 1) / DEC_BN;
-        const int nb = max(1, (nt + DEC_BAL_BLOCK_TILES - 1) / DEC_BAL_BLOCK_TILES);
+        nbs[r] = nt;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) cnt[k] += max(1, (nt + (1 << k) - 1) >> k);
+    }
+    int* wsum = reinterpret_cast<int*>(sm + OFF_V);  // [warp][4]; the V stages are zeroed afterwards
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        const int v = __reduce_add_sync(0xffffffffu, cnt[k]);
+        if (lane == 0) wsum[warp * 4 + k] = v;
+    }
+    __syncthreads();
+    int bt = bt_min;
+    {
+        // the four totals, summed over the warps by the lanes of every warp
+        static_assert(DEC_THREADS / 32 <= 32, "one lane per warp partial");
+        int tot[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) tot[k] = __reduce_add_sync(0xffffffffu, lane < DEC_THREADS / 32 ? wsum[lane * 4 + k] : 0);
+        const int members = (int)gridDim.x / a.Hkv;
+#pragma unroll
+        for (int k = 3; k >= 0; --k) {
+            const long long T = tot[k];
+            const long long L = members > 0 ? (T + members - 1) / members : 0;
+            if ((1 << k) >= bt_min && members > 0 && (long long)(members - 1) * L < T) {  // the last member gets a block
+                bt = 1 << k;
+                break;
+            }
+        }
+    }
+    int sum = 0;
+    for (int r = r0; r < r1; ++r) {
+        const int nb = max(1, (nbs[r] + bt - 1) / bt);
         nbs[r] = nb;
         sum += nb;
     }
@@ -854,7 +899,6 @@ __device__ __noinline__ void bal_schedule(const DecodeArgs& a, uint8_t* sm, DecC
         if (lane >= off) inc += v;
     }
     if (lane == 31) ctl->scan[warp] = inc;
-    if (tid == 0) ctl->epoch = __ldcg(a.bal_sync);  // the previous launch's last CTA advanced it in L2
     __syncthreads();
     int wbase = 0, total = 0;
 #pragma unroll 1
@@ -890,8 +934,8 @@ __device__ __noinline__ void bal_schedule(const DecodeArgs& a, uint8_t* sm, DecC
                 const int nb = nbs[b];
                 const long long blo = P > lo ? P : lo, bhi = P + nb < hi ? P + nb : hi;
                 sg[n][0] = b * Hkv + h;
-                sg[n][1] = (int)(blo - P) * DEC_BAL_BLOCK_TILES;
-                sg[n][2] = (int)(bhi - P) * DEC_BAL_BLOCK_TILES;
+                sg[n][1] = (int)(blo - P) * bt;
+                sg[n][2] = (int)(bhi - P) * bt;
                 sg[n][3] = (P < lo ? DEC_SEG_IMPORT : 0) | (P + nb > hi ? DEC_SEG_EXPORT : 0);
                 ++n;
                 P += nb;
@@ -1060,6 +1104,23 @@ __device__ __noinline__ Angles anchor_angles(const DecCtrl* ctl, uint32_t t, int
         rope_cos_sin(t, ctl->turns[8 * u + 2 * e + 1], r.c[e].y, r.s[e].y);
     }
     return r;
+}
+
+// Angles of row r0 of tile ta: exact at the last anchor tile, then the row
+// steps of the tiles since (none when ta is an anchor tile).
+__device__ __noinline__ Angles anchor_replay(const DecCtrl* ctl, int ta, int r0, int u) {
+    const int tz = ta - ta % XF_ANCHOR_TILES;
+    Angles an = anchor_angles(ctl, (uint32_t)(tz * DEC_BN + r0), u);
+    float2 dcs[4], dsn[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+        const float2 s0 = ctl->step[8 * u + 2 * e], s1 = ctl->step[8 * u + 2 * e + 1];
+        dcs[e] = make_float2(s0.x, s1.x);
+        dsn[e] = make_float2(s0.y, s1.y);
+    }
+#pragma unroll 1
+    for (int q = 0; q < (ta - tz) * XF_ROWS; ++q) rope_step(an.c, an.s, dcs, dsn);
+    return an;
 }
 
 // Q^T of a segment (thread (h, u) rotates chunk pair u of query head h at the
@@ -1420,11 +1481,25 @@ __global__ void __launch_bounds__(DEC_THREADS, 1)
             // (a thread's rows are XF_ROW_STEP apart and the next tile continues the
             // sequence), so at most XF_ANCHOR_TILES * XF_ROWS steps follow an anchor.
             float2 c[4], sn[4];
-            for (int it = 0; it < n_loc && kok; ++it, ++gcons) {
+            // Tiles are counted from the anchor tile at or before the segment's
+            // first (it = aph there), so it % XF_ANCHOR_TILES == 0 marks the anchor
+            // tiles; a segment that starts between anchors takes its first angles
+            // from the anchor before it (out of line, once per segment).
+            const int aph = (t_begin / DEC_BN) & (XF_ANCHOR_TILES - 1);
+            const int t_anchor = t_begin - aph * DEC_BN;
+            if (aph != 0) {
+                const Angles an = anchor_replay(ctl, t_begin / DEC_BN, r0, u);
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    c[e] = an.c[e];
+                    sn[e] = an.s[e];
+                }
+            }
+            for (int it = aph; it < aph + n_loc && kok; ++it, ++gcons) {
                 const int k = gcons % DEC_KSTAGES;
                 cp_async_wait<DEC_KAHEAD - 1>();  // this thread's chunks of the tile have landed
                 uint8_t* kt = sm + OFF_K + k * DEC_TILE_BYTES;
-                const int t0 = t_begin + it * DEC_BN;
+                const int t0 = t_anchor + it * DEC_BN;
                 if (it % XF_ANCHOR_TILES == 0) {
                     const Angles an = anchor_angles(ctl, (uint32_t)(t0 + r0), u);
 #pragma unroll

@@ -430,12 +430,19 @@ int decode_common(const rk_paged_plan_t* plan, int32_t split_tokens, const void*
         if (e != cudaSuccess) return fail(RK_E_CUDA, "decode occupancy: %s", cudaGetErrorString(e));
         // Hkv chains of `members` CTAs (one per KV head)
         const int members = std::min(ctas, RK_PAGED_BALANCED_MAX_CTAS) / plan->Hkv;
-        // blocks of 8 tiles a row can have, and the most one CTA could get
-        const int64_t row_blocks = std::max<int64_t>(1, ((int64_t)plan->W * rk::PAGE + 1023) / 1024);
-        const int64_t per_cta = members > 0 ? ((int64_t)plan->B * row_blocks + members - 1) / members : 0;
-        if (members >= 2 && plan->B >= members && plan->B <= rk::DEC_BAL_MAX_ROWS &&
-            per_cta + 2 <= rk::DEC_BAL_MAX_SEGS) {
+        // the finest block (tiles, a power of two up to 8) for which the most
+        // blocks one CTA could get (every row as wide as the table) still fit its
+        // segment list; finer blocks balance the chains more evenly
+        int block_tiles = 0;
+        for (int bt = 1; members > 0 && bt <= rk::DEC_BAL_MAX_BLOCK_TILES && !block_tiles; bt *= 2) {
+            const int64_t row_blocks =
+                std::max<int64_t>(1, ((int64_t)plan->W * rk::PAGE + bt * rk::DEC_BN - 1) / (bt * rk::DEC_BN));
+            const int64_t per_cta = ((int64_t)plan->B * row_blocks + members - 1) / members;
+            if (per_cta + 2 <= rk::DEC_BAL_MAX_SEGS) block_tiles = bt;
+        }
+        if (members >= 2 && plan->B >= members && plan->B <= rk::DEC_BAL_MAX_ROWS && block_tiles > 0) {
             a.balanced = 1;
+            a.bal_block_tiles = block_tiles;
             a.bal_grid = members * plan->Hkv;
             a.bal_sync = static_cast<uint32_t*>(scratch);
             a.bal_state = reinterpret_cast<float*>(static_cast<char*>(scratch) + 4096);

@@ -61,7 +61,7 @@ struct DecodeArgs {
     uint32_t wait_limit_ns;       // pipeline wait limit (0: RK_WAIT_LIMIT_NS)
     int32_t timeout_drill;        // nonzero: the score MMA issuer first waits on a barrier nothing completes
     // Balanced schedule (balanced != 0; padded split-free decode only): each
-    // (row, KV head)'s tiles are cut in blocks of DEC_BAL_BLOCK_TILES, the blocks
+    // (row, KV head)'s tiles are cut in blocks of bal_block_tiles, the blocks
     // of all of them laid end to end in (row, KV head) order and dealt to the
     // CTAs in equal contiguous runs.  A row whose blocks cross from CTA c's run
     // into CTA c + 1's hands its running softmax state (m, l, O) over through
@@ -71,10 +71,11 @@ struct DecodeArgs {
     uint32_t* bal_sync;           // [0] launch epoch, [1] CTAs done, [2 + c] hand-off flag of slot c
     float* bal_state;             // [grid - 1][DEC_BAL_STATE_FLOATS]
     int32_t bal_grid;             // CTAs of a balanced launch (all resident at once)
+    int32_t bal_block_tiles;      // tiles per block of the balanced schedule (1 .. DEC_BAL_MAX_BLOCK_TILES)
     uint64_t rope_turns[ROPE_PAIRS];
 };
 constexpr int DEC_SPLIT_GRAIN = PAGE;  // split lengths are multiples of the page size
-constexpr int DEC_BAL_BLOCK_TILES = 8;       // tiles per block (a multiple of the RoPE anchor spacing)
+constexpr int DEC_BAL_MAX_BLOCK_TILES = 8;   // the largest block the host picks (tiles)
 constexpr int DEC_BAL_MAX_SEGS = 32;         // segments one CTA can hold
 constexpr int DEC_BAL_MAX_ROWS = 12288;      // rows whose block counts fit the set-up scratch
 // Hand-off state of one row: m per head [8], info [8] (ok, range_bad), l

@@ -274,8 +274,10 @@ int rk_paged_attn_decode_split_static(const rk_paged_plan_t *plan, int32_t split
  * one ascending-KV pass, "flashinfer_fa2 backend for Ada (SM89)", "Split-KV
  * is disabled" design note), on a schedule that keeps every SM busy to the
  * end.  One CTA per SM (a cooperative launch: all resident at once), the
- * CTAs in Hkv chains, one per KV head.  The tiles of every row are grouped in
- * blocks of 8 (1024 tokens), the rows' blocks laid end to end in row order and
+ * CTAs in Hkv chains, one per KV head.  The 128-token tiles of every row are
+ * grouped in blocks of 1, 2, 4 or 8 tiles (the coarsest that still gives every
+ * CTA of a chain work, no finer than the plan's B and W allow for a bounded
+ * segment list), the rows' blocks laid end to end in row order and
  * dealt to a chain's CTAs in equal contiguous runs (the same runs for every
  * head, so the CTAs serving a row's heads read its pages together); where a
  * row crosses from one CTA's run to the next, the first CTA hands its running

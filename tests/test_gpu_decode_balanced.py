@@ -1,8 +1,9 @@
 """GPU tests of the balanced split-free decode (rk_paged_attn_decode_balanced).
 
-The balanced schedule deals 8-tile blocks of every (row, KV head) to one CTA
-per SM and hands a row's running state from CTA to CTA where it crosses a
-boundary, so each row is still reduced tile after tile in ascending order by
+The balanced schedule deals blocks of 1-8 tiles of every (row, KV head) to one
+CTA per SM and hands a row's running state from CTA to CTA where it crosses a
+boundary (a segment that starts between RoPE anchor tiles replays the angle
+steps since the last anchor), so each row is still reduced tile after tile in ascending order by
 the operations of the one-CTA-per-(row, KV head) launch.  Every test here
 compares the two launches bitwise (the split-free decode's own parity with the
 oracle is tested elsewhere, and again here on ragged rows).  The launch epoch
@@ -123,6 +124,22 @@ def test_balanced_long_row_crosses_many_ctas(scratch):
     equal to the one-CTA launch and within the oracle tolerance."""
     kv = [20000] + [100 + 37 * i for i in range(18)]
     w = workloads.random_case(len(kv), 1, 32, 8, 128, kv, seed=331, mode="decode")
+    e0, _ = _epoch(scratch)
+    (o1, l1, s1), (o2, l2, s2) = _both(w, scratch)
+    assert _epoch(scratch)[0] == e0 + 1
+    assert s1 == s2 == 0
+    assert bitwise_equal(o1, o2) and bitwise_equal(l1, l2)
+    ro, rl = oracle_ref(w)
+    assert_parity(o2, l2, ro, rl)
+
+
+def test_balanced_fine_blocks_segments_between_anchors(scratch):
+    """B=20 x kv 4096: blocks of 8 tiles would leave 3 of each chain's 19 CTAs
+    without work, so the kernel cuts the rows in 2-tile blocks and most
+    segments start between RoPE anchor tiles (their first angles come from the
+    anchor before them and the replayed steps); bitwise equal to the one-CTA
+    launch and within the oracle tolerance."""
+    w = workloads.random_case(20, 1, 32, 8, 128, [4096] * 20, seed=337, mode="decode")
     e0, _ = _epoch(scratch)
     (o1, l1, s1), (o2, l2, s2) = _both(w, scratch)
     assert _epoch(scratch)[0] == e0 + 1
