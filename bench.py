@@ -308,7 +308,9 @@ def measure_prefill_long(args, dev, stream, world, tf_burst, peak_kind):
     from deterministic_paged_kv_gb300 import workloads
     obj = time_prefill(args, workloads.prefill_long(), dev, stream, world, tf_burst, peak_kind,
                        max(5, min(args.steps, 20)))
-    obj["roofline"]["traffic"] = None  # the committed DRAM figure is the chunk workload's
+    # this workload's own ncu capture (the prefill object's is the chunk's)
+    obj["roofline"]["traffic"] = traffic_for("prefill_kernel_long",
+                                             source_hash("prefill.cu", "rk_device.cuh", "rk_internal.h"))
     return obj
 
 
@@ -555,8 +557,9 @@ def run_ours(args):
         if rank == 0:
             print(json.dumps(bw))
         return 0
-    if args.prefill_only:
-        pf = measure_prefill(args, dev, stream, world, tf_burst, peak_kind)
+    if args.prefill_only or args.prefill_long_only:
+        pf = (measure_prefill_long if args.prefill_long_only else measure_prefill)(args, dev, stream, world,
+                                                                                 tf_burst, peak_kind)
         if rank == 0:
             print(json.dumps(pf))
         return 0
@@ -720,6 +723,8 @@ def main():
                     help="time only the prefill backward on the long full-causal workload")
     ap.add_argument("--prefill-only", action="store_true",
                     help="time only the prefill workload and print its object (profiling runs)")
+    ap.add_argument("--prefill-long-only", action="store_true",
+                    help="time only the long full-causal prefill and print its object (profiling runs)")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "ours":
         args.warmup = 3
