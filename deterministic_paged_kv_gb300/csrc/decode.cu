@@ -919,7 +919,9 @@ __device__ __noinline__ void bal_schedule(const DecodeArgs& a, uint8_t* sm, DecC
         const long long T = total;
         const long long L = members > 0 ? (T + members - 1) / members : 0;
         const long long lo = g < members ? (long long)g * L : T, hi = min(T, lo + L);
-        int sg[DEC_BAL_MAX_SEGS][4];
+        // the segments in row order, in shared memory (a local array would go
+        // through local memory on every access); the V stages are zeroed afterwards
+        int(*sg)[4] = reinterpret_cast<int(*)[4]>(sm + OFF_V + 1024);
         int n = 0;
         if (B != a.B && blockIdx.x == 0 && a.status) atomicOr(a.status, RK_STATUS_TIMEOUT);
         if (lo < hi) {
@@ -998,13 +1000,13 @@ __device__ __noinline__ void dec_setup(const DecodeArgs& a, uint8_t* sm, DecCtrl
     }
     const int n_pg = ctl->n_pg;
     int pre[PRE], pre_s[PRE];
+    int s = 0;  // the segment of entry j (entries ascend with e, so the scan resumes)
 #pragma unroll
     for (int e = 0; e < PRE; ++e) {
         const int j = tid + e * DEC_THREADS;
         pre[e] = 0;
         pre_s[e] = -1;
         if (j < n_pg) {
-            int s = 0;
             while (s + 1 < n_seg && ctl->seg[s + 1].pg_off <= j) ++s;
             const DecSeg& d = ctl->seg[s];
             pre_s[e] = s;
