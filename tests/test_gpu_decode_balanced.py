@@ -149,6 +149,23 @@ def test_balanced_fine_blocks_segments_between_anchors(scratch):
     assert_parity(o2, l2, ro, rl)
 
 
+def test_balanced_single_tile_blocks_odd_segment_starts(scratch):
+    """B=20 rows of 1000-1024 keys in a 64-page table: the host allows blocks of
+    one tile and no coarser block gives every chain member work, so segments
+    start on any tile, 1 to 7 tiles past a RoPE anchor (the replay of up to 7
+    tiles of angle steps); bitwise equal to the one-CTA launch and within the
+    oracle tolerance."""
+    kv = [1024 - 3 * i for i in range(20)]
+    w = workloads.random_case(len(kv), 1, 32, 8, 128, kv, seed=341, mode="decode", W=64)
+    e0, _ = _epoch(scratch)
+    (o1, l1, s1), (o2, l2, s2) = _both(w, scratch)
+    assert _epoch(scratch)[0] == e0 + 1
+    assert s1 == s2 == 0
+    assert bitwise_equal(o1, o2) and bitwise_equal(l1, l2)
+    ro, rl = oracle_ref(w)
+    assert_parity(o2, l2, ro, rl)
+
+
 def test_balanced_unsafe_rows_fail_like_the_one_cta_launch(scratch):
     """An out-of-range page id deep inside a long row (a segment other than the
     row's last one meets it) and a kv_len past the table: the same failed rows
