@@ -66,6 +66,7 @@
 // double-buffered by segment, and V pages a partial tile leaves unloaded are
 // zeroed when the stage last held another segment's rows.
 #include <atomic>
+#include <cstring>
 
 #include "rk_device.cuh"
 
@@ -673,16 +674,29 @@ __global__ void __launch_bounds__(DEC_THREADS, 1)
 // FP16 range, timeout) makes the row out = 0, lse = NaN; no visible key at
 // all gives out = 0, lse = -inf.
 __global__ void __launch_bounds__(HEAD_DIM) decode_merge_kernel(const __grid_constant__ DecodeArgs a) {
+    // Launched after the split grid with programmatic stream serialization: the
+    // CTAs may be resident early and wait here until that grid's partials are
+    // complete and visible.
+    griddep_wait();
     const size_t bh = blockIdx.x;  // b * Hq + h
     const int d = threadIdx.x;
-    const float* lp = a.lse_part + bh * a.n_splits;
-    const float* op = a.o_part + bh * a.n_splits * HEAD_DIM + d;
+    const int ns = a.n_splits;
+    const float* lp = a.lse_part + bh * ns;
+    const float* op = a.o_part + bh * ns * HEAD_DIM + d;
+    // The partials are read MERGE_CHUNK splits at a time (independent loads in
+    // flight), the arithmetic stays in split order.
+    constexpr int MERGE_CHUNK = 16;
     float M = -INFINITY;
     bool bad = false;
-    for (int s = 0; s < a.n_splits; ++s) {
-        const float v = lp[s];
-        bad |= v != v;
-        M = fmaxf(M, v);
+    for (int s0 = 0; s0 < ns; s0 += MERGE_CHUNK) {
+        float v[MERGE_CHUNK];
+#pragma unroll
+        for (int e = 0; e < MERGE_CHUNK; ++e) v[e] = s0 + e < ns ? lp[s0 + e] : -INFINITY;
+#pragma unroll
+        for (int e = 0; e < MERGE_CHUNK; ++e) {
+            bad |= v[e] != v[e];
+            M = fmaxf(M, v[e]);
+        }
     }
     __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(a.out) + bh * HEAD_DIM;
     if (bad || M == -INFINITY) {
@@ -691,10 +705,22 @@ __global__ void __launch_bounds__(HEAD_DIM) decode_merge_kernel(const __grid_con
         return;
     }
     float wsum = 0.0f, acc = 0.0f;
-    for (int s = 0; s < a.n_splits; ++s) {
-        const float w = ex2(lp[s] - M);  // 0 for an empty split
-        wsum += w;
-        acc = fmaf(w, op[(size_t)s * HEAD_DIM], acc);
+    for (int s0 = 0; s0 < ns; s0 += MERGE_CHUNK) {
+        float lv[MERGE_CHUNK], ov[MERGE_CHUNK];
+#pragma unroll
+        for (int e = 0; e < MERGE_CHUNK; ++e) {
+            const bool in = s0 + e < ns;
+            lv[e] = in ? lp[s0 + e] : 0.0f;
+            ov[e] = in ? op[(size_t)(s0 + e) * HEAD_DIM] : 0.0f;
+        }
+#pragma unroll
+        for (int e = 0; e < MERGE_CHUNK; ++e) {
+            if (s0 + e < ns) {
+                const float w = ex2(lv[e] - M);  // 0 for an empty split
+                wsum += w;
+                acc = fmaf(w, ov[e], acc);
+            }
+        }
     }
     out[d] = __float2bfloat16_rn(acc / wsum);
     if (d == 0) a.lse[bh] = (M + log2f(wsum)) * 0.693147180559945309f;
@@ -1824,7 +1850,21 @@ cudaError_t launch_decode(const CUtensorMap& vm, const DecodeArgs& a, cudaStream
     decode_kernel<<<(unsigned)grid, DEC_THREADS, DEC_SMEM_BYTES, stream>>>(vm, a);
     e = cudaGetLastError();
     if (e != cudaSuccess || a.split_tokens <= 0) return e;
-    decode_merge_kernel<<<(unsigned)((long long)a.B * a.Hq), HEAD_DIM, 0, stream>>>(a);
+    // the merge may start while the split grid drains (it waits on the grid
+    // dependency before it reads a partial)
+    cudaLaunchConfig_t cfg;
+    std::memset(&cfg, 0, sizeof cfg);
+    cfg.gridDim = dim3((unsigned)((long long)a.B * a.Hq));
+    cfg.blockDim = dim3(HEAD_DIM);
+    cfg.stream = stream;
+    cudaLaunchAttribute attr;
+    std::memset(&attr, 0, sizeof attr);
+    attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr.val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = &attr;
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelEx(&cfg, decode_merge_kernel, a);
+    if (e != cudaSuccess) return e;
     return cudaGetLastError();
 }
 
