@@ -19,8 +19,10 @@ own copy of the workload on its own GPU, there is no collective on the data
 path; the barrier and the max-over-ranks of the timed region are the only
 communication.  value = all ranks' bytes / max rank time ("scaling": "weak").
 
---impl reference times the float64 CPU oracle on the host cores on a bounded
-sample of the same workload (the slow baseline arm).
+--impl reference times the float64 CPU oracle on the host cores on the same
+workload, every step the whole decode-throughput batch (~0.75 s of 16 host
+cores a step), with the same config object as this arm (the slow baseline
+arm).
 """
 from __future__ import annotations
 
@@ -51,6 +53,13 @@ def peaks():
         return (float(d["hbm_gbs"]), float(d["bf16_tflops"]),
                 float(d.get("bf16_tflops_sustained", d["bf16_tflops"])), "measured")
     return FALLBACK_HBM_GBS, FALLBACK_BF16_TFLOPS, FALLBACK_BF16_TFLOPS_SUSTAINED, "fallback"
+
+
+def decode_step_config(w, step_bytes, world):
+    """The config object of the decode step (both arms)."""
+    return {"workload": w.name + " page=16 (16384 shuffled pages, fused RoPE, FP32 LSE)",
+            "l2": "inputs larger than L2 (%.3f GB per step)" % (step_bytes / 1e9),
+            "parallelism": "replicas x%d" % world if world > 1 else "single GPU"}
 
 
 def decode_alg_bytes(w):
@@ -200,36 +209,31 @@ def run_reference(args):
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
         return 0
-    import numpy as np
-
     import oracle
     from deterministic_paged_kv_gb300 import workloads
     oracle.build()
     w = workloads.decode_throughput()
-    B = w.B
-    times, nbytes = [], []
+    step_bytes = decode_alg_bytes(w)
+    times = []
     for step in range(args.warmup + args.steps):
-        row = step % B
-        mask = np.zeros((B, 1), np.uint8)
-        mask[row] = 1
+        # every step the whole batch: all 64 rows, all 32 query heads
         t0 = time.perf_counter()
         oracle.attention(w.q, w.k_cache, w.v_cache, w.block_table, w.kv_lens, w.position_ids,
-                         w.rope_theta, w.rope_scale, row_mask=mask)
+                         w.rope_theta, w.rope_scale)
         dt = time.perf_counter() - t0
         if step >= args.warmup:
             times.append(dt)
-            nbytes.append(int(w.kv_lens[row]) * w.Hkv * w.D * 4 + w.Hq * w.D * 4 + w.Hq * 4)
     total = sum(times)
-    value = sum(nbytes) / total / 1e9
+    value = step_bytes * len(times) / total / 1e9
     cores = oracle.max_threads()
     line = {
         "impl": "reference", "metric": "paged decode HBM GB/s", "value": value, "unit": "GB/s",
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": 1e3 * total / len(times), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": w.name + " page=16", "sample_per_step": "one row (32 query heads)"},
+        "config": decode_step_config(w, step_bytes, 1),
         "cpu_baseline": {"value": value, "unit": "GB/s", "cores": cores, "kind": "oracle",
-                         "sample": "one row of 64 per step, %d steps" % len(times)},
+                         "sample": "the whole batch (64 rows) every step, %d steps" % len(times)},
         "e2e": {"value": value, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line))
@@ -675,9 +679,7 @@ def run_ours(args):
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": region_ms / args.steps,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
             "data": "synthetic",
-            "config": {"workload": w.name + " page=16 (16384 shuffled pages, fused RoPE, FP32 LSE)",
-                       "l2": "inputs larger than L2 (%.3f GB per step)" % (step_bytes / 1e9),
-                       "parallelism": "replicas x%d" % world if world > 1 else "single GPU"},
+            "config": decode_step_config(w, step_bytes, world),
             "roofline": roof,
             "cpu_baseline": cpu,
             "e2e": {"value": world * step_bytes / t_full / 1e9, "unit": "GB/s",
