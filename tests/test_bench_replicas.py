@@ -55,3 +55,25 @@ def test_single_rank_helpers():
     import bench
     assert bench.max_over_ranks(3.5, 1) == 3.5
     assert bench.whole_job_rate(10, 2, 1, 1000.0) == pytest.approx(20.0)
+
+def test_reference_arm_rank0_line(monkeypatch, capsys):
+    """The oracle arm on the host cores: one JSON line with the contract's keys,
+    the whole decode batch per step and the GPU arm's config object."""
+    sys.path.insert(0, ROOT)
+    import json
+    import bench
+    from deterministic_paged_kv_gb300 import workloads
+    monkeypatch.setenv("RANK", "0")
+
+    class A:
+        gpus, steps, warmup = 1, 1, 0
+    assert bench.run_reference(A()) == 0
+    line = json.loads(capsys.readouterr().out.strip().splitlines()[-1])
+    w = workloads.decode_throughput()
+    step_bytes = bench.decode_alg_bytes(w)
+    assert line["impl"] == "reference" and line["metric"] == "paged decode HBM GB/s"
+    assert line["unit"] == "GB/s" and line["higher_is_better"] is True and line["steps"] == 1
+    assert line["config"] == bench.decode_step_config(w, step_bytes, 1)
+    assert line["value"] > 0 and line["value"] == pytest.approx(step_bytes / (line["ms_per_step"] * 1e-3) / 1e9)
+    assert line["cpu_baseline"]["kind"] == "oracle" and line["cpu_baseline"]["value"] == line["value"]
+    assert line["e2e"] == {"value": line["value"], "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}
